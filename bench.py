@@ -1,0 +1,454 @@
+"""Throughput of the paged KV-cache hot path on GB300.
+
+One step = one pass of the whole path over one synthetic batch already resident
+in HBM: copy-on-write block copies (when the workload forks), the K/V append
+scatter, paged-attention decode (partitions + log-sum-exp reduce) and, for the
+mixed workload, the chunked-prefill attention.  The default workload is the
+Llama-3-8B-shaped decode layer (64 sequences, 32 q / 8 kv heads, d 128,
+context U[512, 4096], bf16).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run, one rank per GPU: each rank serves its
+own independent batch of the same shape (sequences shard with no exchange),
+the timed region is bracketed by barriers and the slowest rank's time is used.
+Rank 0 prints one JSON line.  ``--impl reference`` times the fp64 host oracle
+on the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_297_gb300 import accounting  # noqa: E402
+from paged_kv_cache_297_gb300 import workloads as W  # noqa: E402
+
+METRIC = ("paged decode KV-read GB/s & fraction of HBM peak; sequence-steps/sec at 1 GB300")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device: str = "cpu") -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# measurement helpers
+# ----------------------------------------------------------------------------
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4], parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        mhz = sorted(r[0] for r in rows)
+        loaded = [r for r in rows if r[0] >= 0.5 * max(mhz)] or rows
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in loaded:
+            for name, v in zip(names, r[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        lm = sorted(r[0] for r in loaded)
+        return {"sm_mhz": lm[len(lm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+class Step:
+    """Device-resident inputs and the calls of one step of the hot path."""
+
+    def __init__(self, batch: W.Batch, dev: str):
+        import paged_kv_cache_297_gb300 as pkv
+        self.pkv = pkv
+        self.b = batch
+        self.dev = dev
+        t = {}
+        for name in ("k_cache", "v_cache", "k_new", "v_new", "slot_mapping", "q", "block_tables",
+                     "context_lens", "copy_pairs", "prefill_q", "prefill_cu_q_lens",
+                     "prefill_block_tables", "prefill_context_lens"):
+            x = getattr(batch, name)
+            t[name] = None if x is None else x.to(dev)
+        self.t = t
+        S, Hq, d = batch.q.shape
+        self.out = torch.empty((S, Hq, d), dtype=batch.dtype, device=dev)
+        self.max_ctx = max(1, batch.max_context_len)
+        ws = pkv.decode_workspace_bytes(S, Hq, d, self.max_ctx)
+        self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        self.pout = None
+        if batch.prefill_q is not None:
+            self.pout = torch.empty(batch.prefill_q.shape, dtype=batch.dtype, device=dev)
+            cu = batch.prefill_cu_q_lens
+            self.max_q = int((cu[1:] - cu[:-1]).max())
+            self.max_pctx = int(batch.prefill_context_lens.max())
+        self.has_copy = batch.copy_pairs is not None and batch.copy_pairs.numel() > 0
+
+    def launches_per_step(self) -> int:
+        n = 2  # append + decode partitions
+        if self.max_ctx > W_DEFAULT_PARTITION:
+            n += 1  # log-sum-exp reduce
+        if self.has_copy:
+            n += 1
+        if self.pout is not None:
+            n += 1
+        return n
+
+    def calls(self):
+        """(name, thunk) for every call of one step, in order."""
+        t, b, pkv = self.t, self.b, self.pkv
+        out = []
+        if self.has_copy:
+            out.append(("copy_blocks", lambda: pkv.copy_blocks(t["copy_pairs"], t["k_cache"],
+                                                               t["v_cache"])))
+        out.append(("kv_append", lambda: pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"],
+                                                       t["k_cache"], t["v_cache"])))
+        out.append(("decode", lambda: pkv.paged_attention_decode(
+            t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"], b.scale,
+            self.out, max_context_len=self.max_ctx, workspace=self.ws)))
+        if self.pout is not None:
+            out.append(("prefill_chunk", lambda: pkv.paged_attention_prefill_chunk(
+                t["prefill_q"], t["prefill_cu_q_lens"], t["k_cache"], t["v_cache"],
+                t["prefill_block_tables"], t["prefill_context_lens"], b.scale, self.pout,
+                max_q_len=self.max_q, max_context_len=self.max_pctx)))
+        return out
+
+
+W_DEFAULT_PARTITION = 512
+
+
+def time_device(step: Step, steps: int, warmup: int, world: int):
+    calls = step.calls()
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+          for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(calls):
+            fn()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    per_call = {}
+    for j, (name, _) in enumerate(calls):
+        per_call[name] = sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
+    total_ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps))
+    # device time from the first step's start to the last step's end
+    span_ms = ev[0][0].elapsed_time(ev[-1][-1])
+    return span_ms, total_ms, per_call, wall
+
+
+def time_e2e(step: Step, steps: int, warmup: int, world: int):
+    """Same step through the public API with host buffers: each step copies its
+    inputs from pinned host memory and reads the outputs back."""
+    b = step.b
+    names = ["q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens"]
+    if step.has_copy:
+        names.append("copy_pairs")
+    if step.pout is not None:
+        names += ["prefill_q", "prefill_cu_q_lens", "prefill_block_tables", "prefill_context_lens"]
+    host = {n: getattr(b, n).pin_memory() for n in names}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    pout_h = None if step.pout is None else torch.empty(step.pout.shape,
+                                                        dtype=step.pout.dtype).pin_memory()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = out_h.numel() * out_h.element_size() + (
+        0 if pout_h is None else pout_h.numel() * pout_h.element_size())
+    calls = step.calls()
+
+    def one():
+        for n in names:
+            step.t[n].copy_(host[n], non_blocking=True)
+        for _, fn in calls:
+            fn()
+        out_h.copy_(step.out, non_blocking=True)
+        if pout_h is not None:
+            pout_h.copy_(step.pout, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1), h2d, d2h
+
+
+def cpu_baseline(batch: W.Batch, budget_s: float = 12.0):
+    """The fp64 oracle as it stands, on this host's cores, on whole steps of
+    the same batch repeated for about `budget_s` seconds."""
+    import oracle
+    kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
+    reps, seqs, rows = 0, 0, 0
+    t0 = time.perf_counter()
+    while True:
+        if batch.copy_pairs is not None and batch.copy_pairs.numel():
+            oracle.copy_blocks(kc, vc, batch.copy_pairs)
+        oracle.kv_append(batch.k_new, batch.v_new, batch.slot_mapping, kc, vc)
+        oracle.decode(batch.q, kc, vc, batch.block_tables, batch.context_lens, batch.scale)
+        if batch.prefill_q is not None:
+            oracle.prefill_chunk(batch.prefill_q, batch.prefill_cu_q_lens, kc, vc,
+                                 batch.prefill_block_tables, batch.prefill_context_lens,
+                                 batch.scale)
+        reps += 1
+        seqs += batch.num_seqs + (0 if batch.prefill_context_lens is None
+                                  else int(batch.prefill_context_lens.numel()))
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": seqs / dt, "unit": "seq-steps/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{reps} whole steps of the {batch.spec.name} batch "
+                      f"({batch.num_seqs} decode seqs), fp64, {dt:.1f} s"}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    batch = W.make_batch(args.workload, poison=False)
+    step = Step(batch, dev)
+    peaks = read_peaks()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    span_ms, total_ms, per_call, wall = time_device(step, args.steps, args.warmup, world)
+    clk = clocks.stop()
+    span_ms = max_over_ranks(span_ms, world, dev)
+    e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, world)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+
+    seqs_per_step = batch.num_seqs + (0 if batch.prefill_context_lens is None
+                                      else int(batch.prefill_context_lens.numel()))
+    ms_per_step = span_ms / args.steps
+    value = world * seqs_per_step * args.steps / (span_ms / 1e3)
+    S, Hq, d = batch.q.shape
+    elem = batch.q.element_size()
+    # context lengths the decode call sees (after this step's append)
+    db = accounting.decode_bytes(batch.context_lens, Hq, batch.spec.num_kv_heads, d, elem, elem)
+    dec_ms = per_call["decode"]
+    achieved = db["total"] / (dec_ms / 1e3) / 1e9
+    roofline = {"kernel": "paged_attention_decode (partition kernel + log-sum-exp reduce)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": None, "algorithmic_bytes": db["total"],
+                "kv_bytes": db["kv"], "decode_us": round(dec_ms * 1e3, 2)}
+    extra = {}
+    if step.pout is not None:
+        fl = accounting.prefill_flops(batch.prefill_cu_q_lens, batch.prefill_context_lens, Hq, d)
+        tf = fl / (per_call["prefill_chunk"] / 1e3) / 1e12
+        extra["prefill_roofline"] = {"bound": "tensor", "achieved": round(tf, 1),
+                                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                     "frac": round(tf / peaks["bf16_tflops"], 4), "flops": fl}
+    if step.has_copy:
+        cb = accounting.copy_blocks_bytes(int(batch.copy_pairs.shape[0]), batch.spec.num_kv_heads,
+                                          d, elem)
+        extra["copy_blocks"] = {"pairs": int(batch.copy_pairs.shape[0]), "bytes": cb,
+                                "us": round(per_call["copy_blocks"] * 1e3, 2)}
+    ab = accounting.append_bytes(int(batch.slot_mapping.numel()), batch.spec.num_kv_heads, d, elem)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "seq-steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if batch.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "seqs": S, "q_heads": Hq,
+                   "kv_heads": batch.spec.num_kv_heads, "head_dim": d, "block_size": 16,
+                   "max_context_len": batch.max_context_len,
+                   "mean_context_len": round(float(batch.context_lens.float().mean()), 1),
+                   "kv_bytes_per_step": db["kv"],
+                   "l2": "inputs larger than L2 (KV per step %.0f MB > 129 MB L2); no flush"
+                         % (db["kv"] / 1e6) if db["kv"] > 129e6 else
+                         "working set fits L2; numbers are L2-assisted",
+                   "parallelism": f"replicas x{world} (sequences shard, no collective)"},
+        "kv_gbs": round(db["kv"] / (dec_ms / 1e3) / 1e9, 1),
+        "calls_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
+        "append_gbs": round(ab / (per_call["kv_append"] / 1e3) / 1e9, 1),
+        "roofline": roofline,
+        "e2e": {"value": round(world * seqs_per_step * args.steps / (e2e_ms / 1e3), 1),
+                "unit": "seq-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk,
+        "wall_s": round(wall, 4),
+    }
+    line.update(extra)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(batch)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the fp64 oracle on host cores
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    batch = W.make_batch(args.workload, poison=False)
+    S = batch.num_seqs
+    # size each step's sample so that warmup + steps stay within ~2 minutes
+    kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
+    t0 = time.perf_counter()
+    oracle.decode(batch.q[:1], kc, vc, batch.block_tables[:1], batch.context_lens[:1], batch.scale)
+    per_seq = max(1e-4, time.perf_counter() - t0)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(S, int(budget / per_seq)))
+    sub = slice(0, n)
+
+    def one():
+        oracle.kv_append(batch.k_new[sub], batch.v_new[sub], batch.slot_mapping[sub], kc, vc)
+        oracle.decode(batch.q[sub], kc, vc, batch.block_tables[sub], batch.context_lens[sub],
+                      batch.scale)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "seq-steps/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "seqs": S, "sample_seqs": n},
+            "cpu_baseline": {"value": round(value, 3), "unit": "seq-steps/s",
+                             "cores": oracle.threads(), "kind": "oracle",
+                             "sample": f"first {n} of {S} sequences per step (append + decode), fp64"},
+            "e2e": {"value": round(value, 3), "unit": "seq-steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.SPECS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

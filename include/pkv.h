@@ -1,0 +1,189 @@
+/*
+ * pkv: paged KV-cache attention for GB300 (sm_103a), C ABI.
+ *
+ * The operations follow the description of the paged KV cache on these pages:
+ *   - "Serving deep dive: KV cache, batching, and inference engines"
+ *     (models.specul.com), sections on PagedAttention and chunked prefill;
+ *   - the ainews.alishangtian.com article on vLLM, "PagedAttention" (16-token
+ *     blocks chained by a block table, shared prefix blocks, copy-on-write);
+ *   - chengxuchu.com "PyTorch #47: KV Cache, batching, sampling", sections 2.1
+ *     (attention formula), 2.2 (append new K/V at a given position, then the
+ *     new query reads all cached K/V), 2.3 (GQA) and 5.2 (the kernel reaches
+ *     K/V through the block table);
+ *   - caffein.top "modern LLM inference runtime", "Chunked Prefill" and
+ *     "Paging".
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is DEVICE memory owned by the caller, except the
+ *     out-parameters of pkv_*_workspace_bytes and pkv_get_status, which are
+ *     host pointers.  The library allocates no device memory and keeps no
+ *     pointer after a call returns.
+ *   - Tensors are dense row-major.  Each KV cache is
+ *       [num_blocks][num_kv_heads][block_size][head_dim]
+ *     (K and V are separate tensors with the same shape).  Logical token t of
+ *     sequence s is row (t % block_size) of physical block
+ *     block_tables[s * max_blocks_per_seq + t / block_size].  A slot is
+ *     block * block_size + row.
+ *   - block_size must be 16; head_dim must be 64 or 128.  dtype is the element
+ *     type of q, k, v and both caches (one type for all of them); out_dtype
+ *     the element type of out.  Cache, q, k, v and out pointers must be
+ *     16-byte aligned.
+ *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns without waiting.
+ *   - Return value: PKV_OK, or PKV_ERR_INVALID when an argument is rejected on
+ *     the host (nothing is launched), or PKV_ERR_CUDA when a launch fails.
+ *     pkv_last_error_string() describes the last failure on this host thread.
+ *   - Indices that are only known on the device (slots, block ids, context
+ *     lengths) are checked by the kernels.  A bad one is skipped and recorded
+ *     in a per-device status word; no kernel traps.  pkv_get_status() reads
+ *     and clears that word.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define PKV_OK 0
+#define PKV_ERR_INVALID 1
+#define PKV_ERR_CUDA 2
+#define PKV_ERR_OOB 3
+
+/* element types */
+#define PKV_F32 0
+#define PKV_BF16 1
+
+/* status-word bits (pkv_get_status) */
+#define PKV_STATUS_BAD_SLOT 1u       /* kv_append: slot >= num_blocks * block_size */
+#define PKV_STATUS_BAD_BLOCK 2u      /* block id < 0 or >= num_blocks (gather or copy) */
+#define PKV_STATUS_BAD_LENGTH 4u     /* context_len < 0, > max_blocks_per_seq * block_size,
+                                        or > max_context_len */
+#define PKV_STATUS_BAD_QLEN 8u       /* prefill: chunk longer than its context, or than max_q_len */
+
+#define PKV_BLOCK_SIZE 16
+#define PKV_DEFAULT_PARTITION 512    /* decode split-K partition, tokens */
+
+/*
+ * KV append (scatter).  chengxuchu #47 section 2.2: production code
+ * preallocates blocks and writes each new token's K/V at its position.
+ *   k, v          [num_tokens][num_kv_heads][head_dim], dtype
+ *   slot_mapping  [num_tokens] int64; token i goes to slot slot_mapping[i].
+ *                 A negative slot skips the token (padding).  A slot at or
+ *                 past num_blocks * block_size is skipped and sets
+ *                 PKV_STATUS_BAD_SLOT.  Two tokens with the same slot are a
+ *                 caller error (which one lands is unspecified).
+ *   k_cache, v_cache  updated in place (bit copy, no conversion).
+ */
+int pkv_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int num_tokens,
+                  void *k_cache, void *v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                  int block_size, int dtype, void *stream);
+
+/*
+ * Copy-on-write block copy.  ainews article, "PagedAttention": when requests
+ * sharing prefix blocks diverge, only the forked block is copied.
+ *   src_dst_pairs  [num_pairs][2] int64 (src, dst): block dst of both caches
+ *                  becomes a copy of block src (all kv heads, all 16 rows).
+ *                  Destinations must be distinct and must not be sources of
+ *                  the same call (caller contract).  An id outside
+ *                  [0, num_blocks) skips the pair and sets PKV_STATUS_BAD_BLOCK.
+ */
+int pkv_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, int num_pairs,
+                    int num_blocks, int num_kv_heads, int head_dim, int block_size, int dtype,
+                    void *stream);
+
+/*
+ * Workspace (device bytes) that pkv_paged_attention_decode needs for its
+ * split-K partials with these sizes.  partition_size 0 means the default.
+ * *bytes is a host pointer.  Returns PKV_ERR_INVALID for bad sizes.
+ */
+int pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
+                               int partition_size, size_t *bytes);
+
+/*
+ * Paged-attention decode.  One query token per sequence and head attends to
+ * every cached token of its sequence:
+ *   out[s,h,:] = softmax_t(scale * q[s,h,:] . K_t) V_t,  t = 0 .. L_s - 1,
+ * chengxuchu #47 sections 2.1-2.2, with K_t and V_t fetched through the block
+ * table (section 5.2) and kv head h / (num_q_heads / num_kv_heads) (GQA,
+ * section 2.3).  The caller appends the new token first, so context_lens
+ * include it.  A sequence with L_s = 0 gets a zero row.
+ *   q             [num_seqs][num_q_heads][head_dim], dtype
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32; entries at or past
+ *                 ceil(L_s / 16) are never read
+ *   context_lens  [num_seqs] int32
+ *   max_context_len  host-side upper bound on every L_s, sizes the grid; a
+ *                 sequence longer than it sets PKV_STATUS_BAD_LENGTH and its
+ *                 output is undefined
+ *   partition_size   tokens per split-K partition (multiple of 16), 0 for
+ *                 the default 512.  Sequences longer than one partition are
+ *                 processed as independent partitions whose results are merged
+ *                 by a log-sum-exp reduction (a second launch).
+ *   out           [num_seqs][num_q_heads][head_dim], out_dtype
+ *   workspace     device scratch of at least pkv_decode_workspace_bytes(...)
+ *                 bytes (may be NULL when that is 0); contents need no
+ *                 initialisation and are clobbered.
+ */
+int pkv_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               int max_context_len, int partition_size, float scale, void *out,
+                               int dtype, int out_dtype, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/*
+ * Workspace (device bytes) that pkv_paged_attention_prefill_chunk needs.
+ */
+int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                                int head_dim, int max_q_len, int max_context_len, size_t *bytes);
+
+/*
+ * Chunked-prefill attention.  caffein.top "Chunked Prefill" and the
+ * "Serving deep dive" page: a long prompt is cut into chunks that run in the
+ * same steps as decode.  Sequence s contributes the n_s = cu_q_lens[s+1] -
+ * cu_q_lens[s] query rows cu_q_lens[s] .. cu_q_lens[s+1]-1; its cache already
+ * holds the chunk (appended by the caller), so its L_s = context_lens[s]
+ * tokens end with the chunk and query j sits at position L_s - n_s + j.  It
+ * attends causally to tokens 0 .. L_s - n_s + j.
+ *   q          [total_q][num_q_heads][head_dim], dtype
+ *   cu_q_lens  [num_seqs + 1] int32, non-decreasing, cu_q_lens[0] = 0,
+ *              cu_q_lens[num_seqs] = total_q
+ *   max_q_len  host-side bound on every n_s (sizes the grid)
+ *   max_context_len  host-side bound on every L_s
+ *   out        [total_q][num_q_heads][head_dim], out_dtype
+ * n_s > L_s or n_s > max_q_len sets PKV_STATUS_BAD_QLEN and skips the sequence.
+ */
+int pkv_paged_attention_prefill_chunk(const void *q, const int32_t *cu_q_lens,
+                                      const void *k_cache, const void *v_cache,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *context_lens, int num_seqs, int total_q,
+                                      int max_q_len, int max_context_len, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int num_blocks, float scale, void *out, int dtype,
+                                      int out_dtype, void *workspace, size_t workspace_bytes,
+                                      void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the status word of the current
+ * device.  *flags (host pointer, may be NULL) receives the PKV_STATUS_* bits.
+ * Returns PKV_OK when no bit was set, PKV_ERR_OOB when one was, PKV_ERR_CUDA
+ * on a CUDA error.  The word is shared by every stream of the device.
+ */
+int pkv_get_status(void *stream, unsigned int *flags);
+
+/* Description of the last failure on the calling host thread ("" if none). */
+const char *pkv_last_error_string(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,1 +1,238 @@
-"""GB300-native paged KV-cache attention (placeholder, binding added next)."""
+"""GB300-native paged KV-cache attention.
+
+Thin ctypes binding over ``libpkv.so`` (the C ABI of ``include/pkv.h``).  The
+functions here only check and marshal torch tensors (device memory, the current
+stream); every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or no GPU is present the calls
+raise.
+
+Calls (names follow the C ABI without the ``pkv_`` prefix):
+  kv_append(k, v, slot_mapping, k_cache, v_cache)
+  copy_blocks(src_dst_pairs, k_cache, v_cache)
+  paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out)
+  paged_attention_prefill_chunk(q, cu_q_lens, k_cache, v_cache, block_tables,
+                                context_lens, scale, out)
+  get_status()
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "BLOCK_SIZE", "DEFAULT_PARTITION", "PkvError", "load", "library_path", "kv_append",
+    "copy_blocks", "decode_workspace_bytes", "paged_attention_decode",
+    "prefill_workspace_bytes", "paged_attention_prefill_chunk", "get_status", "STATUS_BITS",
+    "EXPORTED",
+]
+
+BLOCK_SIZE = 16
+DEFAULT_PARTITION = 512
+OK, ERR_INVALID, ERR_CUDA, ERR_OOB = 0, 1, 2, 3
+F32, BF16 = 0, 1
+STATUS_BITS = {"bad_slot": 1, "bad_block": 2, "bad_length": 4, "bad_qlen": 8}
+
+# every entry point declared in include/pkv.h
+EXPORTED = (
+    "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes",
+    "pkv_paged_attention_decode", "pkv_prefill_workspace_bytes",
+    "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_last_error_string",
+    "pkv_version",
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpkv.so")
+_lib = None
+
+
+class PkvError(RuntimeError):
+    """A call of the C ABI returned an error code."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"pkv error {code}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load ``libpkv.so`` (built by ``paged_kv_cache_297_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                           "`python -m paged_kv_cache_297_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.pkv_kv_append.argtypes = [P, P, P, I, P, P, I, I, I, I, I, P]
+    lib.pkv_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I, P]
+    lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.pkv_paged_attention_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I,
+                                               I, P, SZ, P]
+    lib.pkv_prefill_workspace_bytes.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.pkv_paged_attention_prefill_chunk.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, I,
+                                                      I, F, P, I, I, P, SZ, P]
+    lib.pkv_get_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+    lib.pkv_last_error_string.argtypes = []
+    lib.pkv_version.argtypes = []
+    for name in EXPORTED:
+        getattr(lib, name).restype = I
+    lib.pkv_last_error_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(rc: int) -> None:
+    if rc != OK:
+        msg = load().pkv_last_error_string()
+        raise PkvError(rc, msg.decode() if msg else "")
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None) -> int:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _cache_dims(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must both be [num_blocks, num_kv_heads, 16, head_dim]")
+    NB, H, bs, d = k_cache.shape
+    return int(NB), int(H), int(bs), int(d)
+
+
+def kv_append(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Write token i's K/V rows (``k``/``v`` ``[T, Hkv, d]``) at slot ``slot_mapping[i]``."""
+    NB, H, bs, d = _cache_dims(k_cache, v_cache)
+    if k.shape != v.shape or k.dim() != 3 or k.shape[1:] != (H, d) or k.dtype != k_cache.dtype:
+        raise ValueError("k/v must be [T, num_kv_heads, head_dim] in the cache dtype")
+    if slot_mapping.shape != (k.shape[0],):
+        raise ValueError("slot_mapping must be [T]")
+    _check(load().pkv_kv_append(
+        _dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping", torch.int64),
+        int(k.shape[0]), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), NB, H, d, bs,
+        _dt(k_cache), _stream(stream)))
+
+
+def copy_blocks(src_dst_pairs, k_cache, v_cache, stream=None) -> None:
+    """Copy-on-write: block dst of both caches becomes a copy of block src."""
+    NB, H, bs, d = _cache_dims(k_cache, v_cache)
+    if src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be [n, 2]")
+    _check(load().pkv_copy_blocks(
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(src_dst_pairs, "src_dst_pairs", torch.int64), int(src_dst_pairs.shape[0]), NB, H, d,
+        bs, _dt(k_cache), _stream(stream)))
+
+
+def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
+                           partition_size: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().pkv_decode_workspace_bytes(int(num_seqs), int(num_q_heads), int(head_dim),
+                                             int(max_context_len), int(partition_size),
+                                             ctypes.byref(out)))
+    return int(out.value)
+
+
+def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                           max_context_len: Optional[int] = None, partition_size: int = 0,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[s, h] = softmax(scale * q[s, h] . K^T) V over sequence s's cached tokens."""
+    NB, Hkv, bs, d = _cache_dims(k_cache, v_cache)
+    S, Hq, dq = q.shape
+    if dq != d or q.dtype != k_cache.dtype:
+        raise ValueError("q must be [S, Hq, head_dim] in the cache dtype")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks] and context_lens [S]")
+    mb = int(block_tables.shape[1])
+    if max_context_len is None:
+        max_context_len = mb * bs
+    need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pkv_paged_attention_decode(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), mb,
+        _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, d, bs, NB,
+        int(max_context_len), int(partition_size), float(scale), _dev(out, "out"), _dt(q),
+        _dt(out), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def prefill_workspace_bytes(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, max_q_len,
+                            max_context_len) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().pkv_prefill_workspace_bytes(int(num_seqs), int(total_q), int(num_q_heads),
+                                              int(num_kv_heads), int(head_dim), int(max_q_len),
+                                              int(max_context_len), ctypes.byref(out)))
+    return int(out.value)
+
+
+def paged_attention_prefill_chunk(q, cu_q_lens, k_cache, v_cache, block_tables, context_lens,
+                                  scale, out, max_q_len: Optional[int] = None,
+                                  max_context_len: Optional[int] = None,
+                                  workspace: Optional[torch.Tensor] = None,
+                                  stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's prompt chunk over its whole cache."""
+    NB, Hkv, bs, d = _cache_dims(k_cache, v_cache)
+    total_q, Hq, dq = q.shape
+    S = int(context_lens.shape[0])
+    if dq != d or q.dtype != k_cache.dtype or out.shape != q.shape:
+        raise ValueError("q/out must be [total_q, Hq, head_dim] in the cache dtype")
+    if cu_q_lens.shape != (S + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("cu_q_lens must be [S+1] and block_tables [S, max_blocks]")
+    mb = int(block_tables.shape[1])
+    if max_q_len is None:
+        max_q_len = total_q
+    if max_context_len is None:
+        max_context_len = mb * bs
+    need = prefill_workspace_bytes(S, total_q, Hq, Hkv, d, max_q_len, max_context_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pkv_paged_attention_prefill_chunk(
+        _dev(q, "q"), _dev(cu_q_lens, "cu_q_lens", torch.int32), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables", torch.int32), mb,
+        _dev(context_lens, "context_lens", torch.int32), S, int(total_q), int(max_q_len),
+        int(max_context_len), Hq, Hkv, d, bs, NB, float(scale), _dev(out, "out"), _dt(q),
+        _dt(out), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def get_status(stream=None) -> int:
+    """Synchronise the stream, read and clear this device's status word."""
+    flags = ctypes.c_uint(0)
+    rc = load().pkv_get_status(_stream(stream), ctypes.byref(flags))
+    if rc == ERR_CUDA:
+        _check(rc)
+    return int(flags.value)

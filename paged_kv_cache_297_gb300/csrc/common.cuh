@@ -1,0 +1,109 @@
+// Shared device helpers for the pkv kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kBlock = 16;  // tokens per cache block
+
+// ---------------------------------------------------------------- host side
+
+// Device address of this device's status word (nullptr if it cannot be had).
+unsigned *status_ptr();
+// Record a message for pkv_last_error_string() and return `code`.
+int fail(int code, const char *fmt, ...);
+// Turn a pending launch error into PKV_ERR_CUDA.
+int check_launch(const char *what);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- device side
+
+__device__ __forceinline__ void flag(unsigned *status, unsigned bits) {
+    if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared copy; src_bytes = 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                        const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                          const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+
+// D += A(16x16, row) * B(16x8, col); bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Split x into hi + lo with both halves bf16 (hi = RNE(x), lo = RNE(x - hi)).
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    lo = x - hi;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+
+// Byte offset of 16-byte chunk `c` of row `r` in a tile whose rows are
+// `row_bytes` long, XOR-swizzled so that 8 consecutive rows at the same chunk
+// land in 8 different bank groups (conflict-free ldmatrix).
+__device__ __forceinline__ int swz(int r, int c, int row_bytes) {
+    return r * row_bytes + ((c ^ (r & 7)) << 4);
+}
+
+template <typename T>
+__device__ __forceinline__ void store2(T *p, float a, float b);
+template <>
+__device__ __forceinline__ void store2<float>(float *p, float a, float b) {
+    *reinterpret_cast<float2 *>(p) = make_float2(a, b);
+}
+template <>
+__device__ __forceinline__ void store2<__nv_bfloat16>(__nv_bfloat16 *p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+}
+template <typename T>
+__device__ __forceinline__ void store1(T *p, float a);
+template <>
+__device__ __forceinline__ void store1<float>(float *p, float a) { *p = a; }
+template <>
+__device__ __forceinline__ void store1<__nv_bfloat16>(__nv_bfloat16 *p, float a) {
+    *p = __float2bfloat16_rn(a);
+}
+
+}  // namespace pkv

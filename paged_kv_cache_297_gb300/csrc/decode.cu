@@ -1,0 +1,593 @@
+// Paged-attention decode with split-K partitions and a log-sum-exp reduce.
+//
+// Work unit: one CTA per (kv head [x q-head chunk of 16], sequence, partition of
+// `partition` tokens).  The G = Hq / Hkv query heads that share a kv head form
+// the M = 16 rows of a tensor-core tile, so every K/V byte fetched is used by
+// all G heads (GQA, chengxuchu #47 section 2.3).  The partition's 16-token
+// blocks are split between the CTA's 4 warps; each warp streams its blocks
+// through a private ring of shared-memory stages filled by 16-byte cp.async
+// copies, looked up through the block table (section 5.2), and keeps its own
+// online-softmax state (running max m, sum l, unnormalised O).  The 4 warp
+// states are merged in shared memory; a sequence that fits one partition gets
+// its final output here, otherwise (m, l, O) go to the workspace and a second
+// launch merges the partitions:
+//   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p 2^(m_p - M) O_p / L.
+// Logits are kept in base-2 units (scale * log2 e folded into one multiply).
+#include <math.h>
+
+#include "common.cuh"
+
+namespace {
+
+using pkv::kBlock;
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;   // per-warp ring depth, in blocks
+constexpr int kRows = 16;    // q heads per tile (mma M)
+
+struct DecodeParams {
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    void *out;
+    float *part_o;   // [S][Hq][max_parts][D]
+    float *part_ml;  // [S][Hq][max_parts][2]
+    int max_blocks;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;       // Hq / Hkv
+    int head_chunks; // ceil(group / 16)
+    int num_blocks;
+    int len_cap;     // min(max_blocks * 16, max_context_len)
+    int partition;
+    int max_parts;
+    float scale_log2;
+    unsigned *status;
+};
+
+__device__ __forceinline__ int clamp_len(int L, int cap, unsigned *status, bool report) {
+    if (L < 0 || L > cap) {
+        if (report) pkv::flag(status, PKV_STATUS_BAD_LENGTH);
+        L = L < 0 ? 0 : cap;
+    }
+    return L;
+}
+
+// ----------------------------------------------------------------------------
+// bf16 tensor-core decode
+// ----------------------------------------------------------------------------
+
+template <int D>
+struct DecodeSmem {
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kTile = kBlock * kRowBytes;      // one block of one kv head
+    static constexpr int kStage = 2 * kTile;               // K + V
+    static constexpr int kWarp = kStages * kStage;
+    static constexpr int kStaging = kWarps * kWarp;
+    static constexpr int kMergeStride = D + 8;             // floats per merged row
+    static constexpr int kMergeWarp = kRows * kMergeStride + 2 * kRows;
+    static constexpr int kMerge = kWarps * kMergeWarp * 4;
+    static constexpr int kBytes = kStaging > kMerge ? kStaging : kMerge;
+};
+
+template <int D, typename OutT>
+__global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodeParams p) {
+    using Sm = DecodeSmem<D>;
+    constexpr int CH = D / 8;                 // 16-byte chunks per row
+    constexpr int PER_LANE = kBlock * CH / 32;
+    constexpr int KSTEPS = D / 16;
+    constexpr int NT = D / 8;                 // n-tiles of the output
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int kvh = blockIdx.x / p.head_chunks, chunk = blockIdx.x - kvh * p.head_chunks;
+    const int s = blockIdx.y, part = blockIdx.z;
+
+    const int L = clamp_len(p.context_lens[s], p.len_cap, p.status,
+                            part == 0 && blockIdx.x == 0 && threadIdx.x == 0);
+    const int nparts = L > 0 ? (L + p.partition - 1) / p.partition : 1;
+    if (part >= nparts) return;
+
+    const int h0 = kvh * p.group + chunk * kRows;
+    const int rows = min(kRows, p.group - chunk * kRows);
+    const int t_end = min(L, (part + 1) * p.partition);
+    const int blk_begin = (part * p.partition) / kBlock;
+    const int nblk = (t_end + kBlock - 1) / kBlock - blk_begin;
+    const int wb = blk_begin + (nblk * warp) / kWarps;
+    const int we = blk_begin + (nblk * (warp + 1)) / kWarps;
+    const int n = max(0, we - wb);
+
+    const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *kc = static_cast<const __nv_bfloat16 *>(p.k_cache);
+    const __nv_bfloat16 *vc = static_cast<const __nv_bfloat16 *>(p.v_cache);
+    const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
+
+    // query rows of this tile as mma A fragments (rows >= `rows` are zero)
+    uint32_t qa[KSTEPS][4];
+    {
+        const bool va = gid < rows, vb = gid + 8 < rows;
+        const __nv_bfloat16 *qa_row = qb + ((size_t)s * p.num_q_heads + h0 + gid) * D;
+        const __nv_bfloat16 *qb_row = qa_row + 8 * D;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; kk++) {
+            const int col = kk * 16 + tig * 2;
+            qa[kk][0] = va ? *reinterpret_cast<const uint32_t *>(qa_row + col) : 0u;
+            qa[kk][1] = vb ? *reinterpret_cast<const uint32_t *>(qb_row + col) : 0u;
+            qa[kk][2] = va ? *reinterpret_cast<const uint32_t *>(qa_row + col + 8) : 0u;
+            qa[kk][3] = vb ? *reinterpret_cast<const uint32_t *>(qb_row + col + 8) : 0u;
+        }
+    }
+
+    unsigned char *ring = smem + warp * Sm::kWarp;
+
+    // rows of logical block `bi` that hold tokens of this partition (0 for a bad id)
+    auto block_rows = [&](int bi, int &phys) -> int {
+        phys = table[bi];
+        if (phys < 0 || phys >= p.num_blocks) return -1;
+        return min(kBlock, t_end - bi * kBlock);
+    };
+
+    auto issue = [&](int bi, int st) {
+        int phys;
+        int valid = block_rows(bi, phys);
+        if (valid < 0) {
+            if (lane == 0) pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+            valid = 0;
+            phys = 0;
+        }
+        const size_t base = ((size_t)phys * p.num_kv_heads + kvh) * kBlock * D;
+        const unsigned char *kg = reinterpret_cast<const unsigned char *>(kc + base);
+        const unsigned char *vg = reinterpret_cast<const unsigned char *>(vc + base);
+        unsigned char *ks = ring + st * Sm::kStage;
+        unsigned char *vs = ks + Sm::kTile;
+#pragma unroll
+        for (int j = 0; j < PER_LANE; j++) {
+            const int i = lane + 32 * j;
+            const int r = i / CH, c = i - (i / CH) * CH;
+            const int nb = r < valid ? 16 : 0;
+            const int go = r * Sm::kRowBytes + c * 16;
+            pkv::cp_async16(ks + pkv::swz(r, c, Sm::kRowBytes), kg + (nb ? go : 0), nb);
+            pkv::cp_async16(vs + pkv::swz(r, c, Sm::kRowBytes), vg + (nb ? go : 0), nb);
+        }
+    };
+
+    float o[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+
+#pragma unroll
+    for (int st = 0; st < kStages - 1; st++) {
+        if (st < n) issue(wb + st, st);
+        pkv::cp_async_commit();
+    }
+
+    for (int i = 0; i < n; i++) {
+        {
+            const int nx = i + kStages - 1;
+            if (nx < n) issue(wb + nx, nx % kStages);
+            pkv::cp_async_commit();
+        }
+        pkv::cp_async_wait<kStages - 1>();
+        __syncwarp();
+
+        const int st = i % kStages;
+        const unsigned char *ks = ring + st * Sm::kStage;
+        const unsigned char *vs = ks + Sm::kTile;
+        int phys;
+        int valid = block_rows(wb + i, phys);
+        if (valid < 0) valid = 0;
+
+        // S = q . K^T for the block's 16 tokens (two n-tiles of 8 tokens)
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; kk++) {
+            uint32_t b0, b1, b2, b3;
+            const int tok = ((lane >> 4) << 3) + (lane & 7);
+            const int ch = kk * 2 + ((lane >> 3) & 1);
+            pkv::ldsm_x4(b0, b1, b2, b3, ks + pkv::swz(tok, ch, Sm::kRowBytes));
+            pkv::mma_bf16(s0, qa[kk], b0, b1);
+            pkv::mma_bf16(s1, qa[kk], b2, b3);
+        }
+        // scale to base-2 units and mask rows past the context
+        const int t0 = tig * 2;
+        float x[8] = {s0[0], s0[1], s1[0], s1[1], s0[2], s0[3], s1[2], s1[3]};
+        const int tk[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            x[e] = tk[e & 3] < valid ? x[e] * p.scale_log2 : -INFINITY;
+        }
+        float mxA = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        float mxB = fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]));
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+        const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
+        const float baseA = nA == -INFINITY ? 0.f : nA;
+        const float baseB = nB == -INFINITY ? 0.f : nB;
+        const float alA = pkv::fast_exp2(mA - baseA), alB = pkv::fast_exp2(mB - baseB);
+        mA = nA;
+        mB = nB;
+        float pr[8];
+#pragma unroll
+        for (int e = 0; e < 4; e++) pr[e] = pkv::fast_exp2(x[e] - baseA);
+#pragma unroll
+        for (int e = 4; e < 8; e++) pr[e] = pkv::fast_exp2(x[e] - baseB);
+        lA = lA * alA + (pr[0] + pr[1] + pr[2] + pr[3]);
+        lB = lB * alB + (pr[4] + pr[5] + pr[6] + pr[7]);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            o[nt][0] *= alA;
+            o[nt][1] *= alA;
+            o[nt][2] *= alB;
+            o[nt][3] *= alB;
+        }
+        // P as two bf16 A fragments, hi + lo, so P keeps ~16 significant bits
+        float hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) pkv::split_bf16(pr[e], hi[e], lo[e]);
+        const uint32_t ph[4] = {pkv::pack_bf16(hi[0], hi[1]), pkv::pack_bf16(hi[4], hi[5]),
+                                pkv::pack_bf16(hi[2], hi[3]), pkv::pack_bf16(hi[6], hi[7])};
+        const uint32_t pl[4] = {pkv::pack_bf16(lo[0], lo[1]), pkv::pack_bf16(lo[4], lo[5]),
+                                pkv::pack_bf16(lo[2], lo[3]), pkv::pack_bf16(lo[6], lo[7])};
+        // O += P . V
+#pragma unroll
+        for (int nn = 0; nn < D / 16; nn++) {
+            uint32_t v0, v1, v2, v3;
+            const int j = lane >> 3;
+            const int tok = ((j & 1) << 3) + (lane & 7);
+            const int ch = nn * 2 + (j >> 1);
+            pkv::ldsm_x4_t(v0, v1, v2, v3, vs + pkv::swz(tok, ch, Sm::kRowBytes));
+            pkv::mma_bf16(o[2 * nn], ph, v0, v1);
+            pkv::mma_bf16(o[2 * nn], pl, v0, v1);
+            pkv::mma_bf16(o[2 * nn + 1], ph, v2, v3);
+            pkv::mma_bf16(o[2 * nn + 1], pl, v2, v3);
+        }
+        __syncwarp();
+    }
+
+    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+
+    pkv::cp_async_wait<0>();
+    __syncthreads();  // every warp is done with its ring; reuse it for the merge
+
+    float *mw = reinterpret_cast<float *>(smem) + warp * Sm::kMergeWarp;
+    float *mm = mw + kRows * Sm::kMergeStride;
+    float *ll = mm + kRows;
+    if (tig == 0) {
+        mm[gid] = mA;
+        mm[gid + 8] = mB;
+        ll[gid] = lA;
+        ll[gid + 8] = lB;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+        const int col = nt * 8 + tig * 2;
+        *reinterpret_cast<float2 *>(mw + gid * Sm::kMergeStride + col) = make_float2(o[nt][0], o[nt][1]);
+        *reinterpret_cast<float2 *>(mw + (gid + 8) * Sm::kMergeStride + col) =
+            make_float2(o[nt][2], o[nt][3]);
+    }
+    __syncthreads();
+
+    const float *base = reinterpret_cast<const float *>(smem);
+    for (int idx = threadIdx.x; idx < rows * D; idx += kThreads) {
+        const int r = idx / D, c = idx - (idx / D) * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; w++) M = fmaxf(M, base[w * Sm::kMergeWarp + kRows * Sm::kMergeStride + r]);
+        float acc = 0.f, lsum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; w++) {
+                const float *bw = base + w * Sm::kMergeWarp;
+                const float f = pkv::fast_exp2(bw[kRows * Sm::kMergeStride + r] - M);
+                lsum += bw[kRows * Sm::kMergeStride + kRows + r] * f;
+                acc += bw[r * Sm::kMergeStride + c] * f;
+            }
+        }
+        const size_t orow = (size_t)s * p.num_q_heads + h0 + r;
+        if (nparts == 1) {
+            pkv::store1(static_cast<OutT *>(p.out) + orow * D + c, lsum > 0.f ? acc / lsum : 0.f);
+        } else {
+            const size_t prow = orow * p.max_parts + part;
+            p.part_o[prow * D + c] = acc;
+            if (c == 0) {
+                p.part_ml[prow * 2] = M;
+                p.part_ml[prow * 2 + 1] = lsum;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// CUDA-core decode for fp32 caches (and any head group): one CTA per
+// (q head, sequence, partition), one token per thread per pass of 128 tokens,
+// two-pass softmax within the pass and online rescaling across passes.
+// ----------------------------------------------------------------------------
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T *p);
+template <>
+__device__ __forceinline__ float ld_elem<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
+}
+
+__device__ __forceinline__ float block_reduce(float v, float *red, bool is_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        const float u = __shfl_xor_sync(0xffffffffu, v, off);
+        v = is_max ? fmaxf(v, u) : v + u;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; w++) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    return r;
+}
+
+// Attention of one query row over tokens [t_begin, t_end) of one sequence.
+// Returns (m, l) and leaves this thread's output column (tid < D) in `acc`.
+template <typename T>
+__device__ void rows_cuda_core(const T *qrow, const T *kc, const T *vc, const int32_t *table,
+                               int t_begin, int t_end, int num_blocks, int num_kv_heads, int kvh,
+                               int D, float scale_log2, unsigned *status, float *sq, float *sp,
+                               int *sb, float *red, float &m, float &l, float &acc) {
+    const int tid = threadIdx.x;
+    for (int c = tid; c < D; c += kThreads) sq[c] = ld_elem(qrow + c);
+    m = -INFINITY;
+    l = 0.f;
+    acc = 0.f;
+    __syncthreads();
+    for (int t0 = t_begin; t0 < t_end; t0 += kThreads) {
+        const int t = t0 + tid;
+        float x = -INFINITY;
+        int phys = -1;
+        if (t < t_end) {
+            phys = table[t / kBlock];
+            if (phys < 0 || phys >= num_blocks) {
+                pkv::flag(status, PKV_STATUS_BAD_BLOCK);
+                phys = -1;
+            } else {
+                const T *kr = kc + (((size_t)phys * num_kv_heads + kvh) * kBlock + t % kBlock) * D;
+                float dot = 0.f;
+                for (int c = 0; c < D; c++) dot = fmaf(sq[c], ld_elem(kr + c), dot);
+                x = dot * scale_log2;
+            }
+        }
+        const float cmax = block_reduce(x, red, true);
+        const float mn = fmaxf(m, cmax);
+        const float base = mn == -INFINITY ? 0.f : mn;
+        const float alpha = pkv::fast_exp2(m - base);
+        const float pt = pkv::fast_exp2(x - base);
+        sp[tid] = pt;
+        sb[tid] = phys;
+        const float psum = block_reduce(pt, red, false);  // also orders sp/sb writes
+        l = l * alpha + psum;
+        m = mn;
+        acc *= alpha;
+        const int cnt = min(kThreads, t_end - t0);
+        if (tid < D) {
+            for (int i = 0; i < cnt; i++) {
+                if (sb[i] < 0) continue;
+                const int t2 = t0 + i;
+                const T *vr = vc + (((size_t)sb[i] * num_kv_heads + kvh) * kBlock + t2 % kBlock) * D;
+                acc = fmaf(sp[i], ld_elem(vr + tid), acc);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T, typename OutT>
+__global__ void __launch_bounds__(kThreads) decode_cuda_core_kernel(const DecodeParams p, int D) {
+    __shared__ float sq[128];
+    __shared__ float sp[kThreads];
+    __shared__ int sb[kThreads];
+    __shared__ float red[kWarps];
+    const int h = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
+    const int L = clamp_len(p.context_lens[s], p.len_cap, p.status,
+                            part == 0 && h == 0 && threadIdx.x == 0);
+    const int nparts = L > 0 ? (L + p.partition - 1) / p.partition : 1;
+    if (part >= nparts) return;
+    const int kvh = h / p.group;
+    const T *qrow = static_cast<const T *>(p.q) + ((size_t)s * p.num_q_heads + h) * D;
+    float m, l, acc;
+    rows_cuda_core<T>(qrow, static_cast<const T *>(p.k_cache), static_cast<const T *>(p.v_cache),
+                      p.block_tables + (size_t)s * p.max_blocks, part * p.partition,
+                      min(L, (part + 1) * p.partition), p.num_blocks, p.num_kv_heads, kvh, D,
+                      p.scale_log2, p.status, sq, sp, sb, red, m, l, acc);
+    const int c = threadIdx.x;
+    if (c >= D) return;
+    const size_t orow = (size_t)s * p.num_q_heads + h;
+    if (nparts == 1) {
+        pkv::store1(static_cast<OutT *>(p.out) + orow * D + c, l > 0.f ? acc / l : 0.f);
+    } else {
+        const size_t prow = orow * p.max_parts + part;
+        p.part_o[prow * D + c] = acc;
+        if (c == 0) {
+            p.part_ml[prow * 2] = m;
+            p.part_ml[prow * 2 + 1] = l;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// log-sum-exp merge of the partitions of each (sequence, q head)
+// ----------------------------------------------------------------------------
+
+template <typename OutT>
+__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p, int D) {
+    const int h = blockIdx.x, s = blockIdx.y, c = threadIdx.x;
+    const int L = clamp_len(p.context_lens[s], p.len_cap, p.status, false);
+    const int nparts = L > 0 ? (L + p.partition - 1) / p.partition : 1;
+    if (nparts <= 1 || c >= D) return;
+    const size_t prow = ((size_t)s * p.num_q_heads + h) * p.max_parts;
+    const float *ml = p.part_ml + prow * 2;
+    float M = -INFINITY;
+    for (int q = 0; q < nparts; q++) M = fmaxf(M, ml[2 * q]);
+    float acc = 0.f, lsum = 0.f;
+    if (M != -INFINITY) {
+        const float *po = p.part_o + prow * D + c;
+        for (int q = 0; q < nparts; q++) {
+            const float f = pkv::fast_exp2(ml[2 * q] - M);
+            lsum += ml[2 * q + 1] * f;
+            acc += po[(size_t)q * D] * f;
+        }
+    }
+    pkv::store1(static_cast<OutT *>(p.out) + ((size_t)s * p.num_q_heads + h) * D + c,
+                lsum > 0.f ? acc / lsum : 0.f);
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
+    if (max_parts <= 1) return 0;
+    const size_t rows = (size_t)num_seqs * num_q_heads * max_parts;
+    return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float));
+}
+
+int resolve_partition(int partition_size, int *out) {
+    if (partition_size == 0) partition_size = PKV_DEFAULT_PARTITION;
+    if (partition_size < kBlock || partition_size % kBlock != 0)
+        return pkv::fail(PKV_ERR_INVALID, "partition_size must be a positive multiple of 16 (got %d)",
+                         partition_size);
+    *out = partition_size;
+    return PKV_OK;
+}
+
+template <int D, typename OutT>
+int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
+    constexpr int bytes = DecodeSmem<D>::kBytes;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(decode_bf16_kernel<D, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 bytes) != cudaSuccess)
+            return pkv::check_launch("decode: set shared memory size");
+        attr_set[dev] = true;
+    }
+    dim3 grid((unsigned)(p.num_kv_heads * p.head_chunks), (unsigned)num_seqs, (unsigned)p.max_parts);
+    decode_bf16_kernel<D, OutT><<<grid, kThreads, bytes, st>>>(p);
+    return pkv::check_launch("decode_bf16");
+}
+
+template <typename T, typename OutT>
+int launch_core(const DecodeParams &p, int num_seqs, int D, cudaStream_t st) {
+    dim3 grid((unsigned)p.num_q_heads, (unsigned)num_seqs, (unsigned)p.max_parts);
+    decode_cuda_core_kernel<T, OutT><<<grid, kThreads, 0, st>>>(p, D);
+    return pkv::check_launch("decode_cuda_core");
+}
+
+template <typename OutT>
+int launch_decode(const DecodeParams &p, int num_seqs, int D, int dtype, cudaStream_t st) {
+    int rc;
+    if (dtype == PKV_BF16) {
+        rc = D == 128 ? launch_bf16<128, OutT>(p, num_seqs, st) : launch_bf16<64, OutT>(p, num_seqs, st);
+    } else {
+        rc = launch_core<float, OutT>(p, num_seqs, D, st);
+    }
+    if (rc || p.max_parts <= 1) return rc;
+    decode_reduce_kernel<OutT><<<dim3((unsigned)p.num_q_heads, (unsigned)num_seqs), 128, 0, st>>>(p, D);
+    return pkv::check_launch("decode_reduce");
+}
+
+}  // namespace
+
+extern "C" int pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                          int max_context_len, int partition_size, size_t *bytes) {
+    int part;
+    int rc = resolve_partition(partition_size, &part);
+    if (rc) return rc;
+    if (!bytes || num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 ||
+        (head_dim != 64 && head_dim != 128))
+        return pkv::fail(PKV_ERR_INVALID, "decode_workspace_bytes: bad argument");
+    const int max_parts = max_context_len > 0 ? (max_context_len + part - 1) / part : 1;
+    *bytes = workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
+    return PKV_OK;
+}
+
+extern "C" int pkv_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables, int max_blocks_per_seq,
+                                          const int32_t *context_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_blocks, int max_context_len,
+                                          int partition_size, float scale, void *out, int dtype,
+                                          int out_dtype, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+    int part;
+    int rc = resolve_partition(partition_size, &part);
+    if (rc) return rc;
+    if (block_size != kBlock) return pkv::fail(PKV_ERR_INVALID, "block_size must be 16 (got %d)", block_size);
+    if (head_dim != 64 && head_dim != 128)
+        return pkv::fail(PKV_ERR_INVALID, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (dtype != PKV_F32 && dtype != PKV_BF16) return pkv::fail(PKV_ERR_INVALID, "bad dtype %d", dtype);
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
+        return pkv::fail(PKV_ERR_INVALID, "bad out_dtype %d", out_dtype);
+    if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0)
+        return pkv::fail(PKV_ERR_INVALID, "decode: negative size");
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return pkv::fail(PKV_ERR_INVALID, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                         num_q_heads, num_kv_heads);
+    if (!(scale == scale)) return pkv::fail(PKV_ERR_INVALID, "decode: scale is NaN");
+    if (num_seqs == 0) return PKV_OK;
+    if (num_seqs > 65535) return pkv::fail(PKV_ERR_INVALID, "decode: at most 65535 sequences per call");
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return pkv::fail(PKV_ERR_INVALID, "decode: null pointer");
+    if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) || !pkv::aligned16(out))
+        return pkv::fail(PKV_ERR_INVALID, "decode: q, caches and out must be 16-byte aligned");
+
+    DecodeParams p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = out;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_q_heads / num_kv_heads;
+    p.head_chunks = (p.group + kRows - 1) / kRows;
+    p.num_blocks = num_blocks;
+    const long long cap = (long long)max_blocks_per_seq * kBlock;
+    p.len_cap = (int)(cap < max_context_len ? cap : max_context_len);
+    p.partition = part;
+    p.max_parts = p.len_cap > 0 ? (p.len_cap + part - 1) / part : 1;
+    if (p.max_parts > 65535) return pkv::fail(PKV_ERR_INVALID, "decode: too many partitions");
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = pkv::status_ptr();
+
+    const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, p.max_parts);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need)
+            return pkv::fail(PKV_ERR_INVALID, "decode: workspace of %zu bytes needed, %zu given", need,
+                             workspace_bytes);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return pkv::fail(PKV_ERR_INVALID, "decode: workspace must be 256-byte aligned");
+        const size_t rows = (size_t)num_seqs * num_q_heads * p.max_parts;
+        p.part_o = static_cast<float *>(workspace);
+        p.part_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                              align256(rows * head_dim * sizeof(float)));
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return out_dtype == PKV_F32 ? launch_decode<float>(p, num_seqs, head_dim, dtype, st)
+                                : launch_decode<__nv_bfloat16>(p, num_seqs, head_dim, dtype, st);
+}

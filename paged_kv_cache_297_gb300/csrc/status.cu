@@ -1,0 +1,64 @@
+// Per-device status word, error strings and version.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "common.cuh"
+
+namespace {
+// One word per device that loads the library; kernels OR PKV_STATUS_* bits in.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned *g_status_addr[kMaxDevices];
+thread_local char g_err[512];
+}  // namespace
+
+namespace pkv {
+
+unsigned *status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_status_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_status_addr[dev] = static_cast<unsigned *>(p);
+    }
+    return g_status_addr[dev];
+}
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int check_launch(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_get_status(void *stream, unsigned int *flags) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned *p = pkv::status_ptr();
+    if (!p) return pkv::fail(PKV_ERR_CUDA, "pkv_get_status: no device status word");
+    cudaError_t e = cudaStreamSynchronize(s);
+    unsigned v = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_get_status: %s", cudaGetErrorString(e));
+    if (flags) *flags = v;
+    return v ? PKV_ERR_OOB : PKV_OK;
+}
+
+extern "C" const char *pkv_last_error_string(void) { return g_err; }
+
+extern "C" int pkv_version(void) { return 100; }

@@ -1,0 +1,107 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry
+point that include/pkv.h declares, and rejects bad arguments on the host
+before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_297_gb300 as pkv
+from paged_kv_cache_297_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return pkv.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    return sorted(set(re.findall(r"^(?:int|const char \*)\s*(pkv_\w+)\(", text, re.M)))
+
+
+def test_header_and_binding_agree():
+    assert _declared() == sorted(pkv.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_version(lib):
+    assert lib.pkv_version() >= 100
+
+
+def test_decode_workspace_sizes(lib):
+    n = ctypes.c_size_t(0)
+    # one partition: no workspace
+    assert lib.pkv_decode_workspace_bytes(64, 32, 128, 512, 0, ctypes.byref(n)) == 0
+    assert n.value == 0
+    # 8 partitions of 512 for 4096 tokens: partial O (d floats) and (m, l) per
+    # (seq, q head, partition), each region rounded up to 256 bytes
+    assert lib.pkv_decode_workspace_bytes(64, 32, 128, 4096, 0, ctypes.byref(n)) == 0
+    rows = 64 * 32 * 8
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert n.value == r256(rows * 128 * 4) + r256(rows * 2 * 4)
+    assert lib.pkv_decode_workspace_bytes(64, 32, 128, 4096, 100, ctypes.byref(n)) == pkv.ERR_INVALID
+    assert b"multiple of 16" in lib.pkv_last_error_string()
+
+
+@pytest.mark.parametrize("bad", ["block_size", "head_dim", "dtype", "heads"])
+def test_host_rejects_bad_arguments(lib, bad):
+    P = ctypes.c_void_p
+    dummy = P(256)  # never dereferenced: rejected before any launch
+    args = dict(block_size=16, head_dim=128, dtype=pkv.BF16, hq=32, hkv=8)
+    if bad == "block_size":
+        args["block_size"] = 32
+    elif bad == "head_dim":
+        args["head_dim"] = 96
+    elif bad == "dtype":
+        args["dtype"] = 7
+    else:
+        args["hq"] = 30
+    rc = lib.pkv_paged_attention_decode(
+        dummy, dummy, dummy, dummy, 4, dummy, 2, args["hq"], args["hkv"], args["head_dim"],
+        args["block_size"], 8, 64, 0, ctypes.c_float(0.1), dummy, args["dtype"], pkv.F32, None,
+        0, None)
+    assert rc == pkv.ERR_INVALID
+    assert lib.pkv_last_error_string()
+    rc = lib.pkv_kv_append(dummy, dummy, dummy, 1, dummy, dummy, 8, args["hkv"], args["head_dim"],
+                           args["block_size"], args["dtype"], None)
+    if bad in ("block_size", "head_dim", "dtype"):
+        assert rc == pkv.ERR_INVALID
+
+
+def test_decode_rejects_small_workspace_and_misalignment(lib):
+    P = ctypes.c_void_p
+    a = P(4096)
+    rc = lib.pkv_paged_attention_decode(a, a, a, a, 256, a, 2, 32, 8, 128, 16, 64, 4096, 0,
+                                        ctypes.c_float(0.1), a, pkv.BF16, pkv.F32, a, 16, None)
+    assert rc == pkv.ERR_INVALID and b"workspace" in lib.pkv_last_error_string()
+    rc = lib.pkv_paged_attention_decode(P(4098), a, a, a, 4, a, 2, 32, 8, 128, 16, 64, 64, 0,
+                                        ctypes.c_float(0.1), a, pkv.BF16, pkv.F32, None, 0, None)
+    assert rc == pkv.ERR_INVALID and b"aligned" in lib.pkv_last_error_string()
+
+
+def test_prefill_rejects_wide_groups(lib):
+    P = ctypes.c_void_p
+    a = P(4096)
+    rc = lib.pkv_paged_attention_prefill_chunk(a, a, a, a, a, 4, a, 1, 8, 8, 64, 128, 1, 128, 16,
+                                               8, ctypes.c_float(0.1), a, pkv.BF16, pkv.F32, None,
+                                               0, None)
+    assert rc == pkv.ERR_INVALID
+
+
+def test_zero_sized_calls_launch_nothing(lib):
+    # num_tokens / num_pairs / num_seqs of 0 return OK before any CUDA call
+    assert lib.pkv_kv_append(None, None, None, 0, None, None, 0, 8, 128, 16, pkv.BF16, None) == 0
+    assert lib.pkv_copy_blocks(None, None, None, 0, 0, 8, 128, 16, pkv.BF16, None) == 0
+    assert lib.pkv_paged_attention_decode(None, None, None, None, 0, None, 0, 32, 8, 128, 16, 0, 0,
+                                          0, ctypes.c_float(1.0), None, pkv.BF16, pkv.F32, None, 0,
+                                          None) == 0

@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs.
+
+Indexing work (append scatter, copy-on-write copy, block-table gather) must be
+bit-exact; attention outputs must meet the stated float tolerances.  Every
+cache row that holds no token is NaN, so an over-read shows up as a
+non-finite output.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_297_gb300 as pkv
+from paged_kv_cache_297_gb300 import workloads as W
+from tests._steps import assert_bits_equal, assert_parity, gpu_step, oracle_step, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    if torch.cuda.is_available():
+        pkv.get_status()
+    yield
+    if torch.cuda.is_available():
+        pkv.get_status()
+
+
+def _check_step(b, out_dtype=torch.float32, partition_size=0):
+    kc_o, vc_o, out_o, pout_o = oracle_step(b)
+    kc_g, vc_g, out_g, pout_g = gpu_step(b, out_dtype=out_dtype, partition_size=partition_size)
+    assert_bits_equal(kc_g, kc_o, "k_cache after copy+append")
+    assert_bits_equal(vc_g, vc_o, "v_cache after copy+append")
+    res = {}
+    if b.q.shape[0]:
+        res["decode"] = assert_parity(out_g, out_o, b.dtype, "decode")
+    if pout_o is not None:
+        res["prefill"] = assert_parity(pout_g, pout_o, b.dtype, "prefill")
+    assert pkv.get_status() == 0
+    return res
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+@pytest.mark.parametrize("name", list(W.SPECS))
+def test_workload_parity_fp32_out(name):
+    b = W.make_batch(name)
+    res = _check_step(b, torch.float32)
+    print(name, res)
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_decode", "long_context", "mixed_step"])
+def test_workload_parity_bf16_out(name):
+    b = W.make_batch(name)
+    _check_step(b, torch.bfloat16)
+
+
+# ------------------------------------------------------------------ edge cases
+
+EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 511, 512, 513, 1023, 1024, 1025, 2047]
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d", [
+    ("bf16", 32, 8, 128), ("bf16", 64, 8, 128), ("bf16", 8, 8, 64), ("bf16", 16, 1, 128),
+    ("bf16", 32, 1, 64), ("bf16", 48, 2, 128), ("f32", 4, 4, 64), ("f32", 16, 4, 128),
+])
+def test_edge_lengths(dtype, hq, hkv, d):
+    b = W.custom_batch(dtype, len(EDGE_LENS), hq, hkv, d, EDGE_LENS, seed=101 + hq + d)
+    _check_step(b)
+
+
+@pytest.mark.parametrize("partition", [16, 64, 112, 512, 4096])
+def test_partition_sizes_agree(partition):
+    lens = [1, 16, 100, 511, 512, 513, 1500, 4000]
+    b = W.custom_batch("bf16", len(lens), 32, 8, 128, lens, seed=202)
+    _check_step(b, partition_size=partition)
+
+
+def test_split_matches_unsplit():
+    lens = [3000, 4096, 777, 2049]
+    b = W.custom_batch("bf16", len(lens), 32, 8, 128, lens, seed=203)
+    _, _, split, _ = gpu_step(b, partition_size=512)
+    _, _, whole, _ = gpu_step(b, partition_size=4096)
+    assert float((split - whole).abs().max()) <= 2e-3
+
+
+def test_single_token_context_returns_value_row_exactly():
+    b = W.custom_batch("bf16", 6, 32, 8, 128, [1] * 6, seed=204)
+    _, _, out, _ = gpu_step(b)
+    ref = b.v_new.float().repeat_interleave(4, dim=1)
+    assert torch.equal(out.cpu(), ref)
+
+
+def test_outlier_rows_long_mixed_lengths():
+    lens = [40000, 513, 8191, 65536]
+    b = W.custom_batch("bf16", len(lens), 64, 8, 128, lens, seed=205, outlier_p=0.01,
+                       outlier_scale=20.0)
+    _check_step(b)
+
+
+@pytest.mark.parametrize("priors,chunks,hq,hkv,d", [
+    ([0, 5, 100, 16], [1, 17, 64, 200], 32, 8, 128),
+    ([0, 3072], [512, 512], 64, 8, 128),
+    ([7, 0], [130, 33], 8, 8, 64),
+    ([1000], [1], 16, 1, 128),
+])
+def test_prefill_edges(priors, chunks, hq, hkv, d):
+    b = W.custom_prefill("bf16", hq, hkv, d, priors, chunks, seed=301 + sum(chunks))
+    _check_step(b)
+
+
+def test_prefill_fp32():
+    b = W.custom_prefill("f32", 8, 2, 64, [0, 40], [20, 9], seed=302)
+    _check_step(b)
+
+
+# ------------------------------------------------------------------ invariances (bitwise)
+
+def test_block_relabelling_is_bitwise_invariant_on_gpu():
+    b = W.make_batch("llama3_8b_decode", num_seqs=16)
+    _, _, out_a, _ = gpu_step(b)
+    NB = b.num_blocks
+    pi = torch.from_numpy(np.random.default_rng(5).permutation(NB))
+    kc = torch.empty_like(b.k_cache)
+    vc = torch.empty_like(b.v_cache)
+    kc[pi] = b.k_cache
+    vc[pi] = b.v_cache
+    b.k_cache, b.v_cache = kc, vc
+    bt = b.block_tables
+    b.block_tables = torch.where(bt >= 0, pi[bt.clamp(min=0).long()].to(torch.int32), bt)
+    sm = b.slot_mapping
+    b.slot_mapping = pi[sm // 16].to(torch.int64) * 16 + sm % 16
+    _, _, out_b, _ = gpu_step(b)
+    assert torch.equal(out_a.cpu(), out_b.cpu())
+
+
+def test_shared_prefix_equals_private_copies_on_gpu():
+    b = W.make_batch("shared_prefix_cow", num_seqs=32)
+    _, _, shared, _ = gpu_step(b)
+    # give every sequence a private copy of the 128 prefix blocks
+    P = b.meta["prefix_blocks"]
+    S = b.num_seqs
+    prefix = b.block_tables[0, :P].long()
+    NB = b.num_blocks
+    extra = S * P
+    kc = torch.cat([b.k_cache, torch.empty((extra,) + b.k_cache.shape[1:], dtype=b.k_cache.dtype)])
+    vc = torch.cat([b.v_cache, torch.empty((extra,) + b.v_cache.shape[1:], dtype=b.v_cache.dtype)])
+    bt = b.block_tables.clone()
+    for s in range(S):
+        ids = torch.arange(NB + s * P, NB + (s + 1) * P)
+        kc[ids] = b.k_cache[prefix]
+        vc[ids] = b.v_cache[prefix]
+        bt[s, :P] = ids.to(torch.int32)
+    b.k_cache, b.v_cache, b.block_tables, b.num_blocks = kc, vc, bt, NB + extra
+    _, _, private, _ = gpu_step(b)
+    assert torch.equal(shared.cpu(), private.cpu())
+
+
+# ------------------------------------------------------------------ device-side checks
+
+def test_bad_block_id_is_flagged_and_skipped():
+    lens = [40, 40]
+    b = W.custom_batch("bf16", 2, 8, 2, 128, lens, seed=401, poison=False)
+    t = to_dev(b)
+    pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"])
+    bt = t["block_tables"].clone()
+    bt[0, 1] = b.num_blocks + 5  # out of range: must be skipped, not read
+    out = torch.empty(b.q.shape, dtype=torch.float32, device="cuda")
+    pkv.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], bt, t["context_lens"], b.scale,
+                               out, max_context_len=64)
+    flags = pkv.get_status()
+    assert flags & pkv.STATUS_BITS["bad_block"]
+    assert bool(torch.isfinite(out).all())
+    # sequence 1 is untouched by the bad id
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    oracle.kv_append(b.k_new, b.v_new, b.slot_mapping, kc, vc)
+    ref = oracle.decode(b.q[1:], kc, vc, b.block_tables[1:], b.context_lens[1:], b.scale)
+    assert_parity(out[1:], ref, torch.bfloat16, "seq 1")
+
+
+def test_bad_slot_is_flagged_and_skipped():
+    b = W.custom_batch("bf16", 2, 8, 2, 128, [5, 9], seed=402, poison=False)
+    t = to_dev(b)
+    before = t["k_cache"].clone()
+    slots = t["slot_mapping"].clone()
+    slots[0] = b.num_blocks * 16 + 3
+    slots[1] = -1  # padding: skipped silently
+    pkv.kv_append(t["k_new"], t["v_new"], slots, t["k_cache"], t["v_cache"])
+    assert pkv.get_status() & pkv.STATUS_BITS["bad_slot"]
+    assert torch.equal(before.cpu(), t["k_cache"].cpu())
+
+
+def test_too_long_context_is_flagged():
+    b = W.custom_batch("bf16", 2, 8, 2, 128, [100, 30], seed=403, poison=False)
+    t = to_dev(b)
+    out = torch.empty(b.q.shape, dtype=torch.float32, device="cuda")
+    pkv.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                               t["context_lens"], b.scale, out, max_context_len=64)
+    assert pkv.get_status() & pkv.STATUS_BITS["bad_length"]
+
+
+def test_bad_copy_pair_is_flagged():
+    b = W.custom_batch("bf16", 1, 8, 2, 128, [20], seed=404, poison=False)
+    t = to_dev(b)
+    before = t["k_cache"].clone()
+    pairs = torch.tensor([[0, b.num_blocks]], dtype=torch.int64, device="cuda")
+    pkv.copy_blocks(pairs, t["k_cache"], t["v_cache"])
+    assert pkv.get_status() & pkv.STATUS_BITS["bad_block"]
+    assert torch.equal(before.cpu(), t["k_cache"].cpu())
+
+
+def test_python_layer_rejects_bad_tensors():
+    b = W.custom_batch("bf16", 2, 8, 2, 128, [5, 9], seed=405, poison=False)
+    t = to_dev(b)
+    out = torch.empty(b.q.shape, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        pkv.paged_attention_decode(t["q"].cpu(), t["k_cache"], t["v_cache"], t["block_tables"],
+                                   t["context_lens"], b.scale, out)
+    with pytest.raises(TypeError):
+        pkv.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"].long(),
+                                   t["context_lens"], b.scale, out)
+    with pytest.raises(pkv.PkvError):
+        pkv.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                                   t["context_lens"], b.scale, out, partition_size=24)
