@@ -137,6 +137,40 @@ int pkv_paged_attention_decode(const void *q, const void *k_cache, const void *v
                                void *stream);
 
 /*
+ * Paged-attention decode that allocates nothing, for callers that cannot
+ * allocate device memory where they run decode (code inside an allocator or
+ * memory-pool hook that must not re-enter the allocator, or embedders whose
+ * device memory is budgeted up front).  The pages have no counterpart to this
+ * entry point; it exists only for such callers.
+ *
+ * Same arguments and results as pkv_paged_attention_decode, minus the
+ * workspace: the split-K partials go to one scratch array of
+ * PKV_NO_ALLOC_SCRATCH_BYTES that is part of this library's device image.
+ * Every GPU that loads the library holds that array until the process exits.
+ *   - Sizes whose scratch need (pkv_decode_workspace_bytes) exceeds
+ *     PKV_NO_ALLOC_SCRATCH_BYTES are rejected with PKV_ERR_INVALID.
+ *   - The call allocates no memory: no cudaMalloc, cudaFree or allocating
+ *     library routine.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current), which may make the
+ *     CUDA driver load this library's device code; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents (no call needs it zeroed).  Calls whose work overlaps
+ *     on the GPU (other streams, or other host threads) race on it: order
+ *     them on one stream or synchronise between them.
+ *   - The stream must belong to the current device.
+ */
+#define PKV_NO_ALLOC_SCRATCH_BYTES (16u << 20)
+int pkv_paged_attention_decode_no_alloc(const void *q, const void *k_cache, const void *v_cache,
+                                        const int32_t *block_tables, int max_blocks_per_seq,
+                                        const int32_t *context_lens, int num_seqs,
+                                        int num_q_heads, int num_kv_heads, int head_dim,
+                                        int block_size, int num_blocks, int max_context_len,
+                                        int partition_size, float scale, void *out, int dtype,
+                                        int out_dtype, void *stream);
+
+/*
  * Workspace (device bytes) that pkv_paged_attention_prefill_chunk needs.
  */
 int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,

@@ -39,7 +39,8 @@ STATUS_BITS = {"bad_slot": 1, "bad_block": 2, "bad_length": 4, "bad_qlen": 8}
 # every entry point declared in include/pkv.h
 EXPORTED = (
     "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes",
-    "pkv_paged_attention_decode", "pkv_prefill_workspace_bytes",
+    "pkv_paged_attention_decode", "pkv_paged_attention_decode_no_alloc",
+    "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_last_error_string",
     "pkv_version",
 )
@@ -76,6 +77,8 @@ def load():
     lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I, I, ctypes.POINTER(SZ)]
     lib.pkv_paged_attention_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I,
                                                I, P, SZ, P]
+    lib.pkv_paged_attention_decode_no_alloc.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I,
+                                                        I, F, P, I, I, P]
     lib.pkv_prefill_workspace_bytes.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
     lib.pkv_paged_attention_prefill_chunk.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, I,
                                                       I, F, P, I, I, P, SZ, P]
