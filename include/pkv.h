@@ -64,6 +64,8 @@ extern "C" {
 #define PKV_STATUS_BAD_LENGTH 4u     /* context_len < 0, > max_blocks_per_seq * block_size,
                                         or > max_context_len */
 #define PKV_STATUS_BAD_QLEN 8u       /* prefill: chunk longer than its context, or than max_q_len */
+#define PKV_STATUS_INTERNAL 16u      /* a kernel gave up waiting on its own asynchronous work, or its
+                                        shared memory was misaligned; its outputs are undefined */
 
 #define PKV_BLOCK_SIZE 16
 #define PKV_DEFAULT_PARTITION 512    /* decode split-K partition, tokens */

@@ -34,7 +34,7 @@ BLOCK_SIZE = 16
 DEFAULT_PARTITION = 512
 OK, ERR_INVALID, ERR_CUDA, ERR_OOB = 0, 1, 2, 3
 F32, BF16 = 0, 1
-STATUS_BITS = {"bad_slot": 1, "bad_block": 2, "bad_length": 4, "bad_qlen": 8}
+STATUS_BITS = {"bad_slot": 1, "bad_block": 2, "bad_length": 4, "bad_qlen": 8, "internal": 16}
 
 # every entry point declared in include/pkv.h
 EXPORTED = (

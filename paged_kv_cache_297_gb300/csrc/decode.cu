@@ -124,16 +124,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
 
     unsigned char *ring = smem + warp * Sm::kWarp;
 
-    // rows of logical block `bi` that hold tokens of this partition (0 for a bad id)
-    auto block_rows = [&](int bi, int &phys) -> int {
-        phys = table[bi];
+    // The warp's first 32 block ids, fetched with one coalesced load so that
+    // issuing a copy never waits on a dependent block-table read.
+    const int my_id = lane < n ? table[wb + lane] : 0;
+    auto block_id = [&](int li) -> int {
+        return li < 32 ? __shfl_sync(0xffffffffu, my_id, li) : table[wb + li];
+    };
+    // rows of the warp's li-th block that hold tokens of this partition (-1 for a bad id)
+    auto block_rows = [&](int li, int &phys) -> int {
+        phys = block_id(li);
         if (phys < 0 || phys >= p.num_blocks) return -1;
-        return min(kBlock, t_end - bi * kBlock);
+        return min(kBlock, t_end - (wb + li) * kBlock);
     };
 
-    auto issue = [&](int bi, int st) {
+    auto issue = [&](int li, int st) {
         int phys;
-        int valid = block_rows(bi, phys);
+        int valid = block_rows(li, phys);
         if (valid < 0) {
             if (lane == 0) pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
             valid = 0;
@@ -162,14 +168,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
 
 #pragma unroll
     for (int st = 0; st < kStages - 1; st++) {
-        if (st < n) issue(wb + st, st);
+        if (st < n) issue(st, st);
         pkv::cp_async_commit();
     }
 
     for (int i = 0; i < n; i++) {
         {
             const int nx = i + kStages - 1;
-            if (nx < n) issue(wb + nx, nx % kStages);
+            if (nx < n) issue(nx, nx % kStages);
             pkv::cp_async_commit();
         }
         pkv::cp_async_wait<kStages - 1>();
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
         const unsigned char *ks = ring + st * Sm::kStage;
         const unsigned char *vs = ks + Sm::kTile;
         int phys;
-        int valid = block_rows(wb + i, phys);
+        int valid = block_rows(i, phys);
         if (valid < 0) valid = 0;
 
         // S = q . K^T for the block's 16 tokens (two n-tiles of 8 tokens)
@@ -428,27 +434,66 @@ __global__ void __launch_bounds__(kThreads) decode_cuda_core_kernel(const Decode
 // log-sum-exp merge of the partitions of each (sequence, q head)
 // ----------------------------------------------------------------------------
 
-template <typename OutT>
-__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p, int D) {
-    const int h = blockIdx.x, s = blockIdx.y, c = threadIdx.x;
+// One warp per (sequence, q head); each lane owns D/32 output columns.  The
+// partition weights 2^(m_p - M) are computed lane-parallel and broadcast by
+// shuffles, and four partitions' loads are kept in flight.
+template <int D, typename OutT>
+__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p, int rows) {
+    constexpr int VEC = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int s = row / p.num_q_heads;
     const int L = clamp_len(p.context_lens[s], p.len_cap, p.status, false);
     const int nparts = L > 0 ? (L + p.partition - 1) / p.partition : 1;
-    if (nparts <= 1 || c >= D) return;
-    const size_t prow = ((size_t)s * p.num_q_heads + h) * p.max_parts;
+    if (nparts <= 1) return;
+    const size_t prow = (size_t)row * p.max_parts;
     const float *ml = p.part_ml + prow * 2;
     float M = -INFINITY;
-    for (int q = 0; q < nparts; q++) M = fmaxf(M, ml[2 * q]);
-    float acc = 0.f, lsum = 0.f;
+    for (int q = lane; q < nparts; q += 32) M = fmaxf(M, ml[2 * q]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; v++) acc[v] = 0.f;
+    float lsum = 0.f;
     if (M != -INFINITY) {
-        const float *po = p.part_o + prow * D + c;
-        for (int q = 0; q < nparts; q++) {
-            const float f = pkv::fast_exp2(ml[2 * q] - M);
-            lsum += ml[2 * q + 1] * f;
-            acc += po[(size_t)q * D] * f;
+        const float *po = p.part_o + prow * D + lane * VEC;
+        for (int q0 = 0; q0 < nparts; q0 += 32) {
+            const int cnt = min(32, nparts - q0);
+            float w = 0.f;
+            if (lane < cnt) {
+                w = pkv::fast_exp2(ml[2 * (q0 + lane)] - M);
+                lsum += ml[2 * (q0 + lane) + 1] * w;
+            }
+            int j = 0;
+            for (; j + 4 <= cnt; j += 4) {
+                float x[4][VEC];
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+#pragma unroll
+                    for (int v = 0; v < VEC; v++) x[u][v] = po[(size_t)(q0 + j + u) * D + v];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const float wj = __shfl_sync(0xffffffffu, w, j + u);
+#pragma unroll
+                    for (int v = 0; v < VEC; v++) acc[v] = fmaf(wj, x[u][v], acc[v]);
+                }
+            }
+            for (; j < cnt; j++) {
+                const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+                for (int v = 0; v < VEC; v++) acc[v] = fmaf(wj, po[(size_t)(q0 + j) * D + v], acc[v]);
+            }
         }
     }
-    pkv::store1(static_cast<OutT *>(p.out) + ((size_t)s * p.num_q_heads + h) * D + c,
-                lsum > 0.f ? acc / lsum : 0.f);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    OutT *o = static_cast<OutT *>(p.out) + (size_t)row * D + lane * VEC;
+#pragma unroll
+    for (int v = 0; v < VEC; v += 2) pkv::store2(o + v, acc[v] * inv, acc[v + 1] * inv);
 }
 
 // ----------------------------------------------------------------------------
@@ -505,7 +550,12 @@ int launch_decode(const DecodeParams &p, int num_seqs, int D, int dtype, cudaStr
         rc = launch_core<float, OutT>(p, num_seqs, D, st);
     }
     if (rc || p.max_parts <= 1) return rc;
-    decode_reduce_kernel<OutT><<<dim3((unsigned)p.num_q_heads, (unsigned)num_seqs), 128, 0, st>>>(p, D);
+    const int rows = num_seqs * p.num_q_heads;
+    const unsigned blocks = (unsigned)((rows + 3) / 4);
+    if (D == 128)
+        decode_reduce_kernel<128, OutT><<<blocks, 128, 0, st>>>(p, rows);
+    else
+        decode_reduce_kernel<64, OutT><<<blocks, 128, 0, st>>>(p, rows);
     return pkv::check_launch("decode_reduce");
 }
 

@@ -14,10 +14,12 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "prefill_common.cuh"
 
 namespace {
 
 using pkv::kBlock;
+using pkv::PrefillParams;
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
@@ -25,25 +27,6 @@ constexpr int kTileQ = 64;   // packed query rows per CTA
 constexpr int kTileK = 64;   // keys per stage
 constexpr int kStages = 2;
 
-struct PrefillParams {
-    const void *q;
-    const int32_t *cu_q_lens;
-    const void *k_cache;
-    const void *v_cache;
-    const int32_t *block_tables;
-    const int32_t *context_lens;
-    void *out;
-    int max_blocks;
-    int num_q_heads;
-    int num_kv_heads;
-    int group;
-    int num_blocks;
-    int len_cap;
-    int max_q_len;
-    int total_q;
-    float scale_log2;
-    unsigned *status;
-};
 
 template <int D>
 struct PrefillSmem {
@@ -366,6 +349,8 @@ int launch_bf16(const PrefillParams &p, int num_seqs, cudaStream_t st) {
 
 template <typename OutT>
 int launch_prefill(const PrefillParams &p, int num_seqs, int D, int dtype, cudaStream_t st) {
+    if (pkv::prefill_tc_supported(dtype, D))
+        return pkv::launch_prefill_tc(p, num_seqs, sizeof(OutT) == 4 ? PKV_F32 : PKV_BF16, st);
     if (dtype == PKV_BF16)
         return D == 128 ? launch_bf16<128, OutT>(p, num_seqs, st) : launch_bf16<64, OutT>(p, num_seqs, st);
     dim3 grid((unsigned)p.num_q_heads, (unsigned)p.max_q_len, (unsigned)num_seqs);

@@ -1,0 +1,33 @@
+// Parameters shared by the chunked-prefill kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct PrefillParams {
+    const void *q;
+    const int32_t *cu_q_lens;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    void *out;
+    int max_blocks;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int num_blocks;
+    int len_cap;
+    int max_q_len;
+    int total_q;
+    float scale_log2;
+    unsigned *status;
+};
+
+// tcgen05 kernel (prefill_tc.cu): bf16 caches with head_dim 128.
+bool prefill_tc_supported(int dtype, int head_dim);
+int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaStream_t st);
+
+}  // namespace pkv

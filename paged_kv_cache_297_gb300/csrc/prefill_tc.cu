@@ -1,0 +1,352 @@
+// Chunked-prefill attention on the 5th-generation tensor cores (tcgen05).
+//
+// Same operation as the mma.sync kernel in prefill.cu: query j of a chunk of n
+// tokens of a sequence with L cached tokens attends causally to tokens
+// 0 .. L-n+j (caffein.top, "Chunked Prefill"), K/V gathered through the block
+// table.  Used for bf16 caches with head_dim 128.
+//
+// Work unit: one CTA of 4 warps per (tile of 128 packed query rows, kv head,
+// sequence).  Row r of the tile is query position R / G, head kvh*G + R % G
+// (R = tile*128 + r), so the G heads of a kv head share every K/V tile.
+//   S  = Q K^T   : tcgen05.mma M=128, N=64 keys, K=d, A = Q (smem), B = K (smem)
+//   O += P V     : tcgen05.mma M=128, N=d, K=64 keys, A = P (smem), B = V (smem,
+//                  MN-major), accumulated in TMEM across key tiles.
+// TMEM columns: S in [0, 64), O in [128, 256) (256 allocated; two CTAs per SM).
+// Thread r owns TMEM lane r = query row r: it reads its 64 scores with
+// tcgen05.ld, applies the causal mask and the online softmax entirely in
+// registers, and writes its row of P (bf16) to shared memory for the PV MMA.
+// The running max is only moved when a row's tile maximum exceeds it by more
+// than 8 (log2 units), so P <= 256 and O is rarely rescaled; the final O / l
+// uses the same reference for numerator and denominator, so this is exact.
+//
+// Shared memory (all operands in the 128-byte-swizzled canonical layout:
+// 8-row atoms of 8 x 128 bytes, 16-byte chunk c of row r stored at chunk
+// c ^ (r % 8)):
+//   Q   : two 64-column halves of 128 rows           (32 KB)
+//   K,V : two stages x (K, V) x two 64-column halves of 64 rows (64 KB)
+//   P   : 128 rows x 64 keys                          (16 KB)
+// K/V tiles are filled with 16-byte cp.async copies (zero-filled past the
+// needed keys); tile kt+1 is fetched while tile kt is processed.
+// Every wait on an mbarrier is bounded; on expiry the kernel records
+// PKV_STATUS_INTERNAL, drains its copies, frees its TMEM and returns.
+#include <math.h>
+
+#include "common.cuh"
+#include "prefill_common.cuh"
+#include "tcgen05.cuh"
+
+namespace {
+
+using pkv::kBlock;
+using pkv::PrefillParams;
+
+constexpr int D = 128;
+constexpr int BM = 128;
+constexpr int BN = 64;
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSCol = 0, kOCol = 128;
+
+constexpr int kQHalf = BM * 128;            // 16 KB: 128 rows x 64 bf16
+constexpr int kKVHalf = BN * 128;           // 8 KB: 64 rows x 64 bf16
+constexpr int kTileBytes = 2 * kKVHalf;     // one K or V tile (both halves)
+constexpr int kStageBytes = 2 * kTileBytes; // K + V
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + 2 * kQHalf;              // 32768
+constexpr int kOffP = kOffKV + 2 * kStageBytes;         // 98304
+constexpr int kOffBar = kOffP + BM * BN * 2;            // 114688
+constexpr int kSmemBytes = kOffBar + 64;
+constexpr unsigned kWaitIters = 1u << 24;
+
+constexpr uint32_t kIdescS = pkv::tc::idesc_bf16_f32(BM, BN, false, false);
+constexpr uint32_t kIdescPV = pkv::tc::idesc_bf16_f32(BM, D, false, true);
+
+__device__ __forceinline__ int sw128(int r, int c16) {
+    return (r >> 3) * 1024 + (r & 7) * 128 + ((c16 ^ (r & 7)) << 4);
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillParams p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tile = blockIdx.x, kvh = blockIdx.y;
+    const int s = gridDim.z - 1 - blockIdx.z;  // later (typically longer) sequences first
+    const int G = p.group;
+
+    const int q0 = p.cu_q_lens[s];
+    const int n = p.cu_q_lens[s + 1] - q0;
+    const int L = p.context_lens[s];
+    if (L < 0 || L > p.len_cap) {
+        if (tile == 0 && kvh == 0 && tid == 0) pkv::flag(p.status, PKV_STATUS_BAD_LENGTH);
+        return;
+    }
+    if (q0 < 0 || n < 0 || n > L || n > p.max_q_len || q0 + n > p.total_q) {
+        if (tile == 0 && kvh == 0 && tid == 0) pkv::flag(p.status, PKV_STATUS_BAD_QLEN);
+        return;
+    }
+    if (tile * BM >= n * G) return;
+    const uint32_t sbase = pkv::smem_u32(smem);
+    if (sbase & 1023u) {  // the swizzled layouts need 1024-byte alignment
+        if (tid == 0) pkv::flag(p.status, PKV_STATUS_INTERNAL);
+        return;
+    }
+    const int prior = L - n;
+    const int j_last = min(n - 1, (tile * BM + BM - 1) / G);
+    const int kv_end = prior + j_last + 1;
+    const int nkt = (kv_end + BN - 1) / BN;
+    const int j_first = (tile * BM) / G;
+    const int mask_from = prior + j_first + 1;  // keys below this need no causal mask
+
+    uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *bar_o = bar_s + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_s + 2);
+
+    if (warp == 0) {
+        pkv::tc::tmem_alloc(tmem_slot, kTmemCols);
+        pkv::tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        pkv::tc::mbar_init(bar_s, 1);
+        pkv::tc::mbar_init(bar_o, 1);
+        pkv::tc::fence_mbar_init();
+    }
+
+    const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
+    const unsigned char *kc = static_cast<const unsigned char *>(p.k_cache);
+    const unsigned char *vc = static_cast<const unsigned char *>(p.v_cache);
+    const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
+
+    // Q tile: 128 rows x 16 chunks, 16 copies per thread
+#pragma unroll 4
+    for (int u = 0; u < 16; u++) {
+        const int i = tid + kThreads * u;
+        const int r = i >> 4, c = i & 15;
+        const int R = tile * BM + r;
+        const int jr = R / G;
+        const bool ok = jr < n;
+        const __nv_bfloat16 *src =
+            ok ? qg + ((size_t)(q0 + jr) * p.num_q_heads + kvh * G + (R - jr * G)) * D + c * 8 : qg;
+        pkv::cp_async16(smem + kOffQ + (c >> 3) * kQHalf + sw128(r, c & 7), src, ok ? 16 : 0);
+    }
+
+    auto load_kv = [&](int kt, int st) {
+        unsigned char *kd = smem + kOffKV + st * kStageBytes;
+        unsigned char *vd = kd + kTileBytes;
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int i = tid + kThreads * u;
+            const int r = i >> 4, c = i & 15;
+            const int t = kt * BN + r;
+            int nb = 0;
+            size_t go = 0;
+            if (t < kv_end) {
+                const int phys = table[t / kBlock];
+                if (phys >= 0 && phys < p.num_blocks) {
+                    nb = 16;
+                    go = ((((size_t)phys * p.num_kv_heads + kvh) * kBlock + (t % kBlock)) * D) * 2 + c * 16;
+                } else if (c == 0 && (t % kBlock) == 0) {
+                    pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                }
+            }
+            const int off = (c >> 3) * kKVHalf + sw128(r, c & 7);
+            pkv::cp_async16(kd + off, kc + go, nb);
+            pkv::cp_async16(vd + off, vc + go, nb);
+        }
+    };
+
+    load_kv(0, 0);
+    pkv::cp_async_commit();
+    if (nkt > 1) load_kv(1, 1);
+    pkv::cp_async_commit();
+
+    pkv::tc::fence_before_sync();
+    __syncthreads();
+    pkv::tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+
+    auto issue_s = [&](int st) {
+        const uint32_t qa = sbase + kOffQ;
+        const uint32_t kb = sbase + kOffKV + st * kStageBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ks++) {
+            const uint64_t a = pkv::tc::smem_desc_sw128(qa + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
+            const uint64_t b = pkv::tc::smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
+            pkv::tc::mma_ss(tmem + kSCol, a, b, kIdescS, ks > 0 ? 1u : 0u);
+        }
+        pkv::tc::mma_commit(bar_s);
+    };
+    auto issue_pv = [&](int st, bool first) {
+        const uint32_t pa = sbase + kOffP;
+        const uint32_t vb = sbase + kOffKV + st * kStageBytes + kTileBytes;
+#pragma unroll
+        for (int kq = 0; kq < BN / 16; kq++) {
+            const uint64_t a = pkv::tc::smem_desc_sw128(pa + kq * 32, 16, 1024);
+            // V is MN-major: next 64-column half at +8 KB (LBO), next 8 keys at +1 KB (SBO)
+            const uint64_t b = pkv::tc::smem_desc_sw128(vb + kq * 2048, kKVHalf, 1024);
+            pkv::tc::mma_ss(tmem + kOCol, a, b, kIdescPV, (first && kq == 0) ? 0u : 1u);
+        }
+        pkv::tc::mma_commit(bar_o);
+    };
+
+    // this thread's query row
+    const int R = tile * BM + tid;
+    const int jrow = R / G;
+    const bool row_ok = jrow < n;
+    const int pos = row_ok ? prior + jrow : -1;
+    float m_used = -INFINITY, lsum = 0.f;
+    bool failed = false;
+
+    pkv::cp_async_wait<1>();  // Q and tile 0 have landed
+    pkv::tc::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        pkv::tc::fence_after_sync();
+        issue_s(0);
+    }
+
+    for (int kt = 0; kt < nkt; kt++) {
+        const int st = kt & 1;
+        bool ok = pkv::tc::mbar_wait(bar_s, (unsigned)(kt & 1), kWaitIters);
+        if (kt > 0) ok = ok && pkv::tc::mbar_wait(bar_o, (unsigned)((kt - 1) & 1), kWaitIters);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        pkv::tc::fence_after_sync();
+        // S(kt) is complete, and so is PV(kt-1): P, O and stage st^1 are free.
+        if (kt >= 1 && kt + 1 < nkt) load_kv(kt + 1, st ^ 1);
+        pkv::cp_async_commit();
+
+        float sv[64];
+        {
+            float a[32], b[32];
+            pkv::tc::tmem_ld32(t_lane + kSCol, a);
+            pkv::tc::tmem_ld32(t_lane + kSCol + 32, b);
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+                sv[i] = a[i];
+                sv[32 + i] = b[i];
+            }
+        }
+        const int t0 = kt * BN;
+        float mt = -INFINITY;
+        if (t0 + BN <= mask_from) {
+#pragma unroll
+            for (int i = 0; i < 64; i++) {
+                sv[i] = row_ok ? sv[i] * p.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, sv[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; i++) {
+                sv[i] = (t0 + i <= pos) ? sv[i] * p.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, sv[i]);
+            }
+        }
+        const bool need = mt > m_used + 8.f;
+        float alpha = 1.f;
+        if (need) {
+            alpha = pkv::fast_exp2(m_used - mt);  // 0 when nothing was seen yet
+            lsum *= alpha;
+            m_used = mt;
+        }
+        if (kt > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                float o[32];
+                pkv::tc::tmem_ld32(t_lane + kOCol + c, o);
+#pragma unroll
+                for (int i = 0; i < 32; i++) o[i] *= alpha;
+                pkv::tc::tmem_st32(t_lane + kOCol + c, o);
+            }
+        }
+        const float base = m_used == -INFINITY ? 0.f : m_used;
+        unsigned char *prow = smem + kOffP;
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+            float e[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                e[i] = pkv::fast_exp2(sv[c * 8 + i] - base);
+                lsum += e[i];
+            }
+            uint4 pk;
+            pk.x = pkv::pack_bf16(e[0], e[1]);
+            pk.y = pkv::pack_bf16(e[2], e[3]);
+            pk.z = pkv::pack_bf16(e[4], e[5]);
+            pk.w = pkv::pack_bf16(e[6], e[7]);
+            *reinterpret_cast<uint4 *>(prow + sw128(tid, c)) = pk;
+        }
+        // P and the next K/V tile must be visible to the tensor core
+        pkv::cp_async_wait<0>();
+        pkv::tc::fence_proxy_async_smem();
+        pkv::tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            pkv::tc::fence_after_sync();
+            issue_pv(st, kt == 0);
+            if (kt + 1 < nkt) issue_s(st ^ 1);
+        }
+    }
+
+    if (!failed) {
+        const bool ok = pkv::tc::mbar_wait(bar_o, (unsigned)((nkt - 1) & 1), kWaitIters);
+        failed = __syncthreads_or(!ok);
+    }
+    if (!failed) {
+        pkv::tc::fence_after_sync();
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        OutT *orow = static_cast<OutT *>(p.out) +
+                     ((size_t)(q0 + jrow) * p.num_q_heads + kvh * G + (R - jrow * G)) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+            float o[32];
+            pkv::tc::tmem_ld32(t_lane + kOCol + c, o);
+            if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) pkv::store2(orow + c + i, o[i] * inv, o[i + 1] * inv);
+            }
+        }
+    } else if (tid == 0) {
+        pkv::flag(p.status, PKV_STATUS_INTERNAL);
+    }
+    pkv::cp_async_wait<0>();
+    pkv::tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        pkv::tc::fence_after_sync();
+        pkv::tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+namespace pkv {
+
+bool prefill_tc_supported(int dtype, int head_dim) { return dtype == PKV_BF16 && head_dim == D; }
+
+int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaStream_t st) {
+    static bool attr_set[2][64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int which = out_dtype == PKV_F32 ? 0 : 1;
+    if (dev >= 0 && dev < 64 && !attr_set[which][dev]) {
+        cudaError_t e = which == 0
+                            ? cudaFuncSetAttribute(prefill_tc_kernel<float>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
+                            : cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return check_launch("prefill_tc: set shared memory size");
+        attr_set[which][dev] = true;
+    }
+    const int tiles = (p.max_q_len * p.group + BM - 1) / BM;
+    dim3 grid((unsigned)tiles, (unsigned)p.num_kv_heads, (unsigned)num_seqs);
+    if (which == 0)
+        prefill_tc_kernel<float><<<grid, kThreads, kSmemBytes, st>>>(p);
+    else
+        prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(p);
+    return check_launch("prefill_tc");
+}
+
+}  // namespace pkv
