@@ -5,16 +5,25 @@
 // 0 .. L-n+j (caffein.top, "Chunked Prefill"), K/V gathered through the block
 // table.  Used for bf16 caches with head_dim 128.
 //
-// Work unit: one CTA of 4 warps per (tile of 128 packed query rows, kv head,
+// Work unit: one CTA of 8 warps per (tile of 128 packed query rows, kv head,
 // sequence).  Row r of the tile is query position R / G, head kvh*G + R % G
 // (R = tile*128 + r), so the G heads of a kv head share every K/V tile.
 //   S  = Q K^T   : tcgen05.mma M=128, N=64 keys, K=d, A = Q (smem), B = K (smem)
 //   O += P V     : tcgen05.mma M=128, N=d, K=64 keys, A = P (smem), B = V (smem,
 //                  MN-major), accumulated in TMEM across key tiles.
-// TMEM columns: S in [0, 64), O in [128, 256) (256 allocated; two CTAs per SM).
-// Thread r owns TMEM lane r = query row r: it reads its 64 scores with
-// tcgen05.ld, applies the causal mask and the online softmax entirely in
-// registers, and writes its row of P (bf16) to shared memory for the PV MMA.
+// TMEM columns: two S buffers at [0, 64) and [64, 128), O at [128, 256).
+// Warps w and w+4 share TMEM lane quarter w (query rows 32w .. 32w+31) and
+// split each row's 64 scores into two halves of 32: each thread reads its half
+// with tcgen05.ld, applies the causal mask, exchanges its half-row maximum
+// with its partner through shared memory, and runs the online softmax in
+// registers (scale and max-subtraction fused into one multiply-add, exp2 on
+// the special-function unit), writing its half of the row of P (bf16) to
+// shared memory for the PV MMA.  O's 128 columns are split the same way.
+// Software pipeline, one CTA per SM: at the end of iteration kt one thread
+// issues PV(kt) and S(kt+2), so the tensor core computes them while the
+// threads run the softmax of tile kt+1 (whose S was issued one iteration
+// earlier).  K/V tiles are fetched four tiles ahead into a 5-stage ring, and
+// the block ids they need are read one further tile ahead.
 // The running max is only moved when a row's tile maximum exceeds it by more
 // than 8 (log2 units), so P <= 256 and O is rarely rescaled; the final O / l
 // uses the same reference for numerator and denominator, so this is exact.
@@ -22,11 +31,11 @@
 // Shared memory (all operands in the 128-byte-swizzled canonical layout:
 // 8-row atoms of 8 x 128 bytes, 16-byte chunk c of row r stored at chunk
 // c ^ (r % 8)):
-//   Q   : two 64-column halves of 128 rows           (32 KB)
-//   K,V : two stages x (K, V) x two 64-column halves of 64 rows (64 KB)
-//   P   : 128 rows x 64 keys                          (16 KB)
+//   Q   : two 64-column halves of 128 rows                         (32 KB)
+//   K,V : five stages x (K, V) x two 64-column halves of 64 rows    (160 KB)
+//   P   : two buffers of 128 rows x 64 keys                         (32 KB)
 // K/V tiles are filled with 16-byte cp.async copies (zero-filled past the
-// needed keys); tile kt+1 is fetched while tile kt is processed.
+// needed keys).
 // Every wait on an mbarrier is bounded; on expiry the kernel records
 // PKV_STATUS_INTERNAL, drains its copies, frees its TMEM and returns.
 #include <math.h>
@@ -43,9 +52,10 @@ using pkv::PrefillParams;
 constexpr int D = 128;
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCol = 0, kOCol = 128;
+constexpr uint32_t kOCol = 128;  // S buffers at columns 0 and 64
+constexpr int kStages = 5;
 
 constexpr int kQHalf = BM * 128;            // 16 KB: 128 rows x 64 bf16
 constexpr int kKVHalf = BN * 128;           // 8 KB: 64 rows x 64 bf16
@@ -53,9 +63,11 @@ constexpr int kTileBytes = 2 * kKVHalf;     // one K or V tile (both halves)
 constexpr int kStageBytes = 2 * kTileBytes; // K + V
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + 2 * kQHalf;              // 32768
-constexpr int kOffP = kOffKV + 2 * kStageBytes;         // 98304
-constexpr int kOffBar = kOffP + BM * BN * 2;            // 114688
-constexpr int kSmemBytes = kOffBar + 64;
+constexpr int kPBytes = BM * BN * 2;                    // 16384
+constexpr int kOffP = kOffKV + kStages * kStageBytes;   // 196608
+constexpr int kOffBar = kOffP + 2 * kPBytes;            // 229376
+constexpr int kOffRed = kOffBar + 64;                   // [2][128] floats
+constexpr int kSmemBytes = kOffRed + 2 * BM * 4;
 constexpr unsigned kWaitIters = 1u << 24;
 
 constexpr uint32_t kIdescS = pkv::tc::idesc_bf16_f32(BM, BN, false, false);
@@ -66,9 +78,11 @@ __device__ __forceinline__ int sw128(int r, int c16) {
 }
 
 template <typename OutT>
-__global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter, score-column half
+    const int row = quarter * 32 + lane;             // this thread's query row in the tile
     const int tile = blockIdx.x, kvh = blockIdx.y;
     const int s = gridDim.z - 1 - blockIdx.z;  // later (typically longer) sequences first
     const int G = p.group;
@@ -97,9 +111,10 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillPa
     const int j_first = (tile * BM) / G;
     const int mask_from = prior + j_first + 1;  // keys below this need no causal mask
 
-    uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *bar_o = bar_s + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_s + 2);
+    uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + kOffBar);  // one per S buffer
+    uint64_t *bar_o = bar_s + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_s + 3);
+    float *xmax = reinterpret_cast<float *>(smem + kOffRed);  // [half][row]
 
     if (warp == 0) {
         pkv::tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -107,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillPa
     }
     if (tid == 0) {
         pkv::tc::mbar_init(bar_s, 1);
+        pkv::tc::mbar_init(bar_s + 1, 1);
         pkv::tc::mbar_init(bar_o, 1);
         pkv::tc::fence_mbar_init();
     }
@@ -116,9 +132,9 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillPa
     const unsigned char *vc = static_cast<const unsigned char *>(p.v_cache);
     const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
 
-    // Q tile: 128 rows x 16 chunks, 16 copies per thread
-#pragma unroll 4
-    for (int u = 0; u < 16; u++) {
+    // Q tile: 128 rows x 16 chunks, 8 copies per thread
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
         const int i = tid + kThreads * u;
         const int r = i >> 4, c = i & 15;
         const int R = tile * BM + r;
@@ -129,18 +145,26 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillPa
         pkv::cp_async16(smem + kOffQ + (c >> 3) * kQHalf + sw128(r, c & 7), src, ok ? 16 : 0);
     }
 
-    auto load_kv = [&](int kt, int st) {
-        unsigned char *kd = smem + kOffKV + st * kStageBytes;
+    // physical ids of the 4 blocks holding keys [kt*64, kt*64 + 64)
+    auto tile_ids = [&](int kt, int (&ids)[4]) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int t = kt * BN + q * kBlock;
+            ids[q] = t < kv_end ? table[t / kBlock] : 0;
+        }
+    };
+    auto load_kv = [&](int kt, const int (&ids)[4]) {
+        unsigned char *kd = smem + kOffKV + (kt % kStages) * kStageBytes;
         unsigned char *vd = kd + kTileBytes;
 #pragma unroll
-        for (int u = 0; u < 8; u++) {
+        for (int u = 0; u < 4; u++) {
             const int i = tid + kThreads * u;
-            const int r = i >> 4, c = i & 15;
+            const int r = i >> 4, c = i & 15;  // r >> 4 == u
             const int t = kt * BN + r;
             int nb = 0;
             size_t go = 0;
             if (t < kv_end) {
-                const int phys = table[t / kBlock];
+                const int phys = ids[u];
                 if (phys >= 0 && phys < p.num_blocks) {
                     nb = 16;
                     go = ((((size_t)phys * p.num_kv_heads + kvh) * kBlock + (t % kBlock)) * D) * 2 + c * 16;
@@ -154,121 +178,129 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillPa
         }
     };
 
-    load_kv(0, 0);
+    int ids[4], ids_next[4];
+    tile_ids(0, ids);
+    load_kv(0, ids);  // same copy group as Q
     pkv::cp_async_commit();
-    if (nkt > 1) load_kv(1, 1);
-    pkv::cp_async_commit();
+#pragma unroll
+    for (int t = 1; t < kStages - 1; t++) {
+        tile_ids(t, ids);
+        if (t < nkt) load_kv(t, ids);
+        pkv::cp_async_commit();
+    }
+    tile_ids(kStages - 1, ids_next);
 
     pkv::tc::fence_before_sync();
     __syncthreads();
     pkv::tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
 
-    auto issue_s = [&](int st) {
+    // S(kt) = Q K(kt)^T into S buffer kt & 1
+    auto issue_s = [&](int kt) {
         const uint32_t qa = sbase + kOffQ;
-        const uint32_t kb = sbase + kOffKV + st * kStageBytes;
+        const uint32_t kb = sbase + kOffKV + (kt % kStages) * kStageBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ks++) {
             const uint64_t a = pkv::tc::smem_desc_sw128(qa + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
             const uint64_t b = pkv::tc::smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
-            pkv::tc::mma_ss(tmem + kSCol, a, b, kIdescS, ks > 0 ? 1u : 0u);
+            pkv::tc::mma_ss(tmem + (kt & 1) * BN, a, b, kIdescS, ks > 0 ? 1u : 0u);
         }
-        pkv::tc::mma_commit(bar_s);
+        pkv::tc::mma_commit(bar_s + (kt & 1));
     };
-    auto issue_pv = [&](int st, bool first) {
-        const uint32_t pa = sbase + kOffP;
-        const uint32_t vb = sbase + kOffKV + st * kStageBytes + kTileBytes;
+    // O (+)= P(kt) V(kt)
+    auto issue_pv = [&](int kt) {
+        const uint32_t pa = sbase + kOffP + (kt & 1) * kPBytes;
+        const uint32_t vb = sbase + kOffKV + (kt % kStages) * kStageBytes + kTileBytes;
 #pragma unroll
         for (int kq = 0; kq < BN / 16; kq++) {
             const uint64_t a = pkv::tc::smem_desc_sw128(pa + kq * 32, 16, 1024);
             // V is MN-major: next 64-column half at +8 KB (LBO), next 8 keys at +1 KB (SBO)
             const uint64_t b = pkv::tc::smem_desc_sw128(vb + kq * 2048, kKVHalf, 1024);
-            pkv::tc::mma_ss(tmem + kOCol, a, b, kIdescPV, (first && kq == 0) ? 0u : 1u);
+            pkv::tc::mma_ss(tmem + kOCol, a, b, kIdescPV, (kt == 0 && kq == 0) ? 0u : 1u);
         }
         pkv::tc::mma_commit(bar_o);
     };
 
     // this thread's query row
-    const int R = tile * BM + tid;
+    const int R = tile * BM + row;
     const int jrow = R / G;
     const bool row_ok = jrow < n;
     const int pos = row_ok ? prior + jrow : -1;
     float m_used = -INFINITY, lsum = 0.f;
     bool failed = false;
 
-    pkv::cp_async_wait<1>();  // Q and tile 0 have landed
+    pkv::cp_async_wait<kStages - 3>();  // Q, tile 0 and tile 1 have landed
     pkv::tc::fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
         pkv::tc::fence_after_sync();
         issue_s(0);
+        if (nkt > 1) issue_s(1);
     }
 
     for (int kt = 0; kt < nkt; kt++) {
-        const int st = kt & 1;
-        bool ok = pkv::tc::mbar_wait(bar_s, (unsigned)(kt & 1), kWaitIters);
-        if (kt > 0) ok = ok && pkv::tc::mbar_wait(bar_o, (unsigned)((kt - 1) & 1), kWaitIters);
+        // S(kt) done; it was issued after PV(kt-2), so that one is done too
+        bool ok = pkv::tc::mbar_wait(bar_s + (kt & 1), (unsigned)((kt >> 1) & 1), kWaitIters);
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
         }
         pkv::tc::fence_after_sync();
-        // S(kt) is complete, and so is PV(kt-1): P, O and stage st^1 are free.
-        if (kt >= 1 && kt + 1 < nkt) load_kv(kt + 1, st ^ 1);
-        pkv::cp_async_commit();
 
-        float sv[64];
-        {
-            float a[32], b[32];
-            pkv::tc::tmem_ld32(t_lane + kSCol, a);
-            pkv::tc::tmem_ld32(t_lane + kSCol + 32, b);
+        // this thread's 32 raw scores (keys t0 + i)
+        float sv[32];
+        pkv::tc::tmem_ld32(t_lane + (kt & 1) * BN + half * 32, sv);
+        const int t0 = kt * BN + half * 32;
+        float mraw = -INFINITY;
+        if (kt * BN + BN <= mask_from) {
+            if (!row_ok) {
 #pragma unroll
-            for (int i = 0; i < 32; i++) {
-                sv[i] = a[i];
-                sv[32 + i] = b[i];
-            }
-        }
-        const int t0 = kt * BN;
-        float mt = -INFINITY;
-        if (t0 + BN <= mask_from) {
-#pragma unroll
-            for (int i = 0; i < 64; i++) {
-                sv[i] = row_ok ? sv[i] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sv[i]);
+                for (int i = 0; i < 32; i++) sv[i] = -INFINITY;
             }
         } else {
+            const int lim = pos - t0;  // keys i <= lim are visible
 #pragma unroll
-            for (int i = 0; i < 64; i++) {
-                sv[i] = (t0 + i <= pos) ? sv[i] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sv[i]);
-            }
+            for (int i = 0; i < 32; i++) sv[i] = i <= lim ? sv[i] : -INFINITY;
         }
+#pragma unroll
+        for (int i = 0; i < 32; i++) mraw = fmaxf(mraw, sv[i]);
+        xmax[half * BM + row] = mraw;
+        // warps w and w+4 (same rows) meet on named barrier 1 + w
+        asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
+        mraw = fmaxf(mraw, xmax[(half ^ 1) * BM + row]);
+        const float mt = mraw * p.scale_log2;  // scale > 0 commutes with max; -inf stays
         const bool need = mt > m_used + 8.f;
         float alpha = 1.f;
         if (need) {
-            alpha = pkv::fast_exp2(m_used - mt);  // 0 when nothing was seen yet
+            alpha = pkv::tc::ex2(m_used - mt);  // 0 when nothing was seen yet
             lsum *= alpha;
             m_used = mt;
         }
+        bool ok_o = true;
         if (kt > 0 && __any_sync(0xffffffffu, need)) {
+            // rescaling O needs PV(kt-1) to have finished
+            ok_o = pkv::tc::mbar_wait(bar_o, (unsigned)((kt - 1) & 1), kWaitIters);
+            pkv::tc::fence_after_sync();
+            if (__all_sync(0xffffffffu, ok_o)) {
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                float o[32];
-                pkv::tc::tmem_ld32(t_lane + kOCol + c, o);
+                for (int c = 0; c < D / 2; c += 32) {
+                    float o[32];
+                    pkv::tc::tmem_ld32(t_lane + kOCol + half * (D / 2) + c, o);
 #pragma unroll
-                for (int i = 0; i < 32; i++) o[i] *= alpha;
-                pkv::tc::tmem_st32(t_lane + kOCol + c, o);
+                    for (int i = 0; i < 32; i++) o[i] *= alpha;
+                    pkv::tc::tmem_st32(t_lane + kOCol + half * (D / 2) + c, o);
+                }
             }
         }
-        const float base = m_used == -INFINITY ? 0.f : m_used;
-        unsigned char *prow = smem + kOffP;
+        const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+        unsigned char *prow = smem + kOffP + (kt & 1) * kPBytes;
 #pragma unroll
-        for (int c = 0; c < 8; c++) {
+        for (int c = 0; c < 4; c++) {
             float e[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) {
-                e[i] = pkv::fast_exp2(sv[c * 8 + i] - base);
+                e[i] = pkv::tc::ex2(fmaf(sv[c * 8 + i], p.scale_log2, nbase));
                 lsum += e[i];
             }
             uint4 pk;
@@ -276,17 +308,24 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillPa
             pk.y = pkv::pack_bf16(e[2], e[3]);
             pk.z = pkv::pack_bf16(e[4], e[5]);
             pk.w = pkv::pack_bf16(e[6], e[7]);
-            *reinterpret_cast<uint4 *>(prow + sw128(tid, c)) = pk;
+            *reinterpret_cast<uint4 *>(prow + sw128(row, half * 4 + c)) = pk;
         }
-        // P and the next K/V tile must be visible to the tensor core
-        pkv::cp_async_wait<0>();
+        // PV(kt-1) done frees stage (kt-1) % kStages: fetch tile kt+kStages-1 into it
+        if (kt > 0) ok_o = ok_o && pkv::tc::mbar_wait(bar_o, (unsigned)((kt - 1) & 1), kWaitIters);
+        if (kt + kStages - 1 < nkt) load_kv(kt + kStages - 1, ids_next);
+        pkv::cp_async_commit();
+        tile_ids(kt + kStages, ids_next);
+        pkv::cp_async_wait<kStages - 3>();  // every tile up to kt+2 has landed
         pkv::tc::fence_proxy_async_smem();
         pkv::tc::fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(!ok_o)) {
+            failed = true;
+            break;
+        }
         if (tid == 0) {
             pkv::tc::fence_after_sync();
-            issue_pv(st, kt == 0);
-            if (kt + 1 < nkt) issue_s(st ^ 1);
+            issue_pv(kt);
+            if (kt + 2 < nkt) issue_s(kt + 2);
         }
     }
 
@@ -296,13 +335,16 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillPa
     }
     if (!failed) {
         pkv::tc::fence_after_sync();
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        xmax[half * BM + row] = lsum;
+        __syncthreads();
+        const float ltot = lsum + xmax[(half ^ 1) * BM + row];
+        const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
         OutT *orow = static_cast<OutT *>(p.out) +
-                     ((size_t)(q0 + jrow) * p.num_q_heads + kvh * G + (R - jrow * G)) * D;
+                     ((size_t)(q0 + jrow) * p.num_q_heads + kvh * G + (R - jrow * G)) * D + half * (D / 2);
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < D / 2; c += 32) {
             float o[32];
-            pkv::tc::tmem_ld32(t_lane + kOCol + c, o);
+            pkv::tc::tmem_ld32(t_lane + kOCol + half * (D / 2) + c, o);
             if (row_ok) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) pkv::store2(orow + c + i, o[i] * inv, o[i + 1] * inv);
