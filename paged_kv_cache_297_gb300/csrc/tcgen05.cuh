@@ -26,6 +26,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
+// Arrive once on `bar` (release semantics at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+                 : "memory");
+}
+
 // One bounded attempt sequence; returns true when phase `parity` completed,
 // false after `max_iters` unsuccessful polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned max_iters) {
