@@ -5,43 +5,57 @@
 // 0 .. L-n+j (caffein.top, "Chunked Prefill"), K/V gathered through the block
 // table.  Used for bf16 caches with head_dim 128.
 //
-// Work unit: one CTA of 9 warps per (tile of 128 packed query rows, kv head,
-// sequence): 8 softmax warps and one warp whose first lane issues the MMAs.  Row r of the tile is query position R / G, head kvh*G + R % G
+// Work unit: one CTA per (tile of 128 packed query rows, kv head, sequence);
+// row r of the tile is query position R / G, head kvh*G + R % G
 // (R = tile*128 + r), so the G heads of a kv head share every K/V tile.
-//   S  = Q K^T   : tcgen05.mma M=128, N=64 keys, K=d, A = Q (smem), B = K (smem)
-//   O += P V     : tcgen05.mma M=128, N=d, K=64 keys, A = P (smem), B = V (smem,
-//                  MN-major), accumulated in TMEM across key tiles.
-// TMEM columns: two S buffers at [0, 64) and [64, 128), O at [128, 256).
-// Warps w and w+4 share TMEM lane quarter w (query rows 32w .. 32w+31) and
-// split each row's 64 scores into two halves of 32: each thread reads its half
-// with tcgen05.ld, applies the causal mask, exchanges its half-row maximum
-// with its partner through shared memory, and runs the online softmax in
-// registers (scale and max-subtraction fused into one multiply-add, exp2 on
-// the special-function unit), writing its half of the row of P (bf16) to
-// shared memory for the PV MMA.  O's 128 columns are split the same way.
-// Software pipeline, one CTA per SM: when all 256 softmax threads have
-// arrived on the P barrier of tile kt (P written, tile kt+2 landed), the MMA
-// lane issues PV(kt) and S(kt+2), so the tensor core computes them while the
-// softmax warps work on tile kt+1, whose S was issued one tile earlier.  No
-// CTA-wide barrier is used inside the loop.  K/V tiles are fetched four tiles ahead into a 5-stage ring, and
-// the block ids they need are read one further tile ahead.
-// The running max is only moved when a row's tile maximum exceeds it by more
-// than 8 (log2 units), so P <= 256 and O is rarely rescaled; the final O / l
-// uses the same reference for numerator and denominator, so this is exact.
+//   S(t)  = Q K(t)^T : tcgen05.mma M=128, N=64 keys, K=d; A = Q (TMEM),
+//                      B = K (smem)
+//   O    += P(t) V(t): tcgen05.mma M=128, N=d, K=64 keys; A = P (TMEM),
+//                      B = V (smem, MN-major); accumulators in TMEM.
+// Keeping both A operands in tensor memory leaves shared-memory bandwidth to
+// the K and V tiles alone (an N=64 MMA that re-read Q from shared memory for
+// every tile was limited by shared-memory reads, not by the tensor core).
+// Warp roles (one CTA per SM, 10 warps):
+//   * two softmax teams of 4 warps: team 0 takes key tiles 0, 2, 4, ..., team 1
+//     tiles 1, 3, 5, ...  Thread r of a team owns query row r (TMEM lane r): it
+//     reads its 64 scores with tcgen05.ld, masks, and runs the online softmax
+//     in registers (scale and max-subtraction fused into one multiply-add, exp2
+//     on the special-function unit), then stores its row of P (bf16 pairs)
+//     into the team's P columns of TMEM.  Each
+//     team has its own S buffer, P buffer, O accumulator and running (m, l);
+//     the two partial results are merged by log-sum-exp at the end.  The teams
+//     run independently, so one team's softmax overlaps the other's.
+//   * one MMA warp whose first lane issues S(t+2) as soon as the team has
+//     read S(t) out of TMEM, and PV(t) as soon as P(t) is written;
+//   * one loader warp that gathers K/V tiles through the block table into a
+//     6-stage ring, refilling a stage once the PV that last read it has
+//     finished.  A tile of four whole blocks is fetched with sixteen 2-D TMA
+//     loads (one 16-row x 64-column box per block, K/V half and tensor; the
+//     cache is viewed as [num_blocks * num_kv_heads * 16 rows][128] with
+//     128-byte swizzle, which writes exactly the layout the MMAs read) whose
+//     bytes complete the stage's barrier.  The last tile, which may end inside
+//     a block, is copied with zero-filling 16-byte cp.async instead, because
+//     rows past the context may hold anything (even NaN) and P = 0 times NaN
+//     would still poison O.
+// The running max of a row is only moved when a tile maximum exceeds it by
+// more than 8 (log2 units), so P <= 256 and O is rarely rescaled; numerator
+// and denominator share the same reference, so the result is exact.
 //
-// Shared memory (all operands in the 128-byte-swizzled canonical layout:
-// 8-row atoms of 8 x 128 bytes, 16-byte chunk c of row r stored at chunk
-// c ^ (r % 8)):
-//   Q   : two 64-column halves of 128 rows                         (32 KB)
-//   K,V : five stages x (K, V) x two 64-column halves of 64 rows    (160 KB)
-//   P   : two buffers of 128 rows x 64 keys                         (32 KB)
-// K/V tiles are filled with 16-byte cp.async copies (zero-filled past the
-// needed keys).
+// TMEM columns (all 512): Q at [0,64) (bf16 pairs); S of team t at
+// 64 + 64t; O of team t at 192 + 128t; P of team t at 448 + 32t (bf16 pairs).
+// Shared memory holds only the K/V ring: six stages x (K, V) x two 64-column
+// halves of 64 rows (192 KB), in the 128-byte-swizzled canonical layout
+// (8-row atoms of 8 x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)).
 // Every wait on an mbarrier is bounded.  A thread whose wait expires records
 // the failure and carries on without waiting (its results are garbage), so
-// every arrival and pair barrier is still reached; the CTA then records
-// PKV_STATUS_INTERNAL, drains its copies, frees its TMEM and returns.
+// every arrival is still made; the CTA then records PKV_STATUS_INTERNAL,
+// drains its copies, frees its TMEM and returns.
 #include <math.h>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "prefill_common.cuh"
@@ -55,23 +69,21 @@ using pkv::PrefillParams;
 constexpr int D = 128;
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int kSoftmaxThreads = 256;
-constexpr int kThreads = kSoftmaxThreads + 32;  // + the MMA-issue warp
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kOCol = 128;  // S buffers at columns 0 and 64
-constexpr int kStages = 5;
+constexpr int kTeamThreads = 128;
+constexpr int kMmaWarp = 8, kLoadWarp0 = 9, kLoadWarps = 1;
+constexpr int kThreads = (kLoadWarp0 + kLoadWarps) * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kQCol = 0, kSCol = 64, kOCol = 192, kPCol = 448;
+constexpr int kStages = 6;
 
-constexpr int kQHalf = BM * 128;            // 16 KB: 128 rows x 64 bf16
 constexpr int kKVHalf = BN * 128;           // 8 KB: 64 rows x 64 bf16
 constexpr int kTileBytes = 2 * kKVHalf;     // one K or V tile (both halves)
 constexpr int kStageBytes = 2 * kTileBytes; // K + V
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + 2 * kQHalf;              // 32768
-constexpr int kPBytes = BM * BN * 2;                    // 16384
-constexpr int kOffP = kOffKV + kStages * kStageBytes;   // 196608
-constexpr int kOffBar = kOffP + 2 * kPBytes;            // 229376
-constexpr int kOffRed = kOffBar + 64;                   // [2][2][128] floats
-constexpr int kSmemBytes = kOffRed + 2 * 2 * BM * 4;
+constexpr int kOffKV = 0;
+constexpr int kOffBar = kOffKV + kStages * kStageBytes; // 196608
+constexpr int kNumBars = 2 * 4 + 2 * kStages + 1;       // per team: s, o, sfree, pfull; per stage: full, empty; go
+constexpr int kOffRed = kOffBar + kNumBars * 8 + 8;     // + TMEM address slot
+constexpr int kSmemBytes = kOffRed + 2 * 2 * BM * 4;    // [team][m, l][row]
 constexpr unsigned kWaitIters = 1u << 24;
 
 constexpr uint32_t kIdescS = pkv::tc::idesc_bf16_f32(BM, BN, false, false);
@@ -82,11 +94,11 @@ __device__ __forceinline__ int sw128(int r, int c16) {
 }
 
 template <typename OutT>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter, score-column half
-    const int row = quarter * 32 + lane;             // this thread's query row in the tile
     const int tile = blockIdx.x, kvh = blockIdx.y;
     const int s = gridDim.z - 1 - blockIdx.z;  // later (typically longer) sequences first
     const int G = p.group;
@@ -115,27 +127,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     const int j_first = (tile * BM) / G;
     const int mask_from = prior + j_first + 1;  // keys below this need no causal mask
 
-    uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + kOffBar);  // S(kt) done, per S buffer
-    uint64_t *bar_o = bar_s + 2;   // PV(kt) done
-    uint64_t *bar_p = bar_s + 3;   // P(kt) written and tile kt+2 landed, per P buffer
-    uint64_t *bar_go = bar_s + 5;  // Q, tiles 0 and 1 landed
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_s + 6);
-    // [parity][half][row]: half-row maxima exchanged between partner warps.
-    // Alternating by tile parity, a slot is rewritten only after the next pair
-    // barrier, by which time the partner has read it.
-    float *xmax = reinterpret_cast<float *>(smem + kOffRed);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *bar_s = bars;           // [team] S(t) computed
+    uint64_t *bar_o = bars + 2;       // [team] PV(t) done
+    uint64_t *bar_sfree = bars + 4;   // [team] the team has read S(t) (128 arrivals)
+    uint64_t *bar_pfull = bars + 6;   // [team] P(t) written (128 arrivals)
+    uint64_t *bar_full = bars + 8;    // [stage] K/V tile landed (32 loader arrivals)
+    uint64_t *bar_empty = bars + 8 + kStages;  // [stage] the PV reading it is done
+    uint64_t *bar_go = bars + 8 + 2 * kStages; // Q stored in TMEM (128 arrivals)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    float *red = reinterpret_cast<float *>(smem + kOffRed);  // [team][m, l][row]
 
     if (warp == 0) {
         pkv::tc::tmem_alloc(tmem_slot, kTmemCols);
         pkv::tc::tmem_relinquish();
     }
     if (tid == 0) {
-        pkv::tc::mbar_init(bar_s, 1);
-        pkv::tc::mbar_init(bar_s + 1, 1);
-        pkv::tc::mbar_init(bar_o, 1);
-        pkv::tc::mbar_init(bar_p, kSoftmaxThreads);
-        pkv::tc::mbar_init(bar_p + 1, kSoftmaxThreads);
-        pkv::tc::mbar_init(bar_go, kSoftmaxThreads);
+        for (int t = 0; t < 2; t++) {
+            pkv::tc::mbar_init(bar_s + t, 1);
+            pkv::tc::mbar_init(bar_o + t, 1);
+            pkv::tc::mbar_init(bar_sfree + t, kTeamThreads);
+            pkv::tc::mbar_init(bar_pfull + t, kTeamThreads);
+        }
+        for (int st = 0; st < kStages; st++) {
+            pkv::tc::mbar_init(bar_full + st, 1);
+            pkv::tc::mbar_init(bar_empty + st, 1);
+        }
+        pkv::tc::mbar_init(bar_go, kTeamThreads);
         pkv::tc::fence_mbar_init();
     }
 
@@ -144,165 +162,192 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     const unsigned char *vc = static_cast<const unsigned char *>(p.v_cache);
     const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
 
-    // physical ids of the 4 blocks holding keys [kt*64, kt*64 + 64)
-    auto tile_ids = [&](int kt, int (&ids)[4]) {
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int t = kt * BN + q * kBlock;
-            ids[q] = t < kv_end ? table[t / kBlock] : 0;
-        }
-    };
-    auto load_kv = [&](int kt, const int (&ids)[4]) {
-        unsigned char *kd = smem + kOffKV + (kt % kStages) * kStageBytes;
-        unsigned char *vd = kd + kTileBytes;
-#pragma unroll
-        for (int u = 0; u < 4; u++) {
-            const int i = tid + kSoftmaxThreads * u;
-            const int r = i >> 4, c = i & 15;  // r >> 4 == u
-            const int t = kt * BN + r;
-            int nb = 0;
-            size_t go = 0;
-            if (t < kv_end) {
-                const int phys = ids[u];
-                if (phys >= 0 && phys < p.num_blocks) {
-                    nb = 16;
-                    go = ((((size_t)phys * p.num_kv_heads + kvh) * kBlock + (t % kBlock)) * D) * 2 + c * 16;
-                } else if (c == 0 && (t % kBlock) == 0) {
-                    pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
-                }
-            }
-            const int off = (c >> 3) * kKVHalf + sw128(r, c & 7);
-            pkv::cp_async16(kd + off, kc + go, nb);
-            pkv::cp_async16(vd + off, vc + go, nb);
-        }
-    };
-
-    int ids_next[4];
-    if (warp < 8) {
-        // Q tile: 128 rows x 16 chunks, 8 copies per thread
-#pragma unroll
-        for (int u = 0; u < 8; u++) {
-            const int i = tid + kSoftmaxThreads * u;
-            const int r = i >> 4, c = i & 15;
-            const int R = tile * BM + r;
-            const int jr = R / G;
-            const bool ok = jr < n;
-            const __nv_bfloat16 *src =
-                ok ? qg + ((size_t)(q0 + jr) * p.num_q_heads + kvh * G + (R - jr * G)) * D + c * 8 : qg;
-            pkv::cp_async16(smem + kOffQ + (c >> 3) * kQHalf + sw128(r, c & 7), src, ok ? 16 : 0);
-        }
-
-        int ids[4];
-        tile_ids(0, ids);
-        load_kv(0, ids);  // same copy group as Q
-        pkv::cp_async_commit();
-#pragma unroll
-        for (int t = 1; t < kStages - 1; t++) {
-            tile_ids(t, ids);
-            if (t < nkt) load_kv(t, ids);
-            pkv::cp_async_commit();
-        }
-        tile_ids(kStages - 1, ids_next);
-    }
-
     pkv::tc::fence_before_sync();
     __syncthreads();
     pkv::tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
 
-    // S(kt) = Q K(kt)^T into S buffer kt & 1
-    auto issue_s = [&](int kt) {
-        const uint32_t qa = sbase + kOffQ;
-        const uint32_t kb = sbase + kOffKV + (kt % kStages) * kStageBytes;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ks++) {
-            const uint64_t a = pkv::tc::smem_desc_sw128(qa + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
-            const uint64_t b = pkv::tc::smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
-            pkv::tc::mma_ss(tmem + (kt & 1) * BN, a, b, kIdescS, ks > 0 ? 1u : 0u);
-        }
-        pkv::tc::mma_commit(bar_s + (kt & 1));
-    };
-    // O (+)= P(kt) V(kt)
-    auto issue_pv = [&](int kt) {
-        const uint32_t pa = sbase + kOffP + (kt & 1) * kPBytes;
-        const uint32_t vb = sbase + kOffKV + (kt % kStages) * kStageBytes + kTileBytes;
-#pragma unroll
-        for (int kq = 0; kq < BN / 16; kq++) {
-            const uint64_t a = pkv::tc::smem_desc_sw128(pa + kq * 32, 16, 1024);
-            // V is MN-major: next 64-column half at +8 KB (LBO), next 8 keys at +1 KB (SBO)
-            const uint64_t b = pkv::tc::smem_desc_sw128(vb + kq * 2048, kKVHalf, 1024);
-            pkv::tc::mma_ss(tmem + kOCol, a, b, kIdescPV, (kt == 0 && kq == 0) ? 0u : 1u);
-        }
-        pkv::tc::mma_commit(bar_o);
-    };
-
-    // this thread's query row (softmax warps)
-    const int R = tile * BM + row;
-    const int jrow = R / G;
-    const bool row_ok = jrow < n;
-    const int pos = row_ok ? prior + jrow : -1;
     bool failed = false;
     auto wait = [&](uint64_t *bar, unsigned parity) {
         if (!failed && !pkv::tc::mbar_wait(bar, parity, kWaitIters)) failed = true;
     };
-    auto pair_sync = [&]() {  // warps w and w+4 (same rows) meet on named barrier 1 + w
-        asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
-    };
 
-    if (warp == 8) {
+    if (warp >= kLoadWarp0) {
+        // ---------------- loader: K/V tile t -> stage t % kStages
+        const int box_rows = p.num_blocks * p.num_kv_heads * kBlock;  // rows of the 2-D view
+        for (int t = warp - kLoadWarp0; t < nkt; t += kLoadWarps) {
+            if (t >= kStages) wait(bar_empty + (t % kStages), (unsigned)((t / kStages - 1) & 1));
+            unsigned char *kd = smem + kOffKV + (t % kStages) * kStageBytes;
+            unsigned char *vd = kd + kTileBytes;
+            // physical ids of the 4 blocks holding keys [t*64, t*64 + 64)
+            int my_id = 0;
+            if (lane < 4 && t * BN + lane * kBlock < kv_end) my_id = table[t * 4 + lane];
+            if ((t + 1) * BN <= kv_end) {
+                // four whole blocks: TMA
+                int y = box_rows;  // out of range: the box reads as zeros
+                if (lane < 4) {
+                    if (my_id >= 0 && my_id < p.num_blocks)
+                        y = (my_id * p.num_kv_heads + kvh) * kBlock;
+                    else
+                        pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                }
+                int ys[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
+                if (lane == 0) {
+                    pkv::tc::mbar_arrive_expect_tx(bar_full + (t % kStages), kStageBytes);
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+#pragma unroll
+                        for (int h = 0; h < 2; h++) {
+                            pkv::tc::tma_load_2d(kd + h * kKVHalf + q * 2048, &tmap_k, h * 64, ys[q],
+                                                 bar_full + (t % kStages));
+                            pkv::tc::tma_load_2d(vd + h * kKVHalf + q * 2048, &tmap_v, h * 64, ys[q],
+                                                 bar_full + (t % kStages));
+                        }
+                    }
+                }
+            } else {
+                // the last tile may end inside a block: zero-filling copies
+#pragma unroll 4
+                for (int u = 0; u < 32; u++) {
+                    const int i = lane + 32 * u;
+                    const int r = i >> 4, c = i & 15;  // r >> 4 == u >> 3
+                    const int key = t * BN + r;
+                    const int phys = __shfl_sync(0xffffffffu, my_id, u >> 3);
+                    int nb = 0;
+                    size_t go = 0;
+                    if (key < kv_end) {
+                        if (phys >= 0 && phys < p.num_blocks) {
+                            nb = 16;
+                            go = ((((size_t)phys * p.num_kv_heads + kvh) * kBlock + (key % kBlock)) * D) * 2 + c * 16;
+                        } else if (c == 0 && (key % kBlock) == 0) {
+                            pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                        }
+                    }
+                    const int off = (c >> 3) * kKVHalf + sw128(r, c & 7);
+                    pkv::cp_async16(kd + off, kc + go, nb);
+                    pkv::cp_async16(vd + off, vc + go, nb);
+                }
+                pkv::cp_async_commit();
+                pkv::cp_async_wait<0>();
+                pkv::tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) pkv::tc::mbar_arrive(bar_full + (t % kStages));
+            }
+        }
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one lane)
         if (lane == 0) {
+            auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into the S buffer of team t & 1
+                wait(bar_full + (t % kStages), (unsigned)((t / kStages) & 1));
+                pkv::tc::fence_after_sync();
+                const uint32_t kb = sbase + kOffKV + (t % kStages) * kStageBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ks++) {  // 16 d-columns = 8 TMEM columns of Q
+                    const uint64_t b = pkv::tc::smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
+                    pkv::tc::mma_ts(tmem + kSCol + (t & 1) * BN, tmem + kQCol + ks * 8, b, kIdescS,
+                                    ks > 0 ? 1u : 0u);
+                }
+                pkv::tc::mma_commit(bar_s + (t & 1));
+            };
+            auto issue_pv = [&](int t) {  // O(team t & 1) (+)= P V(t)
+                const uint32_t vb = sbase + kOffKV + (t % kStages) * kStageBytes + kTileBytes;
+#pragma unroll
+                for (int kq = 0; kq < BN / 16; kq++) {  // 16 keys = 8 TMEM columns of P
+                    // V is MN-major: next 64-column half at +8 KB (LBO), next 8 keys at +1 KB (SBO)
+                    const uint64_t b = pkv::tc::smem_desc_sw128(vb + kq * 2048, kKVHalf, 1024);
+                    pkv::tc::mma_ts(tmem + kOCol + (t & 1) * D, tmem + kPCol + (t & 1) * (BN / 2) + kq * 8, b,
+                                    kIdescPV, (t < 2 && kq == 0) ? 0u : 1u);
+                }
+                pkv::tc::mma_commit(bar_o + (t & 1));
+                pkv::tc::mma_commit(bar_empty + (t % kStages));
+            };
             wait(bar_go, 0);
-            pkv::tc::fence_after_sync();
             issue_s(0);
             if (nkt > 1) issue_s(1);
-            for (int kt = 0; kt < nkt; kt++) {
-                wait(bar_p + (kt & 1), (unsigned)((kt >> 1) & 1));
+            for (int t = 0; t < nkt; t++) {
+                if (t + 2 < nkt) {
+                    wait(bar_sfree + (t & 1), (unsigned)((t >> 1) & 1));  // team read S(t)
+                    issue_s(t + 2);
+                }
+                wait(bar_pfull + (t & 1), (unsigned)((t >> 1) & 1));      // P(t) written
                 pkv::tc::fence_after_sync();
-                issue_pv(kt);
-                if (kt + 2 < nkt) issue_s(kt + 2);
+                issue_pv(t);
             }
         }
         __syncwarp();
     } else {
-        // ---------------- softmax warps
+        // ---------------- softmax teams
+        const int team = warp >> 2, quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t s_col = kSCol + (uint32_t)team * BN, o_col = kOCol + (uint32_t)team * D;
+        const uint32_t p_col = kPCol + (uint32_t)team * (BN / 2);
+        const int R = tile * BM + row;
+        const int jrow = R / G;
+        const bool row_ok = jrow < n;
+        const int pos = row_ok ? prior + jrow : -1;
         float m_used = -INFINITY, lsum = 0.f;
-        pkv::cp_async_wait<kStages - 3>();  // Q, tile 0 and tile 1 have landed
-        pkv::tc::fence_proxy_async_smem();
-        pkv::tc::mbar_arrive(bar_go);
 
-        for (int kt = 0; kt < nkt; kt++) {
-            // S(kt) done; it was issued after PV(kt-2), so that one is done too
-            wait(bar_s + (kt & 1), (unsigned)((kt >> 1) & 1));
+        if (team == 0) {
+            // this row of Q -> TMEM columns [0, 64) as bf16 pairs (zeros past the chunk)
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                qg + ((size_t)(q0 + jrow) * p.num_q_heads + kvh * G + (R - jrow * G)) * D);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                float v[32];
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const uint4 x = row_ok ? src[h * 8 + c] : make_uint4(0u, 0u, 0u, 0u);
+                    v[4 * c + 0] = __uint_as_float(x.x);
+                    v[4 * c + 1] = __uint_as_float(x.y);
+                    v[4 * c + 2] = __uint_as_float(x.z);
+                    v[4 * c + 3] = __uint_as_float(x.w);
+                }
+                pkv::tc::tmem_st32(t_lane + kQCol + h * 32, v);
+            }
+            pkv::tc::fence_before_sync();
+            pkv::tc::mbar_arrive(bar_go);
+        }
+
+        for (int t = team; t < nkt; t += 2) {
+            wait(bar_s + team, (unsigned)((t >> 1) & 1));
             pkv::tc::fence_after_sync();
+            float sv[64];
+            {
+                float a[32], b[32];
+                pkv::tc::tmem_ld32(t_lane + s_col, a);
+                pkv::tc::tmem_ld32(t_lane + s_col + 32, b);
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    sv[i] = a[i];
+                    sv[32 + i] = b[i];
+                }
+            }
+            pkv::tc::fence_before_sync();
+            pkv::tc::mbar_arrive(bar_sfree + team);  // S buffer may be overwritten by S(t+2)
 
-            // this thread's 32 raw scores (keys t0 + i)
-            float sv[32];
-            pkv::tc::tmem_ld32(t_lane + (kt & 1) * BN + half * 32, sv);
-            const int t0 = kt * BN + half * 32;
-            if (kt * BN + BN <= mask_from) {
+            const int t0 = t * BN;
+            if (t0 + BN <= mask_from) {
                 if (!row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 32; i++) sv[i] = -INFINITY;
+                    for (int i = 0; i < 64; i++) sv[i] = -INFINITY;
                 }
             } else {
                 const int lim = pos - t0;  // keys i <= lim are visible
 #pragma unroll
-                for (int i = 0; i < 32; i++) sv[i] = i <= lim ? sv[i] : -INFINITY;
+                for (int i = 0; i < 64; i++) sv[i] = i <= lim ? sv[i] : -INFINITY;
             }
-            float mx[8];
+            float mx[16];
 #pragma unroll
-            for (int i = 0; i < 8; i++)
-                mx[i] = fmaxf(fmaxf(sv[i], sv[i + 8]), fmaxf(sv[i + 16], sv[i + 24]));
+            for (int i = 0; i < 16; i++)
+                mx[i] = fmaxf(fmaxf(sv[i], sv[i + 16]), fmaxf(sv[i + 32], sv[i + 48]));
+#pragma unroll
+            for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], mx[i + 8]);
 #pragma unroll
             for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
-            float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            float *xm = xmax + (kt & 1) * 2 * BM;
-            xm[half * BM + row] = mraw;
-            pair_sync();
-            mraw = fmaxf(mraw, xm[(half ^ 1) * BM + row]);
-            const float mt = mraw * p.scale_log2;  // scale > 0 commutes with max; -inf stays
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
             const bool need = mt > m_used + 8.f;
             float alpha = 1.f;
             if (need) {
@@ -310,65 +355,74 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
                 lsum *= alpha;
                 m_used = mt;
             }
-            if (kt > 0 && __any_sync(0xffffffffu, need)) {
-                // rescaling O needs PV(kt-1) to have finished
-                wait(bar_o, (unsigned)((kt - 1) & 1));
+            // PV(t-2) (this team's previous PV) must be done before P and O are touched
+            if (t >= 2) {
+                wait(bar_o + team, (unsigned)(((t - 2) >> 1) & 1));
                 pkv::tc::fence_after_sync();
+                if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                for (int c = 0; c < D / 2; c += 32) {
-                    float o[32];
-                    pkv::tc::tmem_ld32(t_lane + kOCol + half * (D / 2) + c, o);
+                    for (int c = 0; c < D; c += 32) {
+                        float o[32];
+                        pkv::tc::tmem_ld32(t_lane + o_col + c, o);
 #pragma unroll
-                    for (int i = 0; i < 32; i++) o[i] *= alpha;
-                    pkv::tc::tmem_st32(t_lane + kOCol + half * (D / 2) + c, o);
+                        for (int i = 0; i < 32; i++) o[i] *= alpha;
+                        pkv::tc::tmem_st32(t_lane + o_col + c, o);
+                    }
                 }
             }
             const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-            unsigned char *prow = smem + kOffP + (kt & 1) * kPBytes;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            float pk[32];  // P row as 32 bf16 pairs (bit patterns)
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                float e[8];
-#pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    e[i] = pkv::tc::ex2(fmaf(sv[c * 8 + i], p.scale_log2, nbase));
-                    ls[i & 3] += e[i];
-                }
-                uint4 pk;
-                pk.x = pkv::pack_bf16(e[0], e[1]);
-                pk.y = pkv::pack_bf16(e[2], e[3]);
-                pk.z = pkv::pack_bf16(e[4], e[5]);
-                pk.w = pkv::pack_bf16(e[6], e[7]);
-                *reinterpret_cast<uint4 *>(prow + sw128(row, half * 4 + c)) = pk;
+            for (int i = 0; i < 32; i++) {
+                const float e0 = pkv::tc::ex2(fmaf(sv[2 * i], p.scale_log2, nbase));
+                const float e1 = pkv::tc::ex2(fmaf(sv[2 * i + 1], p.scale_log2, nbase));
+                ls[(2 * i) & 3] += e0;
+                ls[(2 * i + 1) & 3] += e1;
+                pk[i] = __uint_as_float(pkv::pack_bf16(e0, e1));
             }
+            pkv::tc::tmem_st32(t_lane + p_col, pk);
             lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // PV(kt-1) done frees stage (kt-1) % kStages: fetch tile kt+kStages-1 into it
-            if (kt > 0) wait(bar_o, (unsigned)((kt - 1) & 1));
-            if (kt + kStages - 1 < nkt) load_kv(kt + kStages - 1, ids_next);
-            pkv::cp_async_commit();
-            tile_ids(kt + kStages, ids_next);
-            pkv::cp_async_wait<kStages - 3>();  // every tile up to kt+2 has landed
-            pkv::tc::fence_proxy_async_smem();
             pkv::tc::fence_before_sync();
-            pkv::tc::mbar_arrive(bar_p + (kt & 1));
+            pkv::tc::mbar_arrive(bar_pfull + team);
         }
 
-        wait(bar_o, (unsigned)((nkt - 1) & 1));
-        pkv::tc::fence_after_sync();
-        float *xl = xmax + (nkt & 1) * 2 * BM;
-        xl[half * BM + row] = lsum;
-        pair_sync();
-        const float ltot = lsum + xl[(half ^ 1) * BM + row];
+        // merge the two teams: exchange (m, l) with the partner thread of the same row
+        const int my_tiles = nkt > team ? (nkt - team + 1) / 2 : 0;
+        if (my_tiles > 0) {
+            const int last = team + 2 * (my_tiles - 1);
+            wait(bar_o + team, (unsigned)((last >> 1) & 1));
+            pkv::tc::fence_after_sync();
+        }
+        red[(team * 2 + 0) * BM + row] = m_used;
+        red[(team * 2 + 1) * BM + row] = lsum;
+        asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
+        const float m0 = red[0 * BM + row], l0 = red[1 * BM + row];
+        const float m1 = red[2 * BM + row], l1 = red[3 * BM + row];
+        const float M = fmaxf(m0, m1);
+        const float f0 = M == -INFINITY ? 0.f : pkv::tc::ex2(m0 - M);
+        const float f1 = (M == -INFINITY || nkt < 2) ? 0.f : pkv::tc::ex2(m1 - M);
+        const float ltot = l0 * f0 + l1 * f1;
         const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+        const float g0 = f0 * inv, g1 = f1 * inv;
+        // team 0 writes output columns 0..63, team 1 columns 64..127
         OutT *orow = static_cast<OutT *>(p.out) +
-                     ((size_t)(q0 + jrow) * p.num_q_heads + kvh * G + (R - jrow * G)) * D + half * (D / 2);
+                     ((size_t)(q0 + jrow) * p.num_q_heads + kvh * G + (R - jrow * G)) * D + team * (D / 2);
 #pragma unroll 1
         for (int c = 0; c < D / 2; c += 32) {
-            float o[32];
-            pkv::tc::tmem_ld32(t_lane + kOCol + half * (D / 2) + c, o);
+            float a[32], b[32];
+            const uint32_t col = (uint32_t)(team * (D / 2) + c);
+            pkv::tc::tmem_ld32(t_lane + kOCol + col, a);
+            if (nkt >= 2) {
+                pkv::tc::tmem_ld32(t_lane + kOCol + D + col, b);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; i++) b[i] = 0.f;
+            }
             if (row_ok && !failed) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) pkv::store2(orow + c + i, o[i] * inv, o[i + 1] * inv);
+                for (int i = 0; i < 32; i += 2)
+                    pkv::store2(orow + c + i, a[i] * g0 + b[i] * g1, a[i + 1] * g0 + b[i + 1] * g1);
             }
         }
     }
@@ -388,7 +442,50 @@ namespace pkv {
 
 bool prefill_tc_supported(int dtype, int head_dim) { return dtype == PKV_BF16 && head_dim == D; }
 
+}  // namespace pkv
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// 2-D view of one cache: [num_blocks * num_kv_heads * 16 rows][128 columns]
+// bf16, boxes of 16 rows x 64 columns, 128-byte swizzle, zero fill.
+int make_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int num_kv_heads) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    if (!g_encode) return pkv::fail(PKV_ERR_CUDA, "prefill: cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_blocks * num_kv_heads * kBlock};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(cache), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return pkv::fail(PKV_ERR_CUDA, "prefill: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+}  // namespace
+
+namespace pkv {
+
 int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaStream_t st) {
+    if ((long long)p.num_blocks * p.num_kv_heads * kBlock > 0x7fffffffLL)
+        return fail(PKV_ERR_INVALID, "prefill: cache too large for 32-bit row coordinates");
+    CUtensorMap tk, tv;
+    int rc = make_cache_map(&tk, p.k_cache, p.num_blocks, p.num_kv_heads);
+    if (rc) return rc;
+    rc = make_cache_map(&tv, p.v_cache, p.num_blocks, p.num_kv_heads);
+    if (rc) return rc;
     static bool attr_set[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -405,9 +502,9 @@ int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaS
     const int tiles = (p.max_q_len * p.group + BM - 1) / BM;
     dim3 grid((unsigned)tiles, (unsigned)p.num_kv_heads, (unsigned)num_seqs);
     if (which == 0)
-        prefill_tc_kernel<float><<<grid, kThreads, kSmemBytes, st>>>(p);
+        prefill_tc_kernel<float><<<grid, kThreads, kSmemBytes, st>>>(p, tk, tv);
     else
-        prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(p);
+        prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(p, tk, tv);
     return check_launch("prefill_tc");
 }
 
