@@ -8,44 +8,47 @@
 // Work unit: one CTA per (tile of 128 packed query rows, kv head, sequence);
 // row r of the tile is query position R / G, head kvh*G + R % G
 // (R = tile*128 + r), so the G heads of a kv head share every K/V tile.
-//   S(t)  = Q K(t)^T : tcgen05.mma M=128, N=64 keys, K=d; A = Q (TMEM),
-//                      B = K (smem)
-//   O    += P(t) V(t): tcgen05.mma M=128, N=d, K=64 keys; A = P (TMEM),
+// Key tiles are 128 keys (8 cache blocks):
+//   S(t)  = Q K(t)^T : tcgen05.mma M=128, N=128, K=d; A = Q, B = K (smem)
+//   O    += P(t) V(t): tcgen05.mma M=128, N=d, K=128; A = P (TMEM),
 //                      B = V (smem, MN-major); accumulators in TMEM.
-// Keeping both A operands in tensor memory leaves shared-memory bandwidth to
-// the K and V tiles alone (an N=64 MMA that re-read Q from shared memory for
-// every tile was limited by shared-memory reads, not by the tensor core).
-// Warp roles (one CTA per SM, 10 warps):
+// A tcgen05.mma costs roughly the same to issue whatever its N, so tiles are
+// as wide as tensor memory allows.
+// Warp roles (one CTA per SM, 11 warps):
 //   * two softmax teams of 4 warps: team 0 takes key tiles 0, 2, 4, ..., team 1
-//     tiles 1, 3, 5, ...  Thread r of a team owns query row r (TMEM lane r): it
-//     reads its 64 scores with tcgen05.ld, masks, and runs the online softmax
-//     in registers (scale and max-subtraction fused into one multiply-add, exp2
-//     on the special-function unit), then stores its row of P (bf16 pairs)
-//     into the team's P columns of TMEM.  Each
-//     team has its own S buffer, P buffer, O accumulator and running (m, l);
-//     the two partial results are merged by log-sum-exp at the end.  The teams
-//     run independently, so one team's softmax overlaps the other's.
-//   * one MMA warp whose first lane issues S(t+2) as soon as the team has
-//     read S(t) out of TMEM, and PV(t) as soon as P(t) is written;
-//   * one loader warp that gathers K/V tiles through the block table into a
-//     6-stage ring, refilling a stage once the PV that last read it has
-//     finished.  A tile of four whole blocks is fetched with sixteen 2-D TMA
-//     loads (one 16-row x 64-column box per block, K/V half and tensor; the
-//     cache is viewed as [num_blocks * num_kv_heads * 16 rows][128] with
-//     128-byte swizzle, which writes exactly the layout the MMAs read) whose
-//     bytes complete the stage's barrier.  The last tile, which may end inside
-//     a block, is copied with zero-filling 16-byte cp.async instead, because
-//     rows past the context may hold anything (even NaN) and P = 0 times NaN
-//     would still poison O.
+//     tiles 1, 3, 5, ...  Thread r of a team owns query row r (TMEM lane r).
+//     In a first pass over its 128 scores (tcgen05.ld, 32 columns at a time) it
+//     finds the masked row maximum; in a second it computes
+//     p = 2^(s * scale * log2 e - m) (one multiply-add and ex2.approx per
+//     element) and stores P as bf16 pairs over the first 64 columns of the
+//     same S buffer.  Each team has its own S/P buffer, O accumulator and
+//     running (m, l); the two partial results are merged by log-sum-exp at
+//     the end.  The teams run independently, so one team's softmax overlaps
+//     the other team's MMAs.
+//   * one MMA warp whose first lane issues, per tile t, PV(t) as soon as P(t)
+//     is stored and then S(t+2) into the same team's buffer.  tcgen05.mma
+//     operations issued by one thread execute in order, so S(t+2) cannot
+//     overwrite P(t) before PV(t) has read it, and a team that sees S(t)
+//     complete also knows its previous PV is done.
+//   * two loader warps, one for K and one for V, that gather tiles through
+//     the block table: a tile of whole blocks with 2-D TMA boxes (one
+//     16-row x 64-column box per block and half; the cache is viewed as
+//     [num_blocks * num_kv_heads * 16 rows][128] with 128-byte swizzle, which
+//     writes exactly the layout the MMAs read); the last tile, which may end
+//     inside a block, with zero-filling 16-byte cp.async instead, because rows
+//     past the context may hold anything (even NaN) and P = 0 times NaN would
+//     still poison O.  K uses a 3-stage ring refilled when the S that read a
+//     stage has finished, V a 2-stage ring refilled when the PV has.
 // The running max of a row is only moved when a tile maximum exceeds it by
 // more than 8 (log2 units), so P <= 256 and O is rarely rescaled; numerator
 // and denominator share the same reference, so the result is exact.
 //
-// TMEM columns (all 512): Q at [0,64) (bf16 pairs); S of team t at
-// 64 + 64t; O of team t at 192 + 128t; P of team t at 448 + 32t (bf16 pairs).
-// Shared memory holds only the K/V ring: six stages x (K, V) x two 64-column
-// halves of 64 rows (192 KB), in the 128-byte-swizzled canonical layout
-// (8-row atoms of 8 x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)).
+// TMEM columns (all 512): S/P of team t at 128t, O of team t at 256 + 128t.
+// Shared memory, all in the 128-byte-swizzled canonical layout (8-row atoms
+// of 8 x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)):
+//   Q : two 64-column halves of 128 rows                       (32 KB)
+//   K : three stages x two 64-column halves of 128 rows        (96 KB)
+//   V : two stages x two 64-column halves of 128 rows          (64 KB)
 // Every wait on an mbarrier is bounded.  A thread whose wait expires records
 // the failure and carries on without waiting (its results are garbage), so
 // every arrival is still made; the CTA then records PKV_STATUS_INTERNAL,
@@ -68,22 +71,24 @@ using pkv::PrefillParams;
 
 constexpr int D = 128;
 constexpr int BM = 128;
-constexpr int BN = 64;
+constexpr int BN = 128;
 constexpr int kTeamThreads = 128;
-constexpr int kMmaWarp = 8, kLoadWarp0 = 9, kLoadWarps = 1;
-constexpr int kThreads = (kLoadWarp0 + kLoadWarps) * 32;
+constexpr int kMmaWarp = 8, kKLoadWarp = 9, kVLoadWarp = 10;
+constexpr int kThreads = 11 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kQCol = 0, kSCol = 64, kOCol = 192, kPCol = 448;
-constexpr int kStages = 6;
+constexpr uint32_t kOCol = 256;  // S/P of team t at 128t, O of team t at kOCol + 128t
+constexpr int kKStages = 3, kVStages = 2;
 
-constexpr int kKVHalf = BN * 128;           // 8 KB: 64 rows x 64 bf16
-constexpr int kTileBytes = 2 * kKVHalf;     // one K or V tile (both halves)
-constexpr int kStageBytes = 2 * kTileBytes; // K + V
-constexpr int kOffKV = 0;
-constexpr int kOffBar = kOffKV + kStages * kStageBytes; // 196608
-constexpr int kNumBars = 2 * 4 + 2 * kStages + 1;       // per team: s, o, sfree, pfull; per stage: full, empty; go
-constexpr int kOffRed = kOffBar + kNumBars * 8 + 8;     // + TMEM address slot
-constexpr int kSmemBytes = kOffRed + 2 * 2 * BM * 4;    // [team][m, l][row]
+constexpr int kHalf = 128 * 128;             // 16 KB: 128 rows x 64 bf16
+constexpr int kTile = 2 * kHalf;             // 32 KB: 128 rows x 128 bf16
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;                     // 32768
+constexpr int kOffV = kOffK + kKStages * kTile;          // 131072
+constexpr int kOffBar = kOffV + kVStages * kTile;        // 196608
+// barriers: per team s, o, pfull (6); K full/empty (6); V full/empty (4); go (1)
+constexpr int kNumBars = 6 + 2 * kKStages + 2 * kVStages + 1;
+constexpr int kOffRed = kOffBar + kNumBars * 8 + 8;      // + TMEM address slot
+constexpr int kSmemBytes = kOffRed + 2 * 2 * BM * 4;     // [team][m, l][row]
 constexpr unsigned kWaitIters = 1u << 24;
 
 constexpr uint32_t kIdescS = pkv::tc::idesc_bf16_f32(BM, BN, false, false);
@@ -128,13 +133,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mask_from = prior + j_first + 1;  // keys below this need no causal mask
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *bar_s = bars;           // [team] S(t) computed
+    uint64_t *bar_s = bars;           // [team] S(t) computed (and the team's PV(t-2) done)
     uint64_t *bar_o = bars + 2;       // [team] PV(t) done
-    uint64_t *bar_sfree = bars + 4;   // [team] the team has read S(t) (128 arrivals)
-    uint64_t *bar_pfull = bars + 6;   // [team] P(t) written (128 arrivals)
-    uint64_t *bar_full = bars + 8;    // [stage] K/V tile landed (32 loader arrivals)
-    uint64_t *bar_empty = bars + 8 + kStages;  // [stage] the PV reading it is done
-    uint64_t *bar_go = bars + 8 + 2 * kStages; // Q stored in TMEM (128 arrivals)
+    uint64_t *bar_pfull = bars + 4;   // [team] P(t) stored (128 arrivals)
+    uint64_t *bar_kfull = bars + 6;   // [stage] K tile landed
+    uint64_t *bar_kempty = bar_kfull + kKStages;   // [stage] the S reading it is done
+    uint64_t *bar_vfull = bar_kempty + kKStages;   // [stage] V tile landed
+    uint64_t *bar_vempty = bar_vfull + kVStages;   // [stage] the PV reading it is done
+    uint64_t *bar_go = bar_vempty + kVStages;      // Q landed (256 arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     float *red = reinterpret_cast<float *>(smem + kOffRed);  // [team][m, l][row]
 
@@ -146,21 +152,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; t++) {
             pkv::tc::mbar_init(bar_s + t, 1);
             pkv::tc::mbar_init(bar_o + t, 1);
-            pkv::tc::mbar_init(bar_sfree + t, kTeamThreads);
             pkv::tc::mbar_init(bar_pfull + t, kTeamThreads);
         }
-        for (int st = 0; st < kStages; st++) {
-            pkv::tc::mbar_init(bar_full + st, 1);
-            pkv::tc::mbar_init(bar_empty + st, 1);
+        for (int st = 0; st < kKStages; st++) {
+            pkv::tc::mbar_init(bar_kfull + st, 1);
+            pkv::tc::mbar_init(bar_kempty + st, 1);
         }
-        pkv::tc::mbar_init(bar_go, kTeamThreads);
+        for (int st = 0; st < kVStages; st++) {
+            pkv::tc::mbar_init(bar_vfull + st, 1);
+            pkv::tc::mbar_init(bar_vempty + st, 1);
+        }
+        pkv::tc::mbar_init(bar_go, 2 * kTeamThreads);
         pkv::tc::fence_mbar_init();
     }
 
     const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
-    const unsigned char *kc = static_cast<const unsigned char *>(p.k_cache);
-    const unsigned char *vc = static_cast<const unsigned char *>(p.v_cache);
     const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
+
+    if (warp < 8) {
+        // Q tile: 128 rows x 16 chunks, 8 copies per softmax thread
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int i = tid + 2 * kTeamThreads * u;
+            const int r = i >> 4, c = i & 15;
+            const int R = tile * BM + r;
+            const int jr = R / G;
+            const bool ok = jr < n;
+            const __nv_bfloat16 *src =
+                ok ? qg + ((size_t)(q0 + jr) * p.num_q_heads + kvh * G + (R - jr * G)) * D + c * 8 : qg;
+            pkv::cp_async16(smem + kOffQ + (c >> 3) * kHalf + sw128(r, c & 7), src, ok ? 16 : 0);
+        }
+        pkv::cp_async_commit();
+    }
 
     pkv::tc::fence_before_sync();
     __syncthreads();
@@ -172,45 +195,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!failed && !pkv::tc::mbar_wait(bar, parity, kWaitIters)) failed = true;
     };
 
-    if (warp >= kLoadWarp0) {
-        // ---------------- loader: K/V tile t -> stage t % kStages
+    if (warp == kKLoadWarp || warp == kVLoadWarp) {
+        // ---------------- loaders: K tile t -> K stage t % 3, V tile t -> V stage t % 2
+        const bool is_k = warp == kKLoadWarp;
+        const int nst = is_k ? kKStages : kVStages;
+        uint64_t *full = is_k ? bar_kfull : bar_vfull;
+        uint64_t *empty = is_k ? bar_kempty : bar_vempty;
+        const void *tmap = is_k ? static_cast<const void *>(&tmap_k) : static_cast<const void *>(&tmap_v);
+        const unsigned char *cache = static_cast<const unsigned char *>(is_k ? p.k_cache : p.v_cache);
         const int box_rows = p.num_blocks * p.num_kv_heads * kBlock;  // rows of the 2-D view
-        for (int t = warp - kLoadWarp0; t < nkt; t += kLoadWarps) {
-            if (t >= kStages) wait(bar_empty + (t % kStages), (unsigned)((t / kStages - 1) & 1));
-            unsigned char *kd = smem + kOffKV + (t % kStages) * kStageBytes;
-            unsigned char *vd = kd + kTileBytes;
-            // physical ids of the 4 blocks holding keys [t*64, t*64 + 64)
+        for (int t = 0; t < nkt; t++) {
+            const int st = t % nst;
+            if (t >= nst) wait(empty + st, (unsigned)((t / nst - 1) & 1));
+            unsigned char *dst = smem + (is_k ? kOffK : kOffV) + st * kTile;
+            // physical ids of the 8 blocks holding keys [t*128, t*128 + 128)
             int my_id = 0;
-            if (lane < 4 && t * BN + lane * kBlock < kv_end) my_id = table[t * 4 + lane];
+            if (lane < 8 && t * BN + lane * kBlock < kv_end) my_id = table[t * 8 + lane];
             if ((t + 1) * BN <= kv_end) {
-                // four whole blocks: TMA
+                // eight whole blocks: TMA
                 int y = box_rows;  // out of range: the box reads as zeros
-                if (lane < 4) {
+                if (lane < 8) {
                     if (my_id >= 0 && my_id < p.num_blocks)
                         y = (my_id * p.num_kv_heads + kvh) * kBlock;
                     else
                         pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
                 }
-                int ys[4];
+                int ys[8];
 #pragma unroll
-                for (int q = 0; q < 4; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
+                for (int q = 0; q < 8; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
                 if (lane == 0) {
-                    pkv::tc::mbar_arrive_expect_tx(bar_full + (t % kStages), kStageBytes);
+                    pkv::tc::mbar_arrive_expect_tx(full + st, kTile);
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
+                    for (int q = 0; q < 8; q++) {
 #pragma unroll
-                        for (int h = 0; h < 2; h++) {
-                            pkv::tc::tma_load_2d(kd + h * kKVHalf + q * 2048, &tmap_k, h * 64, ys[q],
-                                                 bar_full + (t % kStages));
-                            pkv::tc::tma_load_2d(vd + h * kKVHalf + q * 2048, &tmap_v, h * 64, ys[q],
-                                                 bar_full + (t % kStages));
-                        }
+                        for (int h = 0; h < 2; h++)
+                            pkv::tc::tma_load_2d(dst + h * kHalf + q * 2048, tmap, h * 64, ys[q], full + st);
                     }
                 }
             } else {
                 // the last tile may end inside a block: zero-filling copies
 #pragma unroll 4
-                for (int u = 0; u < 32; u++) {
+                for (int u = 0; u < 64; u++) {
                     const int i = lane + 32 * u;
                     const int r = i >> 4, c = i & 15;  // r >> 4 == u >> 3
                     const int key = t * BN + r;
@@ -225,55 +250,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
                         }
                     }
-                    const int off = (c >> 3) * kKVHalf + sw128(r, c & 7);
-                    pkv::cp_async16(kd + off, kc + go, nb);
-                    pkv::cp_async16(vd + off, vc + go, nb);
+                    pkv::cp_async16(dst + (c >> 3) * kHalf + sw128(r, c & 7), cache + go, nb);
                 }
                 pkv::cp_async_commit();
                 pkv::cp_async_wait<0>();
                 pkv::tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) pkv::tc::mbar_arrive(bar_full + (t % kStages));
+                if (lane == 0) pkv::tc::mbar_arrive(full + st);
             }
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one lane)
         if (lane == 0) {
-            auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into the S buffer of team t & 1
-                wait(bar_full + (t % kStages), (unsigned)((t / kStages) & 1));
+            auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into the S/P buffer of team t & 1
+                wait(bar_kfull + (t % kKStages), (unsigned)((t / kKStages) & 1));
                 pkv::tc::fence_after_sync();
-                const uint32_t kb = sbase + kOffKV + (t % kStages) * kStageBytes;
+                const uint32_t qa = sbase + kOffQ;
+                const uint32_t kb = sbase + kOffK + (t % kKStages) * kTile;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ks++) {  // 16 d-columns = 8 TMEM columns of Q
-                    const uint64_t b = pkv::tc::smem_desc_sw128(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
-                    pkv::tc::mma_ts(tmem + kSCol + (t & 1) * BN, tmem + kQCol + ks * 8, b, kIdescS,
-                                    ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < D / 16; ks++) {
+                    const uint64_t a = pkv::tc::smem_desc_sw128(qa + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
+                    const uint64_t b = pkv::tc::smem_desc_sw128(kb + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
+                    pkv::tc::mma_ss(tmem + (t & 1) * BN, a, b, kIdescS, ks > 0 ? 1u : 0u);
                 }
+                pkv::tc::mma_commit(bar_kempty + (t % kKStages));
                 pkv::tc::mma_commit(bar_s + (t & 1));
             };
-            auto issue_pv = [&](int t) {  // O(team t & 1) (+)= P V(t)
-                const uint32_t vb = sbase + kOffKV + (t % kStages) * kStageBytes + kTileBytes;
+            auto issue_pv = [&](int t) {  // O(team t & 1) (+)= P(t) V(t)
+                wait(bar_vfull + (t % kVStages), (unsigned)((t / kVStages) & 1));
+                pkv::tc::fence_after_sync();
+                const uint32_t vb = sbase + kOffV + (t % kVStages) * kTile;
 #pragma unroll
                 for (int kq = 0; kq < BN / 16; kq++) {  // 16 keys = 8 TMEM columns of P
-                    // V is MN-major: next 64-column half at +8 KB (LBO), next 8 keys at +1 KB (SBO)
-                    const uint64_t b = pkv::tc::smem_desc_sw128(vb + kq * 2048, kKVHalf, 1024);
-                    pkv::tc::mma_ts(tmem + kOCol + (t & 1) * D, tmem + kPCol + (t & 1) * (BN / 2) + kq * 8, b,
-                                    kIdescPV, (t < 2 && kq == 0) ? 0u : 1u);
+                    // V is MN-major: next 64-column half at +16 KB (LBO), next 8 keys at +1 KB (SBO)
+                    const uint64_t b = pkv::tc::smem_desc_sw128(vb + kq * 2048, kHalf, 1024);
+                    pkv::tc::mma_ts(tmem + kOCol + (t & 1) * D, tmem + (t & 1) * BN + kq * 8, b, kIdescPV,
+                                    (t < 2 && kq == 0) ? 0u : 1u);
                 }
+                pkv::tc::mma_commit(bar_vempty + (t % kVStages));
                 pkv::tc::mma_commit(bar_o + (t & 1));
-                pkv::tc::mma_commit(bar_empty + (t % kStages));
             };
             wait(bar_go, 0);
             issue_s(0);
             if (nkt > 1) issue_s(1);
             for (int t = 0; t < nkt; t++) {
-                if (t + 2 < nkt) {
-                    wait(bar_sfree + (t & 1), (unsigned)((t >> 1) & 1));  // team read S(t)
-                    issue_s(t + 2);
-                }
-                wait(bar_pfull + (t & 1), (unsigned)((t >> 1) & 1));      // P(t) written
+                wait(bar_pfull + (t & 1), (unsigned)((t >> 1) & 1));  // P(t) stored
                 pkv::tc::fence_after_sync();
                 issue_pv(t);
+                if (t + 2 < nkt) issue_s(t + 2);
             }
         }
         __syncwarp();
@@ -282,72 +306,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int team = warp >> 2, quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t s_col = kSCol + (uint32_t)team * BN, o_col = kOCol + (uint32_t)team * D;
-        const uint32_t p_col = kPCol + (uint32_t)team * (BN / 2);
+        const uint32_t s_col = (uint32_t)team * BN, o_col = kOCol + (uint32_t)team * D;
         const int R = tile * BM + row;
         const int jrow = R / G;
         const bool row_ok = jrow < n;
         const int pos = row_ok ? prior + jrow : -1;
         float m_used = -INFINITY, lsum = 0.f;
 
-        if (team == 0) {
-            // this row of Q -> TMEM columns [0, 64) as bf16 pairs (zeros past the chunk)
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                qg + ((size_t)(q0 + jrow) * p.num_q_heads + kvh * G + (R - jrow * G)) * D);
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-                float v[32];
-#pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    const uint4 x = row_ok ? src[h * 8 + c] : make_uint4(0u, 0u, 0u, 0u);
-                    v[4 * c + 0] = __uint_as_float(x.x);
-                    v[4 * c + 1] = __uint_as_float(x.y);
-                    v[4 * c + 2] = __uint_as_float(x.z);
-                    v[4 * c + 3] = __uint_as_float(x.w);
-                }
-                pkv::tc::tmem_st32(t_lane + kQCol + h * 32, v);
-            }
-            pkv::tc::fence_before_sync();
-            pkv::tc::mbar_arrive(bar_go);
-        }
+        pkv::cp_async_wait<0>();  // this thread's Q copies
+        pkv::tc::fence_proxy_async_smem();
+        pkv::tc::mbar_arrive(bar_go);
 
         for (int t = team; t < nkt; t += 2) {
+            // S(t) done; the team's PV(t-2), issued before it, is done too
             wait(bar_s + team, (unsigned)((t >> 1) & 1));
             pkv::tc::fence_after_sync();
-            float sv[64];
-            {
-                float a[32], b[32];
-                pkv::tc::tmem_ld32(t_lane + s_col, a);
-                pkv::tc::tmem_ld32(t_lane + s_col + 32, b);
-#pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    sv[i] = a[i];
-                    sv[32 + i] = b[i];
-                }
-            }
-            pkv::tc::fence_before_sync();
-            pkv::tc::mbar_arrive(bar_sfree + team);  // S buffer may be overwritten by S(t+2)
+            const bool full_tile = t * BN + BN <= mask_from;
+            const int lim0 = pos - t * BN;  // keys i <= lim0 of this tile are visible
 
-            const int t0 = t * BN;
-            if (t0 + BN <= mask_from) {
-                if (!row_ok) {
+            // pass 1: masked row maximum of the raw scores
+            float mraw = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                float sv[32];
+                pkv::tc::tmem_ld32(t_lane + s_col + c, sv);
+                float mx[8];
 #pragma unroll
-                    for (int i = 0; i < 64; i++) sv[i] = -INFINITY;
+                for (int i = 0; i < 8; i++) {
+                    float a0 = sv[i], a1 = sv[i + 8], a2 = sv[i + 16], a3 = sv[i + 24];
+                    if (!full_tile) {
+                        a0 = c + i <= lim0 ? a0 : -INFINITY;
+                        a1 = c + i + 8 <= lim0 ? a1 : -INFINITY;
+                        a2 = c + i + 16 <= lim0 ? a2 : -INFINITY;
+                        a3 = c + i + 24 <= lim0 ? a3 : -INFINITY;
+                    }
+                    mx[i] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
                 }
-            } else {
-                const int lim = pos - t0;  // keys i <= lim are visible
 #pragma unroll
-                for (int i = 0; i < 64; i++) sv[i] = i <= lim ? sv[i] : -INFINITY;
+                for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
+                mraw = fmaxf(mraw, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
             }
-            float mx[16];
-#pragma unroll
-            for (int i = 0; i < 16; i++)
-                mx[i] = fmaxf(fmaxf(sv[i], sv[i + 16]), fmaxf(sv[i + 32], sv[i + 48]));
-#pragma unroll
-            for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], mx[i + 8]);
-#pragma unroll
-            for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+            if (!row_ok) mraw = -INFINITY;
+            const float mt = mraw * p.scale_log2;  // scale > 0 commutes with max; -inf stays
             const bool need = mt > m_used + 8.f;
             float alpha = 1.f;
             if (need) {
@@ -355,33 +355,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lsum *= alpha;
                 m_used = mt;
             }
-            // PV(t-2) (this team's previous PV) must be done before P and O are touched
-            if (t >= 2) {
-                wait(bar_o + team, (unsigned)(((t - 2) >> 1) & 1));
-                pkv::tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, need)) {
+            if (t >= 2 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        float o[32];
-                        pkv::tc::tmem_ld32(t_lane + o_col + c, o);
+                for (int c = 0; c < D; c += 32) {
+                    float o[32];
+                    pkv::tc::tmem_ld32(t_lane + o_col + c, o);
 #pragma unroll
-                        for (int i = 0; i < 32; i++) o[i] *= alpha;
-                        pkv::tc::tmem_st32(t_lane + o_col + c, o);
-                    }
+                    for (int i = 0; i < 32; i++) o[i] *= alpha;
+                    pkv::tc::tmem_st32(t_lane + o_col + c, o);
                 }
             }
+            // pass 2: P = 2^(s * scale - m) as bf16 pairs over the first 64 columns
             const float nbase = m_used == -INFINITY ? 0.f : -m_used;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            float pk[32];  // P row as 32 bf16 pairs (bit patterns)
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 64) {
+                float a[32], b[32], pk[32];
+                pkv::tc::tmem_ld32(t_lane + s_col + c, a);
+                pkv::tc::tmem_ld32(t_lane + s_col + c + 32, b);
 #pragma unroll
-            for (int i = 0; i < 32; i++) {
-                const float e0 = pkv::tc::ex2(fmaf(sv[2 * i], p.scale_log2, nbase));
-                const float e1 = pkv::tc::ex2(fmaf(sv[2 * i + 1], p.scale_log2, nbase));
-                ls[(2 * i) & 3] += e0;
-                ls[(2 * i + 1) & 3] += e1;
-                pk[i] = __uint_as_float(pkv::pack_bf16(e0, e1));
+                for (int i = 0; i < 16; i++) {
+                    float x0 = a[2 * i], x1 = a[2 * i + 1];
+                    float y0 = b[2 * i], y1 = b[2 * i + 1];
+                    if (!full_tile || !row_ok) {
+                        x0 = c + 2 * i <= lim0 ? x0 : -INFINITY;
+                        x1 = c + 2 * i + 1 <= lim0 ? x1 : -INFINITY;
+                        y0 = c + 32 + 2 * i <= lim0 ? y0 : -INFINITY;
+                        y1 = c + 33 + 2 * i <= lim0 ? y1 : -INFINITY;
+                    }
+                    const float e0 = pkv::tc::ex2(fmaf(x0, p.scale_log2, nbase));
+                    const float e1 = pkv::tc::ex2(fmaf(x1, p.scale_log2, nbase));
+                    const float f0 = pkv::tc::ex2(fmaf(y0, p.scale_log2, nbase));
+                    const float f1 = pkv::tc::ex2(fmaf(y1, p.scale_log2, nbase));
+                    ls[0] += e0;
+                    ls[1] += e1;
+                    ls[2] += f0;
+                    ls[3] += f1;
+                    pk[i] = __uint_as_float(pkv::pack_bf16(e0, e1));
+                    pk[16 + i] = __uint_as_float(pkv::pack_bf16(f0, f1));
+                }
+                // keys c .. c+63 -> P columns c/2 .. c/2+31 (those scores are already read)
+                pkv::tc::tmem_st32(t_lane + s_col + c / 2, pk);
             }
-            pkv::tc::tmem_st32(t_lane + p_col, pk);
             lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             pkv::tc::fence_before_sync();
             pkv::tc::mbar_arrive(bar_pfull + team);
