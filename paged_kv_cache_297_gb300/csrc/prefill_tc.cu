@@ -17,11 +17,11 @@
 // Warp roles (one CTA per SM, 11 warps):
 //   * two softmax teams of 4 warps: team 0 takes key tiles 0, 2, 4, ..., team 1
 //     tiles 1, 3, 5, ...  Thread r of a team owns query row r (TMEM lane r).
-//     In a first pass over its 128 scores (tcgen05.ld, 32 columns at a time) it
-//     finds the masked row maximum; in a second it computes
-//     p = 2^(s * scale * log2 e - m) (one multiply-add and ex2.approx per
-//     element) and stores P as bf16 pairs over the first 64 columns of the
-//     same S buffer.  Each team has its own S/P buffer, O accumulator and
+//     It reads its 128 scores with one tcgen05.ld, masks them, finds the row
+//     maximum, computes p = 2^(s * scale * log2 e - m) (one multiply-add per
+//     element; a quarter of the powers on the FMA pipe with a polynomial, the
+//     rest with ex2.approx on the special-function unit) and stores P as bf16
+//     pairs over the first 64 columns of the same S buffer.  Each team has its own S/P buffer, O accumulator and
 //     running (m, l); the two partial results are merged by log-sum-exp at
 //     the end.  The teams run independently, so one team's softmax overlaps
 //     the other team's MMAs.
@@ -324,28 +324,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool full_tile = t * BN + BN <= mask_from;
             const int lim0 = pos - t * BN;  // keys i <= lim0 of this tile are visible
 
-            // pass 1: masked row maximum of the raw scores
-            float mraw = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                float sv[32];
-                pkv::tc::tmem_ld32(t_lane + s_col + c, sv);
-                float mx[8];
+            // all 128 raw scores of this row, masked
+            float sv[128];
+            pkv::tc::tmem_ld128(t_lane + s_col, sv);
+            if (!full_tile || !row_ok) {
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    float a0 = sv[i], a1 = sv[i + 8], a2 = sv[i + 16], a3 = sv[i + 24];
-                    if (!full_tile) {
-                        a0 = c + i <= lim0 ? a0 : -INFINITY;
-                        a1 = c + i + 8 <= lim0 ? a1 : -INFINITY;
-                        a2 = c + i + 16 <= lim0 ? a2 : -INFINITY;
-                        a3 = c + i + 24 <= lim0 ? a3 : -INFINITY;
-                    }
-                    mx[i] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-                }
-#pragma unroll
-                for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
-                mraw = fmaxf(mraw, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
+                for (int i = 0; i < 128; i++) sv[i] = i <= lim0 ? sv[i] : -INFINITY;
             }
+            float mx[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++)
+                mx[i] = fmaxf(fmaxf(fmaxf(sv[i], sv[i + 16]), fmaxf(sv[i + 32], sv[i + 48])),
+                              fmaxf(fmaxf(sv[i + 64], sv[i + 80]), fmaxf(sv[i + 96], sv[i + 112])));
+#pragma unroll
+            for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], mx[i + 8]);
+#pragma unroll
+            for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
+            float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             if (!row_ok) mraw = -INFINITY;
             const float mt = mraw * p.scale_log2;  // scale > 0 commutes with max; -inf stays
             const bool need = mt > m_used + 8.f;
@@ -365,36 +360,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pkv::tc::tmem_st32(t_lane + o_col + c, o);
                 }
             }
-            // pass 2: P = 2^(s * scale - m) as bf16 pairs over the first 64 columns
+            // P = 2^(s * scale - m) as bf16 pairs over the first 64 columns
             const float nbase = m_used == -INFINITY ? 0.f : -m_used;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 64) {
-                float a[32], b[32], pk[32];
-                pkv::tc::tmem_ld32(t_lane + s_col + c, a);
-                pkv::tc::tmem_ld32(t_lane + s_col + c + 32, b);
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    float x0 = a[2 * i], x1 = a[2 * i + 1];
-                    float y0 = b[2 * i], y1 = b[2 * i + 1];
-                    if (!full_tile || !row_ok) {
-                        x0 = c + 2 * i <= lim0 ? x0 : -INFINITY;
-                        x1 = c + 2 * i + 1 <= lim0 ? x1 : -INFINITY;
-                        y0 = c + 32 + 2 * i <= lim0 ? y0 : -INFINITY;
-                        y1 = c + 33 + 2 * i <= lim0 ? y1 : -INFINITY;
-                    }
-                    const float e0 = pkv::tc::ex2(fmaf(x0, p.scale_log2, nbase));
-                    const float e1 = pkv::tc::ex2(fmaf(x1, p.scale_log2, nbase));
-                    const float f0 = pkv::tc::ex2(fmaf(y0, p.scale_log2, nbase));
-                    const float f1 = pkv::tc::ex2(fmaf(y1, p.scale_log2, nbase));
-                    ls[0] += e0;
-                    ls[1] += e1;
-                    ls[2] += f0;
-                    ls[3] += f1;
+            for (int c = 0; c < BN; c += 64) {
+                float pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    const float x0 = fmaf(sv[c + 2 * i], p.scale_log2, nbase);
+                    const float x1 = fmaf(sv[c + 2 * i + 1], p.scale_log2, nbase);
+                    // one pair in four on the FMA pipe, the rest on the special-function unit
+                    const float e0 = (i & 3) == 3 ? pkv::tc::exp2_poly(x0) : pkv::tc::ex2(x0);
+                    const float e1 = (i & 3) == 3 ? pkv::tc::exp2_poly(x1) : pkv::tc::ex2(x1);
+                    ls[(2 * i) & 3] += e0;
+                    ls[(2 * i + 1) & 3] += e1;
                     pk[i] = __uint_as_float(pkv::pack_bf16(e0, e1));
-                    pk[16 + i] = __uint_as_float(pkv::pack_bf16(f0, f1));
                 }
-                // keys c .. c+63 -> P columns c/2 .. c/2+31 (those scores are already read)
+                // keys c .. c+63 -> P columns c/2 .. c/2+31
                 pkv::tc::tmem_st32(t_lane + s_col + c / 2, pk);
             }
             lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
