@@ -37,8 +37,9 @@
 //     writes exactly the layout the MMAs read); the last tile, which may end
 //     inside a block, with zero-filling 16-byte cp.async instead, because rows
 //     past the context may hold anything (even NaN) and P = 0 times NaN would
-//     still poison O.  K uses a 3-stage ring refilled when the S that read a
-//     stage has finished, V a 2-stage ring refilled when the PV has.
+//     still poison O.  K uses a 2-stage ring refilled when the S that read a
+//     stage has finished, V a 3-stage ring refilled when the PV has (K(t) is
+//     needed two tiles before V(t), so both get about the same lead).
 // The running max of a row is only moved when a tile maximum exceeds it by
 // more than 8 (log2 units), so P <= 256 and O is rarely rescaled; numerator
 // and denominator share the same reference, so the result is exact.
@@ -47,8 +48,8 @@
 // Shared memory, all in the 128-byte-swizzled canonical layout (8-row atoms
 // of 8 x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)):
 //   Q : two 64-column halves of 128 rows                       (32 KB)
-//   K : three stages x two 64-column halves of 128 rows        (96 KB)
-//   V : two stages x two 64-column halves of 128 rows          (64 KB)
+//   K : two stages x two 64-column halves of 128 rows          (64 KB)
+//   V : three stages x two 64-column halves of 128 rows        (96 KB)
 // Every wait on an mbarrier is bounded.  A thread whose wait expires records
 // the failure and carries on without waiting (its results are garbage), so
 // every arrival is still made; the CTA then records PKV_STATUS_INTERNAL,
@@ -77,13 +78,13 @@ constexpr int kMmaWarp = 8, kKLoadWarp = 9, kVLoadWarp = 10;
 constexpr int kThreads = 11 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;  // S/P of team t at 128t, O of team t at kOCol + 128t
-constexpr int kKStages = 3, kVStages = 2;
+constexpr int kKStages = 2, kVStages = 3;
 
 constexpr int kHalf = 128 * 128;             // 16 KB: 128 rows x 64 bf16
 constexpr int kTile = 2 * kHalf;             // 32 KB: 128 rows x 128 bf16
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTile;                     // 32768
-constexpr int kOffV = kOffK + kKStages * kTile;          // 131072
+constexpr int kOffV = kOffK + kKStages * kTile;          // 98304
 constexpr int kOffBar = kOffV + kVStages * kTile;        // 196608
 // barriers: per team s, o, pfull (6); K full/empty (6); V full/empty (4); go (1)
 constexpr int kNumBars = 6 + 2 * kKStages + 2 * kVStages + 1;
@@ -144,10 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     float *red = reinterpret_cast<float *>(smem + kOffRed);  // [team][m, l][row]
 
-    if (warp == 0) {
-        pkv::tc::tmem_alloc(tmem_slot, kTmemCols);
-        pkv::tc::tmem_relinquish();
-    }
     if (tid == 0) {
         for (int t = 0; t < 2; t++) {
             pkv::tc::mbar_init(bar_s + t, 1);
@@ -165,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pkv::tc::mbar_init(bar_go, 2 * kTeamThreads);
         pkv::tc::fence_mbar_init();
     }
+    __syncthreads();  // barriers initialised: the loaders can start right away
 
     const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
     const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
@@ -185,10 +183,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         pkv::cp_async_commit();
     }
 
-    pkv::tc::fence_before_sync();
-    __syncthreads();
-    pkv::tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
+    // TMEM for every warp but the loaders (which never touch it); they meet on
+    // named barrier 5 so that the loaders need not wait for the allocation
+    uint32_t tmem = 0;
+    if (warp < kKLoadWarp) {
+        if (warp == 0) {
+            pkv::tc::tmem_alloc(tmem_slot, kTmemCols);
+            pkv::tc::tmem_relinquish();
+        }
+        pkv::tc::fence_before_sync();
+        asm volatile("bar.sync 5, %0;\n" ::"r"(kKLoadWarp * 32) : "memory");
+        pkv::tc::fence_after_sync();
+        tmem = *tmem_slot;
+    }
 
     bool failed = false;
     auto wait = [&](uint64_t *bar, unsigned parity) {
@@ -262,9 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one lane)
         if (lane == 0) {
-            auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into the S/P buffer of team t & 1
-                wait(bar_kfull + (t % kKStages), (unsigned)((t / kKStages) & 1));
-                pkv::tc::fence_after_sync();
+            auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into the S/P buffer of team t & 1 (K(t) landed)
                 const uint32_t qa = sbase + kOffQ;
                 const uint32_t kb = sbase + kOffK + (t % kKStages) * kTile;
 #pragma unroll
@@ -276,9 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pkv::tc::mma_commit(bar_kempty + (t % kKStages));
                 pkv::tc::mma_commit(bar_s + (t & 1));
             };
-            auto issue_pv = [&](int t) {  // O(team t & 1) (+)= P(t) V(t)
-                wait(bar_vfull + (t % kVStages), (unsigned)((t / kVStages) & 1));
-                pkv::tc::fence_after_sync();
+            auto issue_pv = [&](int t) {  // O(team t & 1) (+)= P(t) V(t) (V(t) landed, P(t) stored)
                 const uint32_t vb = sbase + kOffV + (t % kVStages) * kTile;
 #pragma unroll
                 for (int kq = 0; kq < BN / 16; kq++) {  // 16 keys = 8 TMEM columns of P
@@ -290,10 +293,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pkv::tc::mma_commit(bar_vempty + (t % kVStages));
                 pkv::tc::mma_commit(bar_o + (t & 1));
             };
+            auto wait_k = [&](int t) { wait(bar_kfull + (t % kKStages), (unsigned)((t / kKStages) & 1)); };
+            auto wait_v = [&](int t) { wait(bar_vfull + (t % kVStages), (unsigned)((t / kVStages) & 1)); };
             wait(bar_go, 0);
+            wait_k(0);
+            pkv::tc::fence_after_sync();
             issue_s(0);
-            if (nkt > 1) issue_s(1);
+            if (nkt > 1) {
+                wait_k(1);
+                pkv::tc::fence_after_sync();
+                issue_s(1);
+            }
             for (int t = 0; t < nkt; t++) {
+                // operand tiles first, while the team is still computing P(t):
+                // each wait costs some hundreds of cycles even when already satisfied
+                wait_v(t);
+                if (t + 2 < nkt) wait_k(t + 2);
                 wait(bar_pfull + (t & 1), (unsigned)((t >> 1) & 1));  // P(t) stored
                 pkv::tc::fence_after_sync();
                 issue_pv(t);
@@ -403,9 +418,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ltot = l0 * f0 + l1 * f1;
         const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
         const float g0 = f0 * inv, g1 = f1 * inv;
-        // team 0 writes output columns 0..63, team 1 columns 64..127
-        OutT *orow = static_cast<OutT *>(p.out) +
-                     ((size_t)(q0 + jrow) * p.num_q_heads + kvh * G + (R - jrow * G)) * D + team * (D / 2);
+        // Output: each thread puts its half row (team 0 columns 0..63, team 1
+        // columns 64..127) into shared memory, and the 256 softmax threads
+        // then write whole rows with coalesced 16-byte stores.  The staging
+        // area is the Q and K region: every S has completed by now (the last
+        // one was issued before either team's last PV), whereas the other
+        // team's last PV may still be reading V.
+        constexpr int kRowBytes = D * (int)sizeof(OutT);
+        constexpr int kStride = kRowBytes + 16;  // padded rows
+        static_assert(BM * kStride <= kOffV, "output staging must not reach the V ring");
+        unsigned char *stage = smem + kOffQ;
 #pragma unroll 1
         for (int c = 0; c < D / 2; c += 32) {
             float a[32], b[32];
@@ -417,10 +439,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; i++) b[i] = 0.f;
             }
-            if (row_ok && !failed) {
+            OutT *srow = reinterpret_cast<OutT *>(stage + row * kStride) + col;
 #pragma unroll
-                for (int i = 0; i < 32; i += 2)
-                    pkv::store2(orow + c + i, a[i] * g0 + b[i] * g1, a[i + 1] * g0 + b[i + 1] * g1);
+            for (int i = 0; i < 32; i += 2) pkv::store2(srow + i, a[i] * g0 + b[i] * g1, a[i + 1] * g0 + b[i + 1] * g1);
+        }
+        asm volatile("bar.sync 6, %0;\n" ::"r"(2 * kTeamThreads) : "memory");
+        constexpr int kChunks = kRowBytes / 16;  // 16-byte chunks per row
+        for (int i = tid; i < BM * kChunks; i += 2 * kTeamThreads) {
+            const int r = i / kChunks, ch = i - r * kChunks;
+            const int Rr = tile * BM + r;
+            const int jr = Rr / G;
+            if (jr < n && !failed) {
+                unsigned char *dst = reinterpret_cast<unsigned char *>(static_cast<OutT *>(p.out)) +
+                                     ((size_t)(q0 + jr) * p.num_q_heads + kvh * G + (Rr - jr * G)) * kRowBytes +
+                                     ch * 16;
+                *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(stage + r * kStride + ch * 16);
             }
         }
     }
