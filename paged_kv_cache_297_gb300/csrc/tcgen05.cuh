@@ -57,6 +57,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
 // false after `max_iters` unsuccessful polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned max_iters) {
     const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    {  // non-blocking test first: cheap when the phase has already completed
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
     for (unsigned it = 0; it < max_iters; it++) {
         uint32_t done;
         asm volatile(
