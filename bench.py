@@ -20,6 +20,7 @@ on the same workload instead.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -74,6 +75,27 @@ def max_over_ranks(value: float, world: int, device: str = "cpu") -> float:
 # measurement helpers
 # ----------------------------------------------------------------------------
 
+def kernel_source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_cache_297_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, files):
+    """DRAM bytes per call from the committed ncu summary, only while the
+    kernel's sources still hash to what was profiled (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel, {}).get(workload)
+    if not rec or rec.get("source_sha") != kernel_source_hash(files):
+        return None
+    return rec.get("dram_bytes_per_call")
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -105,7 +127,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
@@ -208,6 +230,7 @@ class Step:
 
 
 W_DEFAULT_PARTITION = 512
+DECODE_SOURCES = ("common.cuh", "decode.cu")
 
 
 def time_device(step: Step, steps: int, warmup: int, world: int):
@@ -336,11 +359,13 @@ def run_ours(args):
     db = accounting.decode_bytes(batch.context_lens, Hq, batch.spec.num_kv_heads, d, elem, elem)
     dec_ms = per_call["decode"]
     achieved = db["total"] / (dec_ms / 1e3) / 1e9
+    traffic = recorded_traffic("paged_attention_decode", args.workload, DECODE_SOURCES)
     roofline = {"kernel": "paged_attention_decode (partition kernel + log-sum-exp reduce)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": None, "algorithmic_bytes": db["total"],
+                "traffic": traffic, "traffic_unit": "bytes per call (ncu dram read+write)",
+                "algorithmic_bytes": db["total"],
                 "kv_bytes": db["kv"], "decode_us": round(dec_ms * 1e3, 2)}
     extra = {}
     if step.pout is not None:
@@ -436,7 +461,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.SPECS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -1,0 +1,68 @@
+"""Multi-process paths of bench.py on the host (gloo, world size 2).
+
+Sequences shard across ranks with no data-path collective; the only
+cross-rank steps are the barriers around the timed region and taking the
+slowest rank's time.  These run without a GPU.
+"""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, values, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    bench.init_dist(world, "gloo")
+    bench.barrier(world)
+    results[rank] = bench.max_over_ranks(values[rank], world)
+    bench.barrier(world)
+    dist.destroy_process_group()
+
+
+def test_slowest_rank_time_is_taken():
+    world = 2
+    values = [3.25, 7.5]
+    with mp.Manager() as m:
+        results = m.dict()
+        mp.spawn(_worker, args=(world, _free_port(), values, results), nprocs=world, join=True)
+        assert dict(results) == {0: 7.5, 1: 7.5}
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(1.5, 1) == 1.5
+    bench.barrier(1)
+
+
+def test_reference_arm_prints_once_under_torchrun():
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--workload", "tiny_fp32", "--gpus", "2", "--steps", "2",
+           "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
