@@ -174,7 +174,7 @@ class ClockSampler:
 class Step:
     """Device-resident inputs and the calls of one step of the hot path."""
 
-    def __init__(self, batch: W.Batch, dev: str):
+    def __init__(self, batch: W.Batch, dev: str, partition: int = 0):
         import paged_kv_cache_297_gb300 as pkv
         self.pkv = pkv
         self.b = batch
@@ -189,7 +189,8 @@ class Step:
         S, Hq, d = batch.q.shape
         self.out = torch.empty((S, Hq, d), dtype=batch.dtype, device=dev)
         self.max_ctx = max(1, batch.max_context_len)
-        ws = pkv.decode_workspace_bytes(S, Hq, d, self.max_ctx)
+        self.partition = partition
+        ws = pkv.decode_workspace_bytes(S, Hq, d, self.max_ctx, partition)
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
         self.pout = None
         if batch.prefill_q is not None:
@@ -201,7 +202,7 @@ class Step:
 
     def launches_per_step(self) -> int:
         n = 2  # append + decode partitions
-        if self.max_ctx > W_DEFAULT_PARTITION:
+        if self.max_ctx > (self.partition or W_DEFAULT_PARTITION):
             n += 1  # log-sum-exp reduce
         if self.has_copy:
             n += 1
@@ -220,7 +221,7 @@ class Step:
                                                        t["k_cache"], t["v_cache"])))
         out.append(("decode", lambda: pkv.paged_attention_decode(
             t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"], b.scale,
-            self.out, max_context_len=self.max_ctx, workspace=self.ws)))
+            self.out, max_context_len=self.max_ctx, partition_size=self.partition, workspace=self.ws)))
         if self.pout is not None:
             out.append(("prefill_chunk", lambda: pkv.paged_attention_prefill_chunk(
                 t["prefill_q"], t["prefill_cu_q_lens"], t["k_cache"], t["v_cache"],
@@ -338,7 +339,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     batch = W.make_batch(args.workload, poison=False)
-    step = Step(batch, dev)
+    step = Step(batch, dev, args.partition)
     peaks = read_peaks()
 
     clocks = ClockSampler(local)
@@ -466,6 +467,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.SPECS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition", type=int, default=0,
+                    help="decode split-K partition in tokens (0: the library default, 512)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

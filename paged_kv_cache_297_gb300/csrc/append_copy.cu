@@ -14,6 +14,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
     int num_tokens, uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots,
     int num_kv_heads, int chunks_per_row, unsigned *status) {
+    pkv::allow_dependents();
+    pkv::grid_dependency_wait();
     int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     int64_t per_token = (int64_t)num_kv_heads * chunks_per_row;
     if (i >= (int64_t)num_tokens * per_token) return;
@@ -83,10 +85,12 @@ extern "C" int pkv_kv_append(const void *k, const void *v, const int64_t *slot_m
     int64_t total = (int64_t)num_tokens * num_kv_heads * chunks;
     int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
-    kv_append_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+    cudaError_t e = pkv::launch_dependent(
+        kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0, static_cast<cudaStream_t>(stream),
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), (int64_t)num_blocks * kBlock,
         num_kv_heads, chunks, pkv::status_ptr());
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "kv_append: %s", cudaGetErrorString(e));
     return pkv::check_launch("kv_append");
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pkv.h"
 
 namespace pkv {
@@ -22,7 +24,39 @@ int check_launch(const char *what);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launch `kernel` with programmatic stream serialisation, so that its launch
+// overlaps the tail of the previous kernel on the stream (see
+// grid_dependency_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ---------------------------------------------------------------- device side
+
+// Programmatic dependent launch.  A kernel launched with
+// pkv::launch_dependent may start while the previous kernel on the stream is
+// still running; it must call grid_dependency_wait() before reading anything
+// that kernel writes (the wait returns once the previous grid has completed and
+// its memory is visible; without the launch attribute it returns at once).
+// allow_dependents() lets the next dependent kernel launch early.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 
 __device__ __forceinline__ void flag(unsigned *status, unsigned bits) {
     if (status) atomicOr(status, bits);

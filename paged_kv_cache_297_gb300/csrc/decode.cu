@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
     constexpr int NT = D / 8;                 // n-tiles of the output
 
     extern __shared__ __align__(128) unsigned char smem[];
+    pkv::allow_dependents();
+    pkv::grid_dependency_wait();  // the appended tokens of the previous launch
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gid = lane >> 2, tig = lane & 3;
     const int kvh = blockIdx.x / p.head_chunks, chunk = blockIdx.x - kvh * p.head_chunks;
@@ -440,6 +442,7 @@ __global__ void __launch_bounds__(kThreads) decode_cuda_core_kernel(const Decode
 template <int D, typename OutT>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p, int rows) {
     constexpr int VEC = D / 32;
+    pkv::grid_dependency_wait();  // the partials of the partition launch
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (row >= rows) return;
@@ -530,7 +533,8 @@ int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
         attr_set[dev] = true;
     }
     dim3 grid((unsigned)(p.num_kv_heads * p.head_chunks), (unsigned)num_seqs, (unsigned)p.max_parts);
-    decode_bf16_kernel<D, OutT><<<grid, kThreads, bytes, st>>>(p);
+    cudaError_t e = pkv::launch_dependent(decode_bf16_kernel<D, OutT>, grid, dim3(kThreads), bytes, st, p);
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "decode_bf16: %s", cudaGetErrorString(e));
     return pkv::check_launch("decode_bf16");
 }
 
@@ -552,10 +556,11 @@ int launch_decode(const DecodeParams &p, int num_seqs, int D, int dtype, cudaStr
     if (rc || p.max_parts <= 1) return rc;
     const int rows = num_seqs * p.num_q_heads;
     const unsigned blocks = (unsigned)((rows + 3) / 4);
-    if (D == 128)
-        decode_reduce_kernel<128, OutT><<<blocks, 128, 0, st>>>(p, rows);
-    else
-        decode_reduce_kernel<64, OutT><<<blocks, 128, 0, st>>>(p, rows);
+    cudaError_t e = D == 128 ? pkv::launch_dependent(decode_reduce_kernel<128, OutT>, dim3(blocks), dim3(128), 0,
+                                                     st, p, rows)
+                             : pkv::launch_dependent(decode_reduce_kernel<64, OutT>, dim3(blocks), dim3(128), 0,
+                                                     st, p, rows);
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "decode_reduce: %s", cudaGetErrorString(e));
     return pkv::check_launch("decode_reduce");
 }
 
