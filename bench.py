@@ -174,7 +174,7 @@ class ClockSampler:
 class Step:
     """Device-resident inputs and the calls of one step of the hot path."""
 
-    def __init__(self, batch: W.Batch, dev: str, partition: int = 0):
+    def __init__(self, batch: W.Batch, dev: str, partition: int = 0, unfused: bool = False):
         import paged_kv_cache_297_gb300 as pkv
         self.pkv = pkv
         self.b = batch
@@ -190,6 +190,8 @@ class Step:
         self.out = torch.empty((S, Hq, d), dtype=batch.dtype, device=dev)
         self.max_ctx = max(1, batch.max_context_len)
         self.partition = partition
+        # the partition the library uses (decides whether the reduce launches)
+        self.part_used = pkv.decode_partition_size(S, batch.spec.num_kv_heads, self.max_ctx, partition)
         ws = pkv.decode_workspace_bytes(S, Hq, d, self.max_ctx, partition)
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
         self.pout = None
@@ -199,10 +201,22 @@ class Step:
             self.max_q = int((cu[1:] - cu[:-1]).max())
             self.max_pctx = int(batch.prefill_context_lens.max())
         self.has_copy = batch.copy_pairs is not None and batch.copy_pairs.numel() > 0
+        # decode-only steps whose new tokens are exactly one per sequence at
+        # position L-1 take the fused append + decode call
+        self.fused = (not unfused) and batch.prefill_q is None and self._one_token_per_seq()
+
+    def _one_token_per_seq(self) -> bool:
+        b = self.b
+        L = b.context_lens.long()
+        if b.slot_mapping.numel() != L.numel() or bool((L <= 0).any()):
+            return False
+        pos = L - 1
+        blk = b.block_tables.long().gather(1, (pos // 16).unsqueeze(1)).squeeze(1)
+        return bool(torch.equal(blk * 16 + pos % 16, b.slot_mapping.long()))
 
     def launches_per_step(self) -> int:
-        n = 2  # append + decode partitions
-        if self.max_ctx > (self.partition or W_DEFAULT_PARTITION):
+        n = 1 if self.fused else 2  # (append +) decode partitions
+        if self.max_ctx > self.part_used:
             n += 1  # log-sum-exp reduce
         if self.has_copy:
             n += 1
@@ -217,6 +231,12 @@ class Step:
         if self.has_copy:
             out.append(("copy_blocks", lambda: pkv.copy_blocks(t["copy_pairs"], t["k_cache"],
                                                                t["v_cache"])))
+        if self.fused:
+            out.append(("decode", lambda: pkv.decode_step(
+                t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["block_tables"],
+                t["context_lens"], b.scale, self.out, max_context_len=self.max_ctx,
+                partition_size=self.partition, workspace=self.ws)))
+            return out
         out.append(("kv_append", lambda: pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"],
                                                        t["k_cache"], t["v_cache"])))
         out.append(("decode", lambda: pkv.paged_attention_decode(
@@ -230,37 +250,49 @@ class Step:
         return out
 
 
-W_DEFAULT_PARTITION = 512
 DECODE_SOURCES = ("common.cuh", "decode.cu")
 
 
 def time_device(step: Step, steps: int, warmup: int, world: int):
+    """Two timed passes of `steps` steps each.  The throughput pass records an
+    event only before the first and after the last step, so consecutive
+    launches keep their programmatic-dependent overlap; the breakdown pass
+    brackets every call with events (for per-call durations and the
+    roofline), which serialises the calls."""
     calls = step.calls()
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         for _, fn in calls:
             fn()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
-          for _ in range(steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(steps):
+        for _, fn in calls:
+            fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    span_ms = e0.elapsed_time(e1)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+          for _ in range(steps)]
+    torch.cuda.synchronize()
     for i in range(steps):
         ev[i][0].record(stream)
         for j, (_, fn) in enumerate(calls):
             fn()
             ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    barrier(world)
     per_call = {}
     for j, (name, _) in enumerate(calls):
         per_call[name] = sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
-    total_ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps))
-    # device time from the first step's start to the last step's end
-    span_ms = ev[0][0].elapsed_time(ev[-1][-1])
-    return span_ms, total_ms, per_call, wall
+    serial_ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)) / steps
+    return span_ms, serial_ms, per_call, wall
 
 
 def time_e2e(step: Step, steps: int, warmup: int, world: int):
@@ -339,12 +371,12 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     batch = W.make_batch(args.workload, poison=False)
-    step = Step(batch, dev, args.partition)
+    step = Step(batch, dev, args.partition, args.unfused)
     peaks = read_peaks()
 
     clocks = ClockSampler(local)
     clocks.start()
-    span_ms, total_ms, per_call, wall = time_device(step, args.steps, args.warmup, world)
+    span_ms, serial_ms, per_call, wall = time_device(step, args.steps, args.warmup, world)
     clk = clocks.stop()
     span_ms = max_over_ranks(span_ms, world, dev)
     e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, world)
@@ -358,15 +390,22 @@ def run_ours(args):
     elem = batch.q.element_size()
     # context lengths the decode call sees (after this step's append)
     db = accounting.decode_bytes(batch.context_lens, Hq, batch.spec.num_kv_heads, d, elem, elem)
+    ab = accounting.append_bytes(int(batch.slot_mapping.numel()), batch.spec.num_kv_heads, d, elem)
     dec_ms = per_call["decode"]
-    achieved = db["total"] / (dec_ms / 1e3) / 1e9
-    traffic = recorded_traffic("paged_attention_decode", args.workload, DECODE_SOURCES)
-    roofline = {"kernel": "paged_attention_decode (partition kernel + log-sum-exp reduce)",
+    # the fused call also writes the appended K and V rows (it reads them from
+    # k_new/v_new instead of the cache, which the KV count already covers)
+    dec_bytes = db["total"] + (2 * S * batch.spec.num_kv_heads * d * elem if step.fused else 0)
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    kname = "decode_step" if step.fused else "paged_attention_decode"
+    traffic = recorded_traffic(kname, args.workload, DECODE_SOURCES)
+    roofline = {"kernel": ("decode_step (fused append + partition kernel + log-sum-exp reduce)"
+                           if step.fused else
+                           "paged_attention_decode (partition kernel + log-sum-exp reduce)"),
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": traffic, "traffic_unit": "bytes per call (ncu dram read+write)",
-                "algorithmic_bytes": db["total"],
+                "algorithmic_bytes": dec_bytes, "partition": step.part_used,
                 "kv_bytes": db["kv"], "decode_us": round(dec_ms * 1e3, 2)}
     extra = {}
     if step.pout is not None:
@@ -380,7 +419,6 @@ def run_ours(args):
                                           d, elem)
         extra["copy_blocks"] = {"pairs": int(batch.copy_pairs.shape[0]), "bytes": cb,
                                 "us": round(per_call["copy_blocks"] * 1e3, 2)}
-    ab = accounting.append_bytes(int(batch.slot_mapping.numel()), batch.spec.num_kv_heads, d, elem)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "seq-steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -397,7 +435,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world} (sequences shard, no collective)"},
         "kv_gbs": round(db["kv"] / (dec_ms / 1e3) / 1e9, 1),
         "calls_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
-        "append_gbs": round(ab / (per_call["kv_append"] / 1e3) / 1e9, 1),
+        "serial_ms_per_step": round(serial_ms, 5),
         "roofline": roofline,
         "e2e": {"value": round(world * seqs_per_step * args.steps / (e2e_ms / 1e3), 1),
                 "unit": "seq-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -405,6 +443,8 @@ def run_ours(args):
         "clocks": clk,
         "wall_s": round(wall, 4),
     }
+    if "kv_append" in per_call:
+        extra["append_gbs"] = round(ab / (per_call["kv_append"] / 1e3) / 1e9, 1)
     line.update(extra)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(batch)
@@ -468,7 +508,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition", type=int, default=0,
-                    help="decode split-K partition in tokens (0: the library default, 512)")
+                    help="decode split-K partition in tokens (0: the library's adaptive choice)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="separate append and decode calls even where the fused step applies")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -68,7 +68,7 @@ extern "C" {
                                         shared memory was misaligned; its outputs are undefined */
 
 #define PKV_BLOCK_SIZE 16
-#define PKV_DEFAULT_PARTITION 512    /* decode split-K partition, tokens */
+#define PKV_DEFAULT_PARTITION 512    /* smallest decode split-K partition, tokens */
 
 /*
  * KV append (scatter).  chengxuchu #47 section 2.2: production code
@@ -100,11 +100,23 @@ int pkv_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, 
 
 /*
  * Workspace (device bytes) that pkv_paged_attention_decode needs for its
- * split-K partials with these sizes.  partition_size 0 means the default.
+ * split-K partials with these sizes.  partition_size 0 means the adaptive
+ * default; the size returned then covers every partition it may choose.
  * *bytes is a host pointer.  Returns PKV_ERR_INVALID for bad sizes.
  */
 int pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
                                int partition_size, size_t *bytes);
+
+/*
+ * The split-K partition (tokens) that a decode call with these sizes uses:
+ * partition_size itself when it is non-zero, else the adaptive choice
+ * described under pkv_paged_attention_decode, made for the current device.
+ * A call whose max_context_len (capped at max_blocks_per_seq * 16) exceeds it
+ * makes the second, log-sum-exp launch.  *out is a host pointer.  Launches
+ * nothing; returns PKV_ERR_INVALID for bad sizes.
+ */
+int pkv_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len,
+                              int partition_size, int *out);
 
 /*
  * Paged-attention decode.  One query token per sequence and head attends to
@@ -121,10 +133,13 @@ int pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int 
  *   max_context_len  host-side upper bound on every L_s, sizes the grid; a
  *                 sequence longer than it sets PKV_STATUS_BAD_LENGTH and its
  *                 output is undefined
- *   partition_size   tokens per split-K partition (multiple of 16), 0 for
- *                 the default 512.  Sequences longer than one partition are
- *                 processed as independent partitions whose results are merged
- *                 by a log-sum-exp reduction (a second launch).
+ *   partition_size   tokens per split-K partition (multiple of 16), or 0 to
+ *                 let the library choose: the largest of 3072, 2048, 1536 and
+ *                 1024 that leaves about 4 thread blocks per SM (estimated from
+ *                 num_seqs, num_kv_heads and max_context_len), else 512.
+ *                 Sequences longer than one partition are processed as
+ *                 independent partitions whose results are merged by a
+ *                 log-sum-exp reduction (a second launch).
  *   out           [num_seqs][num_q_heads][head_dim], out_dtype
  *   workspace     device scratch of at least pkv_decode_workspace_bytes(...)
  *                 bytes (may be NULL when that is 0); contents need no
@@ -137,6 +152,27 @@ int pkv_paged_attention_decode(const void *q, const void *k_cache, const void *v
                                int max_context_len, int partition_size, float scale, void *out,
                                int dtype, int out_dtype, void *workspace, size_t workspace_bytes,
                                void *stream);
+
+/*
+ * One decode step: append, then attend, in one launch.  Equivalent to
+ * pkv_kv_append of each sequence's new token at logical position L_s - 1
+ * (slot block_tables[s][(L_s-1)/16] * 16 + (L_s-1) % 16) followed by
+ * pkv_paged_attention_decode with the same arguments: the new K/V are
+ * scattered into the cache first and the query then reads every cached
+ * token (chengxuchu #47 section 2.2).  The thread block that owns a
+ * sequence's last partition writes that sequence's new row of its kv head
+ * before reading the partition, so no separate append launch is needed.
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim], dtype, 16-byte aligned
+ *   k_cache, v_cache  updated in place (bit copy) and then read
+ * Sequences with L_s = 0 append nothing.  A bad block id for position
+ * L_s - 1 skips the write and sets PKV_STATUS_BAD_BLOCK.  All other
+ * arguments, results and errors are those of pkv_paged_attention_decode.
+ */
+int pkv_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    int num_blocks, int max_context_len, int partition_size, float scale, void *out,
+                    int dtype, int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Paged-attention decode that allocates nothing, for callers that cannot

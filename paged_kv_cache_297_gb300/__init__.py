@@ -10,6 +10,7 @@ Calls (names follow the C ABI without the ``pkv_`` prefix):
   kv_append(k, v, slot_mapping, k_cache, v_cache)
   copy_blocks(src_dst_pairs, k_cache, v_cache)
   paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out)
+  decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out)
   paged_attention_prefill_chunk(q, cu_q_lens, k_cache, v_cache, block_tables,
                                 context_lens, scale, out)
   get_status()
@@ -25,7 +26,8 @@ import torch
 
 __all__ = [
     "BLOCK_SIZE", "DEFAULT_PARTITION", "PkvError", "load", "library_path", "kv_append",
-    "copy_blocks", "decode_workspace_bytes", "paged_attention_decode",
+    "copy_blocks", "decode_workspace_bytes", "decode_partition_size", "paged_attention_decode",
+    "decode_step",
     "prefill_workspace_bytes", "paged_attention_prefill_chunk", "get_status", "STATUS_BITS",
     "EXPORTED",
 ]
@@ -38,8 +40,8 @@ STATUS_BITS = {"bad_slot": 1, "bad_block": 2, "bad_length": 4, "bad_qlen": 8, "i
 
 # every entry point declared in include/pkv.h
 EXPORTED = (
-    "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes",
-    "pkv_paged_attention_decode", "pkv_paged_attention_decode_no_alloc",
+    "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes", "pkv_decode_partition_size",
+    "pkv_paged_attention_decode", "pkv_decode_step", "pkv_paged_attention_decode_no_alloc",
     "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_last_error_string",
     "pkv_version",
@@ -75,8 +77,10 @@ def load():
     lib.pkv_kv_append.argtypes = [P, P, P, I, P, P, I, I, I, I, I, P]
     lib.pkv_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I, P]
     lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.pkv_decode_partition_size.argtypes = [I, I, I, I, ctypes.POINTER(I)]
     lib.pkv_paged_attention_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I,
                                                I, P, SZ, P]
+    lib.pkv_decode_step.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I, I, P, SZ, P]
     lib.pkv_paged_attention_decode_no_alloc.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I,
                                                         I, F, P, I, I, P]
     lib.pkv_prefill_workspace_bytes.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
@@ -162,6 +166,15 @@ def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
     return int(out.value)
 
 
+def decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size: int = 0) -> int:
+    """Split-K partition (tokens) a decode call with these sizes uses on the
+    current device; partition_size 0 asks for the adaptive choice."""
+    out = ctypes.c_int(0)
+    _check(load().pkv_decode_partition_size(int(num_seqs), int(num_kv_heads), int(max_context_len),
+                                            int(partition_size), ctypes.byref(out)))
+    return int(out.value)
+
+
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                            max_context_len: Optional[int] = None, partition_size: int = 0,
                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
@@ -188,6 +201,36 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, d, bs, NB,
         int(max_context_len), int(partition_size), float(scale), _dev(out, "out"), _dt(q),
         _dt(out), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out,
+                max_context_len: Optional[int] = None, partition_size: int = 0,
+                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Append each sequence's new K/V (``[S, Hkv, d]``) at position L-1, then
+    decode, in one launch; same result as kv_append + paged_attention_decode."""
+    NB, Hkv, bs, d = _cache_dims(k_cache, v_cache)
+    S, Hq, dq = q.shape
+    if dq != d or q.dtype != k_cache.dtype or out.shape != q.shape:
+        raise ValueError("q/out must be [S, Hq, head_dim] in the cache dtype")
+    if k_new.shape != (S, Hkv, d) or v_new.shape != k_new.shape or k_new.dtype != k_cache.dtype:
+        raise ValueError("k_new/v_new must be [S, num_kv_heads, head_dim] in the cache dtype")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks] and context_lens [S]")
+    mb = int(block_tables.shape[1])
+    if max_context_len is None:
+        max_context_len = mb * bs
+    need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pkv_decode_step(
+        _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables", torch.int32), mb,
+        _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, d, bs, NB,
+        int(max_context_len), int(partition_size), float(scale), _dev(out, "out"), _dt(q), _dt(out),
+        ws_ptr, ws_bytes, _stream(stream)))
     return out
 
 

@@ -46,7 +46,32 @@ struct DecodeParams {
     int max_parts;
     float scale_log2;
     unsigned *status;
+    // fused append: token L-1 of sequence s (k_new/v_new [S][Hkv][D]) is
+    // written into the cache by the CTA(s) of the last partition, or nullptr
+    const void *k_new;
+    const void *v_new;
 };
+
+// Write the new token of sequence s, kv head kvh, at logical position L-1.
+// Called by every thread of a CTA that owns the partition holding L-1,
+// followed by a CTA barrier before the partition is read.
+template <typename T>
+__device__ __forceinline__ void append_new_token(const DecodeParams &p, const int32_t *table, int s, int kvh,
+                                                 int L, int D) {
+    const int t = L - 1;
+    const int phys = table[t / kBlock];
+    if (phys < 0 || phys >= p.num_blocks) return;  // reported by the gather
+    const int chunks = D * (int)sizeof(T) / 16;
+    const size_t dst = (((size_t)phys * p.num_kv_heads + kvh) * kBlock + (t % kBlock)) * chunks;
+    const size_t src = ((size_t)s * p.num_kv_heads + kvh) * chunks;
+    for (int i = threadIdx.x; i < 2 * chunks; i += blockDim.x) {
+        const bool is_v = i >= chunks;
+        const int c = is_v ? i - chunks : i;
+        const uint4 *from = static_cast<const uint4 *>(is_v ? p.v_new : p.k_new) + src + c;
+        uint4 *to = static_cast<uint4 *>(const_cast<void *>(is_v ? p.v_cache : p.k_cache)) + dst + c;
+        *to = *from;
+    }
+}
 
 __device__ __forceinline__ int clamp_len(int L, int cap, unsigned *status, bool report) {
     if (L < 0 || L > cap) {
@@ -122,6 +147,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
             qa[kk][2] = va ? *reinterpret_cast<const uint32_t *>(qa_row + col + 8) : 0u;
             qa[kk][3] = vb ? *reinterpret_cast<const uint32_t *>(qb_row + col + 8) : 0u;
         }
+    }
+
+    if (p.k_new && part == nparts - 1 && L > 0) {
+        append_new_token<__nv_bfloat16>(p, table, s, kvh, L, D);
+        __syncthreads();  // the new row is read below through L2 by other threads
     }
 
     unsigned char *ring = smem + warp * Sm::kWarp;
@@ -411,6 +441,11 @@ __global__ void __launch_bounds__(kThreads) decode_cuda_core_kernel(const Decode
     const int nparts = L > 0 ? (L + p.partition - 1) / p.partition : 1;
     if (part >= nparts) return;
     const int kvh = h / p.group;
+    if (p.k_new && part == nparts - 1 && L > 0) {
+        // every q head of the group writes the same bytes for its kv head
+        append_new_token<T>(p, p.block_tables + (size_t)s * p.max_blocks, s, kvh, L, D);
+        __syncthreads();
+    }
     const T *qrow = static_cast<const T *>(p.q) + ((size_t)s * p.num_q_heads + h) * D;
     float m, l, acc;
     rows_cuda_core<T>(qrow, static_cast<const T *>(p.k_cache), static_cast<const T *>(p.v_cache),
@@ -520,6 +555,29 @@ int resolve_partition(int partition_size, int *out) {
     return PKV_OK;
 }
 
+// partition_size 0: the largest of 3072, 2048, 1536, 1024 tokens that still
+// leaves an estimated 4 work units per SM, else 512.  The host knows only the
+// largest context, so a sequence is assumed to hold half of it.  Larger
+// partitions amortise each thread block's start-up and cut the split-K
+// partials; enough units keep every SM streaming.
+int adaptive_partition(int num_seqs, int num_kv_heads, int max_context_len) {
+    static int sm_count[64] = {0};
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+        if (!sm_count[dev] && cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sm_count[dev] = 0;
+        if (sm_count[dev] > 0) sms = sm_count[dev];
+    }
+    cudaGetLastError();
+    const long long target = 4LL * sms;
+    const int candidates[] = {3072, 2048, 1536, 1024};
+    for (int c : candidates) {
+        const long long per_seq = max(1, (max_context_len + 2 * c - 1) / (2 * c));
+        if ((long long)num_seqs * num_kv_heads * per_seq >= target) return c;
+    }
+    return PKV_DEFAULT_PARTITION;
+}
+
 template <int D, typename OutT>
 int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
     constexpr int bytes = DecodeSmem<D>::kBytes;
@@ -579,14 +637,24 @@ extern "C" int pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int hea
     return PKV_OK;
 }
 
-extern "C" int pkv_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
-                                          const int32_t *block_tables, int max_blocks_per_seq,
-                                          const int32_t *context_lens, int num_seqs,
-                                          int num_q_heads, int num_kv_heads, int head_dim,
-                                          int block_size, int num_blocks, int max_context_len,
-                                          int partition_size, float scale, void *out, int dtype,
-                                          int out_dtype, void *workspace, size_t workspace_bytes,
-                                          void *stream) {
+extern "C" int pkv_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len,
+                                         int partition_size, int *out) {
+    int part;
+    int rc = resolve_partition(partition_size, &part);
+    if (rc) return rc;
+    if (!out || num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0)
+        return pkv::fail(PKV_ERR_INVALID, "decode_partition_size: bad argument");
+    *out = partition_size == 0 ? adaptive_partition(num_seqs, num_kv_heads, max_context_len) : part;
+    return PKV_OK;
+}
+
+namespace {
+
+int decode_impl(const void *q, const void *k_new, const void *v_new, const void *k_cache, const void *v_cache,
+                const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                int max_context_len, int partition_size, float scale, void *out, int dtype, int out_dtype,
+                void *workspace, size_t workspace_bytes, void *stream) {
     int part;
     int rc = resolve_partition(partition_size, &part);
     if (rc) return rc;
@@ -604,6 +672,7 @@ extern "C" int pkv_paged_attention_decode(const void *q, const void *k_cache, co
     if (!(scale == scale)) return pkv::fail(PKV_ERR_INVALID, "decode: scale is NaN");
     if (num_seqs == 0) return PKV_OK;
     if (num_seqs > 65535) return pkv::fail(PKV_ERR_INVALID, "decode: at most 65535 sequences per call");
+    if (partition_size == 0) part = adaptive_partition(num_seqs, num_kv_heads, max_context_len);
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return pkv::fail(PKV_ERR_INVALID, "decode: null pointer");
     if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) || !pkv::aligned16(out))
@@ -629,6 +698,10 @@ extern "C" int pkv_paged_attention_decode(const void *q, const void *k_cache, co
     if (p.max_parts > 65535) return pkv::fail(PKV_ERR_INVALID, "decode: too many partitions");
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = pkv::status_ptr();
+    p.k_new = k_new;
+    p.v_new = v_new;
+    if ((k_new || v_new) && (!k_new || !v_new || !pkv::aligned16(k_new) || !pkv::aligned16(v_new)))
+        return pkv::fail(PKV_ERR_INVALID, "decode_step: k_new and v_new must both be 16-byte aligned device pointers");
 
     const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, p.max_parts);
     if (need > 0) {
@@ -645,4 +718,33 @@ extern "C" int pkv_paged_attention_decode(const void *q, const void *k_cache, co
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return out_dtype == PKV_F32 ? launch_decode<float>(p, num_seqs, head_dim, dtype, st)
                                 : launch_decode<__nv_bfloat16>(p, num_seqs, head_dim, dtype, st);
+}
+
+}  // namespace
+
+extern "C" int pkv_paged_attention_decode(const void *q, const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables, int max_blocks_per_seq,
+                                          const int32_t *context_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_blocks, int max_context_len,
+                                          int partition_size, float scale, void *out, int dtype,
+                                          int out_dtype, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+    return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len,
+                       partition_size, scale, out, dtype, out_dtype, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pkv_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                               void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               int max_context_len, int partition_size, float scale, void *out,
+                               int dtype, int out_dtype, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+    if (num_seqs > 0 && (!k_new || !v_new))
+        return pkv::fail(PKV_ERR_INVALID, "decode_step: null k_new or v_new");
+    return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len,
+                       partition_size, scale, out, dtype, out_dtype, workspace, workspace_bytes, stream);
 }

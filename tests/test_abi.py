@@ -53,6 +53,24 @@ def test_decode_workspace_sizes(lib):
     assert b"multiple of 16" in lib.pkv_last_error_string()
 
 
+def test_decode_partition_choice(lib):
+    assert pkv.decode_partition_size(64, 8, 4096, 256) == 256
+    # adaptive: the largest partition that still leaves ~4 blocks per SM, for
+    # any device of 129..256 SMs (without a device the library assumes 148)
+    assert pkv.decode_partition_size(64, 8, 4096) == 1536   # 64x8x2 units
+    assert pkv.decode_partition_size(8, 8, 131072) == 3072  # 8x8x22 units
+    assert pkv.decode_partition_size(256, 8, 2560) == 3072
+    assert pkv.decode_partition_size(4, 4, 64) == pkv.DEFAULT_PARTITION
+    assert pkv.decode_partition_size(0, 8, 0) == pkv.DEFAULT_PARTITION
+    # the workspace asked for with partition 0 covers whatever is chosen
+    for S, hkv, L in [(64, 8, 4096), (8, 8, 131072), (4, 4, 64), (1, 1, 70000)]:
+        part = pkv.decode_partition_size(S, hkv, L)
+        assert pkv.decode_workspace_bytes(S, 4 * hkv, 128, L, 0) >= \
+            pkv.decode_workspace_bytes(S, 4 * hkv, 128, L, part)
+    with pytest.raises(pkv.PkvError):
+        pkv.decode_partition_size(1, 8, 100, 24)
+
+
 @pytest.mark.parametrize("bad", ["block_size", "head_dim", "dtype", "heads"])
 def test_host_rejects_bad_arguments(lib, bad):
     P = ctypes.c_void_p

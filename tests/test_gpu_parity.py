@@ -59,6 +59,14 @@ def test_workload_parity_bf16_out(name):
     _check_step(b, torch.bfloat16)
 
 
+@pytest.mark.parametrize("name", ["llama3_8b_decode", "long_context"])
+def test_workload_parity_smallest_partition(name):
+    # the default picks a large partition on these shapes; the smallest one
+    # splits every long sequence and exercises the reduction at full size
+    b = W.make_batch(name)
+    _check_step(b, partition_size=512)
+
+
 # ------------------------------------------------------------------ edge cases
 
 EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 511, 512, 513, 1023, 1024, 1025, 2047]
@@ -116,6 +124,57 @@ def test_prefill_edges(priors, chunks, hq, hkv, d):
 def test_prefill_fp32():
     b = W.custom_prefill("f32", 8, 2, 64, [0, 40], [20, 9], seed=302)
     _check_step(b)
+
+
+# ------------------------------------------------------------------ fused append + decode
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,lens,partition", [
+    ("bf16", 32, 8, 128, [1, 16, 17, 512, 513, 1024, 1025, 3000, 0], 0),
+    ("bf16", 32, 8, 128, [1, 16, 17, 512, 513, 1024, 1025, 3000], 512),
+    ("bf16", 64, 2, 64, [5, 40, 700], 0),
+    ("f32", 16, 4, 128, [1, 33, 600], 256),
+])
+def test_decode_step_equals_append_then_decode(dtype, hq, hkv, d, lens, partition):
+    b = W.custom_batch(dtype, len(lens), hq, hkv, d, lens, seed=501 + d + hq)
+    # the generator's new tokens sit at position L-1 of each non-empty sequence
+    S = len(lens)
+    t = to_dev(b)
+    kc, vc = t["k_cache"].clone(), t["v_cache"].clone()
+    pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"])
+    ref = torch.empty(b.q.shape, dtype=torch.float32, device="cuda")
+    pkv.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
+                               b.scale, ref, max_context_len=max(lens), partition_size=partition)
+    # new-token rows per sequence (zeros for empty sequences, which append nothing)
+    k_new = torch.zeros((S, hkv, d), dtype=b.k_new.dtype, device="cuda")
+    v_new = torch.zeros_like(k_new)
+    rows = [i for i, L in enumerate(lens) if L > 0]
+    k_new[rows] = t["k_new"]
+    v_new[rows] = t["v_new"]
+    got = torch.empty_like(ref)
+    pkv.decode_step(t["q"], k_new, v_new, kc, vc, t["block_tables"], t["context_lens"], b.scale, got,
+                    max_context_len=max(lens), partition_size=partition)
+    torch.cuda.synchronize()
+    assert pkv.get_status() == 0
+    assert_bits_equal(kc, t["k_cache"], "k_cache")
+    assert_bits_equal(vc, t["v_cache"], "v_cache")
+    assert torch.equal(got.cpu(), ref.cpu())
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_decode", "shared_prefix_cow"])
+def test_decode_step_workload_parity(name):
+    b = W.make_batch(name)
+    kc_o, vc_o, out_o, _ = oracle_step(b)
+    t = to_dev(b)
+    if t["copy_pairs"] is not None and t["copy_pairs"].numel():
+        pkv.copy_blocks(t["copy_pairs"], t["k_cache"], t["v_cache"])
+    out = torch.empty(b.q.shape, dtype=torch.float32, device="cuda")
+    pkv.decode_step(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["block_tables"],
+                    t["context_lens"], b.scale, out, max_context_len=b.max_context_len)
+    torch.cuda.synchronize()
+    assert pkv.get_status() == 0
+    assert_bits_equal(t["k_cache"], kc_o, "k_cache")
+    assert_bits_equal(t["v_cache"], vc_o, "v_cache")
+    assert_parity(out, out_o, b.dtype, name)
 
 
 # ------------------------------------------------------------------ invariances (bitwise)
