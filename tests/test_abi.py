@@ -90,9 +90,10 @@ def test_host_rejects_bad_arguments(lib, bad):
         0, None)
     assert rc == pkv.ERR_INVALID
     assert lib.pkv_last_error_string()
-    rc = lib.pkv_kv_append(dummy, dummy, dummy, 1, dummy, dummy, 8, args["hkv"], args["head_dim"],
-                           args["block_size"], args["dtype"], None)
     if bad in ("block_size", "head_dim", "dtype"):
+        # (with valid sizes the append would launch on the dummy pointers)
+        rc = lib.pkv_kv_append(dummy, dummy, dummy, 1, dummy, dummy, 8, args["hkv"],
+                               args["head_dim"], args["block_size"], args["dtype"], None)
         assert rc == pkv.ERR_INVALID
 
 

@@ -96,6 +96,35 @@ def test_split_matches_unsplit():
     assert float((split - whole).abs().max()) <= 2e-3
 
 
+def test_default_matches_unsplit():
+    lens = [3000, 4096, 777, 2049]
+    b = W.custom_batch("bf16", len(lens), 32, 8, 128, lens, seed=206)
+    _, _, dflt, _ = gpu_step(b, partition_size=0)
+    _, _, whole, _ = gpu_step(b, partition_size=4096)
+    assert float((dflt - whole).abs().max()) <= 2e-3
+
+
+# ------------------------------------------------------------------ batch shapes
+
+def _lens(n, lo, hi, seed):
+    import numpy as np
+    return np.random.Generator(np.random.PCG64(seed)).integers(lo, hi + 1, n).tolist()
+
+
+@pytest.mark.parametrize("S,hq,hkv,d,lo,hi,seed", [
+    (300, 32, 8, 128, 0, 200, 601),       # many short sequences, some empty
+    (1, 32, 8, 128, 65536, 65536, 602),   # one long sequence: 128 partitions of 512
+    (2049, 8, 8, 64, 1, 64, 604),         # many tiny sequences, G = 1
+    (7, 16, 1, 128, 1000, 9000, 605),     # a group of 16 on one kv head
+    (33, 12, 4, 64, 1, 3000, 606),        # group of 3 (rows 3..15 of the tile empty)
+])
+def test_batch_shapes(S, hq, hkv, d, lo, hi, seed):
+    lens = _lens(S, lo, hi, seed)
+    b = W.custom_batch("bf16", S, hq, hkv, d, lens, seed=seed)
+    _check_step(b)
+    _check_step(b, out_dtype=torch.bfloat16)
+
+
 def test_single_token_context_returns_value_row_exactly():
     b = W.custom_batch("bf16", 6, 32, 8, 128, [1] * 6, seed=204)
     _, _, out, _ = gpu_step(b)

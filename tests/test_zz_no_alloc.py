@@ -66,8 +66,10 @@ def test_no_alloc_refuses_sizes_beyond_its_scratch():
     assert lib.pkv_decode_workspace_bytes(8, 64, 128, 131072, 0, ctypes.byref(need)) == 0
     assert need.value > (16 << 20)
     dummy = ctypes.c_void_p(4096)
+    # explicit 512-token partitions: 8 x 64 x 256 partials of 130 floats
+    # (68 MB) whatever the device, so the call is refused before any launch
     rc = lib.pkv_paged_attention_decode_no_alloc(dummy, dummy, dummy, dummy, 8192, dummy, 8, 64, 8,
-                                                 128, 16, 1, 131072, 0, ctypes.c_float(0.1), dummy,
+                                                 128, 16, 1, 131072, 512, ctypes.c_float(0.1), dummy,
                                                  pkv.BF16, pkv.F32, None)
     assert rc == pkv.ERR_INVALID
     assert b"static scratch" in lib.pkv_last_error_string()
