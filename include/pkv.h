@@ -209,7 +209,8 @@ int pkv_paged_attention_decode_no_alloc(const void *q, const void *k_cache, cons
                                         int out_dtype, void *stream);
 
 /*
- * Workspace (device bytes) that pkv_paged_attention_prefill_chunk needs.
+ * Workspace (device bytes) that pkv_paged_attention_prefill_chunk needs:
+ * 256 for head_dim 128 (the bf16 kernel's work-item counter), else 0.
  */
 int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
                                 int head_dim, int max_q_len, int max_context_len, size_t *bytes);
@@ -228,6 +229,10 @@ int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_heads, int 
  *   max_q_len  host-side bound on every n_s (sizes the grid)
  *   max_context_len  host-side bound on every L_s
  *   out        [total_q][num_q_heads][head_dim], out_dtype
+ *   workspace  device scratch of pkv_prefill_workspace_bytes(...) bytes,
+ *              8-byte aligned; it needs no initialisation (the call clears
+ *              what it uses on `stream`), and calls that overlap on the GPU
+ *              must not share it.
  * n_s > L_s or n_s > max_q_len sets PKV_STATUS_BAD_QLEN and skips the sequence.
  */
 int pkv_paged_attention_prefill_chunk(const void *q, const int32_t *cu_q_lens,

@@ -366,7 +366,8 @@ extern "C" int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_
     if (!bytes || num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         max_q_len < 0 || max_context_len < 0 || (head_dim != 64 && head_dim != 128))
         return pkv::fail(PKV_ERR_INVALID, "prefill_workspace_bytes: bad argument");
-    *bytes = 0;
+    // the tcgen05 path's work-item counter (one 8-byte word, 256-byte aligned)
+    *bytes = head_dim == 128 ? 256 : 0;
     return PKV_OK;
 }
 
@@ -379,8 +380,6 @@ extern "C" int pkv_paged_attention_prefill_chunk(const void *q, const int32_t *c
                                                  int block_size, int num_blocks, float scale,
                                                  void *out, int dtype, int out_dtype, void *workspace,
                                                  size_t workspace_bytes, void *stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     if (block_size != kBlock) return pkv::fail(PKV_ERR_INVALID, "block_size must be 16 (got %d)", block_size);
     if (head_dim != 64 && head_dim != 128)
         return pkv::fail(PKV_ERR_INVALID, "head_dim must be 64 or 128 (got %d)", head_dim);
@@ -422,6 +421,12 @@ extern "C" int pkv_paged_attention_prefill_chunk(const void *q, const int32_t *c
     p.total_q = total_q;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = pkv::status_ptr();
+    if (pkv::prefill_tc_supported(dtype, head_dim)) {
+        if (!workspace || workspace_bytes < 8 || (reinterpret_cast<uintptr_t>(workspace) & 7u) != 0)
+            return pkv::fail(PKV_ERR_INVALID,
+                             "prefill: workspace of 8 bytes (8-byte aligned) needed, %zu given", workspace_bytes);
+        p.item_counter = static_cast<unsigned long long *>(workspace);
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return out_dtype == PKV_F32 ? launch_prefill<float>(p, num_seqs, head_dim, dtype, st)
                                 : launch_prefill<__nv_bfloat16>(p, num_seqs, head_dim, dtype, st);

@@ -24,6 +24,12 @@ struct PrefillParams {
     int total_q;
     float scale_log2;
     unsigned *status;
+    // tcgen05 kernel only: persistent CTAs take (sequence, q tile, kv head)
+    // items from a counter in the workspace
+    int num_seqs;
+    int tiles_per_seq;
+    int num_items;
+    unsigned long long *item_counter;
 };
 
 // tcgen05 kernel (prefill_tc.cu): bf16 caches with head_dim 128.

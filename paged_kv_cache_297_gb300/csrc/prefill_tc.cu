@@ -14,22 +14,26 @@
 //                      B = V (smem, MN-major); accumulators in TMEM.
 // A tcgen05.mma costs roughly the same to issue whatever its N, so tiles are
 // as wide as tensor memory allows.
-// Warp roles (one CTA per SM, 11 warps):
+// Warp roles (one CTA per SM, 12 warps):
 //   * two softmax teams of 4 warps: team 0 takes key tiles 0, 2, 4, ..., team 1
 //     tiles 1, 3, 5, ...  Thread r of a team owns query row r (TMEM lane r).
-//     It reads its 128 scores with one tcgen05.ld, masks them, finds the row
-//     maximum, computes p = 2^(s * scale * log2 e - m) (one multiply-add per
-//     element; a quarter of the powers on the FMA pipe with a polynomial, the
-//     rest with ex2.approx on the special-function unit) and stores P as bf16
-//     pairs over the first 64 columns of the same S buffer.  Each team has its own S/P buffer, O accumulator and
-//     running (m, l); the two partial results are merged by log-sum-exp at
-//     the end.  The teams run independently, so one team's softmax overlaps
-//     the other team's MMAs.
-//   * one MMA warp whose first lane issues, per tile t, PV(t) as soon as P(t)
-//     is stored and then S(t+2) into the same team's buffer.  tcgen05.mma
-//     operations issued by one thread execute in order, so S(t+2) cannot
-//     overwrite P(t) before PV(t) has read it, and a team that sees S(t)
-//     complete also knows its previous PV is done.
+//     It reads its 128 scores from TMEM 64 at a time, twice (once for the row
+//     maximum, once for the powers, so only 64 stay in registers), masks them,
+//     computes p = 2^(s * scale * log2 e - m) (one paired multiply-add per two
+//     elements; one pair in eight on the FMA pipe with a polynomial, the rest
+//     with ex2.approx on the special-function unit) and stores P as bf16 pairs
+//     over the first 64 columns of the same S buffer, handing each half (64
+//     keys) to the MMA warp as soon as it is stored.  Each team has its own
+//     S/P buffer, O accumulator and running (m, l); the two partial results
+//     are merged by log-sum-exp at the end.  The teams run independently, so
+//     one team's softmax overlaps the other team's MMAs.
+//   * two MMA warps, one per team, whose first lane issues, per tile t of its
+//     team, PV(t) (half by half as P(t) is stored) and then S(t+2) into the
+//     same buffer.  tcgen05.mma operations issued by one thread execute in
+//     order, so S(t+2) cannot overwrite P(t) before PV(t) has read it, and a
+//     team that sees S(t) complete also knows its previous PV is done.  Two
+//     issuing threads halve the issue overhead (barrier waits, descriptors,
+//     commits) that a single thread would serialise across both teams.
 //   * two loader warps, one for K and one for V, that gather tiles through
 //     the block table: a tile of whole blocks with 2-D TMA boxes (one
 //     16-row x 64-column box per block and half; the cache is viewed as
@@ -37,9 +41,9 @@
 //     writes exactly the layout the MMAs read); the last tile, which may end
 //     inside a block, with zero-filling 16-byte cp.async instead, because rows
 //     past the context may hold anything (even NaN) and P = 0 times NaN would
-//     still poison O.  K uses a 2-stage ring refilled when the S that read a
-//     stage has finished, V a 3-stage ring refilled when the PV has (K(t) is
-//     needed two tiles before V(t), so both get about the same lead).
+//     still poison O.  K and V use 3-stage rings, refilled when the S (for
+//     K) or PV (for V) that read a stage has finished: a tile's load then
+//     starts about three tiles before its MMA, more than an HBM round trip.
 // The running max of a row is only moved when a tile maximum exceeds it by
 // more than 8 (log2 units), so P <= 256 and O is rarely rescaled; numerator
 // and denominator share the same reference, so the result is exact.
@@ -48,7 +52,7 @@
 // Shared memory, all in the 128-byte-swizzled canonical layout (8-row atoms
 // of 8 x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)):
 //   Q : two 64-column halves of 128 rows                       (32 KB)
-//   K : two stages x two 64-column halves of 128 rows          (64 KB)
+//   K : three stages x two 64-column halves of 128 rows        (96 KB)
 //   V : three stages x two 64-column halves of 128 rows        (96 KB)
 // Every wait on an mbarrier is bounded.  A thread whose wait expires records
 // the failure and carries on without waiting (its results are garbage), so
@@ -74,22 +78,28 @@ constexpr int D = 128;
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int kTeamThreads = 128;
-constexpr int kMmaWarp = 8, kKLoadWarp = 9, kVLoadWarp = 10;
-constexpr int kThreads = 11 * 32;
+constexpr int kMmaWarp = 8;  // warps 8 and 9: MMA issue for team 0 and team 1
+constexpr int kKLoadWarp = 10, kVLoadWarp = 11;
+constexpr int kThreads = 12 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;  // S/P of team t at 128t, O of team t at kOCol + 128t
-constexpr int kKStages = 2, kVStages = 3;
+constexpr int kKStages = 3, kVStages = 3;
 
 constexpr int kHalf = 128 * 128;             // 16 KB: 128 rows x 64 bf16
 constexpr int kTile = 2 * kHalf;             // 32 KB: 128 rows x 128 bf16
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTile;                     // 32768
-constexpr int kOffV = kOffK + kKStages * kTile;          // 98304
-constexpr int kOffBar = kOffV + kVStages * kTile;        // 196608
-// barriers: per team s, o, pfull (6); K full/empty (6); V full/empty (4); go (1)
-constexpr int kNumBars = 6 + 2 * kKStages + 2 * kVStages + 1;
-constexpr int kOffRed = kOffBar + kNumBars * 8 + 8;      // + TMEM address slot
+constexpr int kOffV = kOffK + kKStages * kTile;          // 131072
+constexpr int kOffBar = kOffV + kVStages * kTile;        // 229376
+// barriers: per team s, o (4); per team and half of P (4); K full/empty; V
+// full/empty; go (2); item queue full/empty (4); per team MMA drain (2)
+constexpr int kNumBars = 8 + 2 * kKStages + 2 * kVStages + 2 + 4 + 2;
+constexpr int kItemReaders = 1 + 2 + 8;  // item queue readers: V loader, MMA lanes, softmax warps
+constexpr int kOffSlots = (kOffBar + kNumBars * 8 + 15) & ~15;  // TMEM address (16 B), two item slots (int4)
+static_assert(kOffSlots % 16 == 0, "item slots are 16-byte vectors");
+constexpr int kOffRed = kOffSlots + 16 + 2 * 16;
 constexpr int kSmemBytes = kOffRed + 2 * 2 * BM * 4;     // [team][m, l][row]
+static_assert(kSmemBytes <= 232448, "more shared memory than a CTA may have");
 constexpr unsigned kWaitIters = 1u << 24;
 
 constexpr uint32_t kIdescS = pkv::tc::idesc_bf16_f32(BM, BN, false, false);
@@ -99,57 +109,89 @@ __device__ __forceinline__ int sw128(int r, int c16) {
     return (r >> 3) * 1024 + (r & 7) * 128 + ((c16 ^ (r & 7)) << 4);
 }
 
+// The next work item for this CTA: items below gridDim.x are each CTA's
+// first; later ones are handed out in order by one fetch-and-add on a
+// counter in the workspace, which the launch clears on the stream first.
+__device__ __forceinline__ int next_item(const PrefillParams &p) {
+    const unsigned long long k = atomicAdd(p.item_counter, 1ull);
+    return k < (unsigned long long)p.num_items ? (int)gridDim.x + (int)k : 0x7fffffff;
+}
+
+// Item (sequence, q tile, kv head) as published in the shared-memory queue:
+// (item, q0, n, L); every role derives the rest.
+struct ItemInfo {
+    int item, s, kvh, tile, q0, n, L, nkt, kv_end, mask_from;
+    bool stop, skip, bad_len, bad_qlen;
+};
+
+__device__ __forceinline__ ItemInfo item_info(const PrefillParams &p, int4 v) {
+    ItemInfo it;
+    it.item = v.x;
+    it.q0 = v.y;
+    it.n = v.z;
+    it.L = v.w;
+    it.stop = v.x >= p.num_items;
+    // later sequences first, later q tiles (more keys) first within a sequence
+    const int per_seq = p.num_kv_heads * p.tiles_per_seq;
+    const int zi = it.stop ? 0 : v.x / per_seq;
+    const int rem = it.stop ? 0 : v.x - zi * per_seq;
+    it.s = p.num_seqs - 1 - zi;
+    it.tile = p.tiles_per_seq - 1 - rem / p.num_kv_heads;
+    it.kvh = rem - (rem / p.num_kv_heads) * p.num_kv_heads;
+    it.bad_len = !it.stop && (it.L < 0 || it.L > p.len_cap);
+    it.bad_qlen = !it.stop && !it.bad_len &&
+                  (it.q0 < 0 || it.n < 0 || it.n > it.L || it.n > p.max_q_len || it.q0 + it.n > p.total_q);
+    it.skip = it.stop || it.bad_len || it.bad_qlen || it.tile * BM >= it.n * p.group;
+    if (it.skip) {
+        it.nkt = it.kv_end = it.mask_from = 0;
+    } else {
+        const int prior = it.L - it.n;
+        const int j_last = min(it.n - 1, (it.tile * BM + BM - 1) / p.group);
+        it.kv_end = prior + j_last + 1;
+        it.nkt = (it.kv_end + BN - 1) / BN;
+        it.mask_from = prior + (it.tile * BM) / p.group + 1;  // keys below this need no causal mask
+    }
+    return it;
+}
+
 template <typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x, kvh = blockIdx.y;
-    const int s = gridDim.z - 1 - blockIdx.z;  // later (typically longer) sequences first
     const int G = p.group;
-
-    const int q0 = p.cu_q_lens[s];
-    const int n = p.cu_q_lens[s + 1] - q0;
-    const int L = p.context_lens[s];
-    if (L < 0 || L > p.len_cap) {
-        if (tile == 0 && kvh == 0 && tid == 0) pkv::flag(p.status, PKV_STATUS_BAD_LENGTH);
-        return;
-    }
-    if (q0 < 0 || n < 0 || n > L || n > p.max_q_len || q0 + n > p.total_q) {
-        if (tile == 0 && kvh == 0 && tid == 0) pkv::flag(p.status, PKV_STATUS_BAD_QLEN);
-        return;
-    }
-    if (tile * BM >= n * G) return;
     const uint32_t sbase = pkv::smem_u32(smem);
     if (sbase & 1023u) {  // the swizzled layouts need 1024-byte alignment
         if (tid == 0) pkv::flag(p.status, PKV_STATUS_INTERNAL);
         return;
     }
-    const int prior = L - n;
-    const int j_last = min(n - 1, (tile * BM + BM - 1) / G);
-    const int kv_end = prior + j_last + 1;
-    const int nkt = (kv_end + BN - 1) / BN;
-    const int j_first = (tile * BM) / G;
-    const int mask_from = prior + j_first + 1;  // keys below this need no causal mask
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *bar_s = bars;           // [team] S(t) computed (and the team's PV(t-2) done)
     uint64_t *bar_o = bars + 2;       // [team] PV(t) done
-    uint64_t *bar_pfull = bars + 4;   // [team] P(t) stored (128 arrivals)
-    uint64_t *bar_kfull = bars + 6;   // [stage] K tile landed
+    uint64_t *bar_pfull = bars + 4;   // [team][half] P(t) of keys 64h .. 64h+63 stored (128 arrivals)
+    uint64_t *bar_kfull = bars + 8;   // [stage] K tile landed
     uint64_t *bar_kempty = bar_kfull + kKStages;   // [stage] the S reading it is done
     uint64_t *bar_vfull = bar_kempty + kKStages;   // [stage] V tile landed
     uint64_t *bar_vempty = bar_vfull + kVStages;   // [stage] the PV reading it is done
-    uint64_t *bar_go = bar_vempty + kVStages;      // Q landed (256 arrivals)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    uint64_t *bar_go = bar_vempty + kVStages;      // [k & 1] Q of the k-th item with work landed (256 arrivals)
+    uint64_t *bar_item_full = bar_go + 2;          // [slot] item published
+    uint64_t *bar_item_empty = bar_item_full + 2;  // [slot] every role has read it
+    uint64_t *bar_done = bar_item_empty + 2;       // [team] all of the team's MMAs finished
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffSlots);
+    int4 *item_slots = reinterpret_cast<int4 *>(smem + kOffSlots + 16);
     float *red = reinterpret_cast<float *>(smem + kOffRed);  // [team][m, l][row]
 
     if (tid == 0) {
         for (int t = 0; t < 2; t++) {
             pkv::tc::mbar_init(bar_s + t, 1);
             pkv::tc::mbar_init(bar_o + t, 1);
-            pkv::tc::mbar_init(bar_pfull + t, kTeamThreads);
+            pkv::tc::mbar_init(bar_pfull + 2 * t, kTeamThreads);
+            pkv::tc::mbar_init(bar_pfull + 2 * t + 1, kTeamThreads);
+            pkv::tc::mbar_init(bar_item_full + t, 1);
+            pkv::tc::mbar_init(bar_item_empty + t, kItemReaders);
+            pkv::tc::mbar_init(bar_done + t, 1);
         }
         for (int st = 0; st < kKStages; st++) {
             pkv::tc::mbar_init(bar_kfull + st, 1);
@@ -160,28 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             pkv::tc::mbar_init(bar_vempty + st, 1);
         }
         pkv::tc::mbar_init(bar_go, 2 * kTeamThreads);
+        pkv::tc::mbar_init(bar_go + 1, 2 * kTeamThreads);
         pkv::tc::fence_mbar_init();
     }
     __syncthreads();  // barriers initialised: the loaders can start right away
-
-    const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
-    const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
-
-    if (warp < 8) {
-        // Q tile: 128 rows x 16 chunks, 8 copies per softmax thread
-#pragma unroll
-        for (int u = 0; u < 8; u++) {
-            const int i = tid + 2 * kTeamThreads * u;
-            const int r = i >> 4, c = i & 15;
-            const int R = tile * BM + r;
-            const int jr = R / G;
-            const bool ok = jr < n;
-            const __nv_bfloat16 *src =
-                ok ? qg + ((size_t)(q0 + jr) * p.num_q_heads + kvh * G + (R - jr * G)) * D + c * 8 : qg;
-            pkv::cp_async16(smem + kOffQ + (c >> 3) * kHalf + sw128(r, c & 7), src, ok ? 16 : 0);
-        }
-        pkv::cp_async_commit();
-    }
 
     // TMEM for every warp but the loaders (which never touch it); they meet on
     // named barrier 5 so that the loaders need not wait for the allocation
@@ -201,9 +225,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait = [&](uint64_t *bar, unsigned parity) {
         if (!failed && !pkv::tc::mbar_wait(bar, parity, kWaitIters)) failed = true;
     };
+    // Take item i from the queue (every role reads every item): lane 0 waits,
+    // the warp reads, lane 0 reports the slot read.
+    auto take_item = [&](int i) {
+        if (lane == 0) wait(bar_item_full + (i & 1), (unsigned)((i >> 1) & 1));
+        __syncwarp();
+        const int4 v = item_slots[i & 1];
+        __syncwarp();
+        if (lane == 0) pkv::tc::mbar_arrive(bar_item_empty + (i & 1));
+        return item_info(p, v);
+    };
+    // Q of the k-th item with work: barrier k & 1, phase k >> 1
+    auto wait_go = [&](int k) { wait(bar_go + (k & 1), (unsigned)((k >> 1) & 1)); };
+
+    // Running counts that carry the barrier phases from one item to the next:
+    // key tiles (K/V rings), tiles of each team (S, P, O barriers) and items
+    // with work (the Q barrier).  Every role walks the same items, so every
+    // role's counts agree.
+    int kt_base = 0, team_base0 = 0, team_base1 = 0, go_count = 0;
+    auto advance = [&](const ItemInfo &it) {
+        kt_base += it.nkt;
+        team_base0 += (it.nkt + 1) / 2;
+        team_base1 += it.nkt / 2;
+        go_count += it.skip ? 0 : 1;
+    };
 
     if (warp == kKLoadWarp || warp == kVLoadWarp) {
-        // ---------------- loaders: K tile t -> K stage t % 3, V tile t -> V stage t % 2
+        // ---------------- loaders; the K loader also runs the item queue
         const bool is_k = warp == kKLoadWarp;
         const int nst = is_k ? kKStages : kVStages;
         uint64_t *full = is_k ? bar_kfull : bar_vfull;
@@ -211,109 +259,179 @@ __global__ void __launch_bounds__(kThreads, 1)
         const void *tmap = is_k ? static_cast<const void *>(&tmap_k) : static_cast<const void *>(&tmap_v);
         const unsigned char *cache = static_cast<const unsigned char *>(is_k ? p.k_cache : p.v_cache);
         const int box_rows = p.num_blocks * p.num_kv_heads * kBlock;  // rows of the 2-D view
-        for (int t = 0; t < nkt; t++) {
-            const int st = t % nst;
-            if (t >= nst) wait(empty + st, (unsigned)((t / nst - 1) & 1));
-            unsigned char *dst = smem + (is_k ? kOffK : kOffV) + st * kTile;
-            // physical ids of the 8 blocks holding keys [t*128, t*128 + 128)
-            int my_id = 0;
-            if (lane < 8 && t * BN + lane * kBlock < kv_end) my_id = table[t * 8 + lane];
-            if ((t + 1) * BN <= kv_end) {
-                // eight whole blocks: TMA
-                int y = box_rows;  // out of range: the box reads as zeros
-                if (lane < 8) {
-                    if (my_id >= 0 && my_id < p.num_blocks)
-                        y = (my_id * p.num_kv_heads + kvh) * kBlock;
-                    else
-                        pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
-                }
-                int ys[8];
-#pragma unroll
-                for (int q = 0; q < 8; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
+        int item = blockIdx.x;  // the CTA's first item; later ones come from the counter
+        for (int i = 0;; i++) {
+            ItemInfo it;
+            if (is_k) {
+                int4 v = make_int4(item, 0, 0, 0);
                 if (lane == 0) {
-                    pkv::tc::mbar_arrive_expect_tx(full + st, kTile);
-#pragma unroll
-                    for (int q = 0; q < 8; q++) {
-#pragma unroll
-                        for (int h = 0; h < 2; h++)
-                            pkv::tc::tma_load_2d(dst + h * kHalf + q * 2048, tmap, h * 64, ys[q], full + st);
+                    if (i >= 2) wait(bar_item_empty + (i & 1), (unsigned)(((i >> 1) - 1) & 1));
+                    if (item < p.num_items) {
+                        const int s = p.num_seqs - 1 - item / (p.num_kv_heads * p.tiles_per_seq);
+                        v.y = p.cu_q_lens[s];
+                        v.z = p.cu_q_lens[s + 1] - v.y;
+                        v.w = p.context_lens[s];
                     }
+                    item_slots[i & 1] = v;
+                    pkv::tc::mbar_arrive(bar_item_full + (i & 1));  // release: the slot is visible to the waiters
+                }
+                v.x = __shfl_sync(0xffffffffu, v.x, 0);
+                v.y = __shfl_sync(0xffffffffu, v.y, 0);
+                v.z = __shfl_sync(0xffffffffu, v.z, 0);
+                v.w = __shfl_sync(0xffffffffu, v.w, 0);
+                it = item_info(p, v);
+                if (lane == 0 && it.tile == 0 && it.kvh == 0) {
+                    if (it.bad_len) pkv::flag(p.status, PKV_STATUS_BAD_LENGTH);
+                    if (it.bad_qlen) pkv::flag(p.status, PKV_STATUS_BAD_QLEN);
                 }
             } else {
-                // the last tile may end inside a block: zero-filling copies
-#pragma unroll 4
-                for (int u = 0; u < 64; u++) {
-                    const int i = lane + 32 * u;
-                    const int r = i >> 4, c = i & 15;  // r >> 4 == u >> 3
-                    const int key = t * BN + r;
-                    const int phys = __shfl_sync(0xffffffffu, my_id, u >> 3);
-                    int nb = 0;
-                    size_t go = 0;
-                    if (key < kv_end) {
-                        if (phys >= 0 && phys < p.num_blocks) {
-                            nb = 16;
-                            go = ((((size_t)phys * p.num_kv_heads + kvh) * kBlock + (key % kBlock)) * D) * 2 + c * 16;
-                        } else if (c == 0 && (key % kBlock) == 0) {
+                it = take_item(i);
+            }
+            if (it.stop) break;
+            const int32_t *table = p.block_tables + (size_t)(it.skip ? 0 : it.s) * p.max_blocks;
+            for (int t = 0; t < it.nkt; t++) {
+                const int g = kt_base + t;  // ring position across items
+                const int st = g % nst;
+                if (g >= nst) wait(empty + st, (unsigned)((g / nst - 1) & 1));
+                unsigned char *dst = smem + (is_k ? kOffK : kOffV) + st * kTile;
+                // physical ids of the 8 blocks holding keys [t*128, t*128 + 128)
+                int my_id = 0;
+                if (lane < 8 && t * BN + lane * kBlock < it.kv_end) my_id = table[t * 8 + lane];
+                if ((t + 1) * BN <= it.kv_end) {
+                    // eight whole blocks: TMA
+                    int y = box_rows;  // out of range: the box reads as zeros
+                    if (lane < 8) {
+                        if (my_id >= 0 && my_id < p.num_blocks)
+                            y = (my_id * p.num_kv_heads + it.kvh) * kBlock;
+                        else
                             pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                    }
+                    int ys[8];
+#pragma unroll
+                    for (int q = 0; q < 8; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
+                    if (lane == 0) {
+                        pkv::tc::mbar_arrive_expect_tx(full + st, kTile);
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+#pragma unroll
+                            for (int h = 0; h < 2; h++)
+                                pkv::tc::tma_load_2d(dst + h * kHalf + q * 2048, tmap, h * 64, ys[q], full + st);
                         }
                     }
-                    pkv::cp_async16(dst + (c >> 3) * kHalf + sw128(r, c & 7), cache + go, nb);
+                } else {
+                    // the last tile may end inside a block: zero-filling copies
+#pragma unroll 4
+                    for (int u = 0; u < 64; u++) {
+                        const int e = lane + 32 * u;
+                        const int r = e >> 4, c = e & 15;  // r >> 4 == u >> 3
+                        const int key = t * BN + r;
+                        const int phys = __shfl_sync(0xffffffffu, my_id, u >> 3);
+                        int nb = 0;
+                        size_t go = 0;
+                        if (key < it.kv_end) {
+                            if (phys >= 0 && phys < p.num_blocks) {
+                                nb = 16;
+                                go = ((((size_t)phys * p.num_kv_heads + it.kvh) * kBlock + (key % kBlock)) * D) * 2 +
+                                     c * 16;
+                            } else if (c == 0 && (key % kBlock) == 0) {
+                                pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                            }
+                        }
+                        pkv::cp_async16(dst + (c >> 3) * kHalf + sw128(r, c & 7), cache + go, nb);
+                    }
+                    pkv::cp_async_commit();
+                    pkv::cp_async_wait<0>();
+                    pkv::tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) pkv::tc::mbar_arrive(full + st);
                 }
-                pkv::cp_async_commit();
-                pkv::cp_async_wait<0>();
-                pkv::tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) pkv::tc::mbar_arrive(full + st);
+            }
+            advance(it);
+            if (is_k) {  // the next item, fetched while the consumers work on this one
+                if (lane == 0) item = next_item(p);
+                item = __shfl_sync(0xffffffffu, item, 0);
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issue (one lane)
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // ---------------- MMA issue: lane 0 of warp 8 + q issues team q's tiles
+        const int q = warp - kMmaWarp;
         if (lane == 0) {
             auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into the S/P buffer of team t & 1 (K(t) landed)
                 const uint32_t qa = sbase + kOffQ;
-                const uint32_t kb = sbase + kOffK + (t % kKStages) * kTile;
+                const uint32_t kb = sbase + kOffK + ((kt_base + t) % kKStages) * kTile;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ks++) {
                     const uint64_t a = pkv::tc::smem_desc_sw128(qa + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
                     const uint64_t b = pkv::tc::smem_desc_sw128(kb + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
                     pkv::tc::mma_ss(tmem + (t & 1) * BN, a, b, kIdescS, ks > 0 ? 1u : 0u);
                 }
-                pkv::tc::mma_commit(bar_kempty + (t % kKStages));
+                pkv::tc::mma_commit(bar_kempty + ((kt_base + t) % kKStages));
                 pkv::tc::mma_commit(bar_s + (t & 1));
             };
-            auto issue_pv = [&](int t) {  // O(team t & 1) (+)= P(t) V(t) (V(t) landed, P(t) stored)
-                const uint32_t vb = sbase + kOffV + (t % kVStages) * kTile;
+            // O(team t & 1) (+)= P(t) V(t) over keys 64h .. 64h+63 (V(t) landed,
+            // that half of P(t) stored)
+            auto issue_pv_half = [&](int t, int h) {
+                const uint32_t vb = sbase + kOffV + ((kt_base + t) % kVStages) * kTile;
 #pragma unroll
-                for (int kq = 0; kq < BN / 16; kq++) {  // 16 keys = 8 TMEM columns of P
+                for (int kq = 4 * h; kq < 4 * h + 4; kq++) {  // 16 keys = 8 TMEM columns of P
                     // V is MN-major: next 64-column half at +16 KB (LBO), next 8 keys at +1 KB (SBO)
                     const uint64_t b = pkv::tc::smem_desc_sw128(vb + kq * 2048, kHalf, 1024);
                     pkv::tc::mma_ts(tmem + kOCol + (t & 1) * D, tmem + (t & 1) * BN + kq * 8, b, kIdescPV,
                                     (t < 2 && kq == 0) ? 0u : 1u);
                 }
-                pkv::tc::mma_commit(bar_vempty + (t % kVStages));
-                pkv::tc::mma_commit(bar_o + (t & 1));
+                if (h == 1) {
+                    pkv::tc::mma_commit(bar_vempty + ((kt_base + t) % kVStages));
+                    pkv::tc::mma_commit(bar_o + (t & 1));
+                }
             };
-            auto wait_k = [&](int t) { wait(bar_kfull + (t % kKStages), (unsigned)((t / kKStages) & 1)); };
-            auto wait_v = [&](int t) { wait(bar_vfull + (t % kVStages), (unsigned)((t / kVStages) & 1)); };
-            wait(bar_go, 0);
-            wait_k(0);
-            pkv::tc::fence_after_sync();
-            issue_s(0);
-            if (nkt > 1) {
-                wait_k(1);
-                pkv::tc::fence_after_sync();
-                issue_s(1);
+            auto wait_k = [&](int t) {
+                const int g = kt_base + t;
+                wait(bar_kfull + g % kKStages, (unsigned)((g / kKStages) & 1));
+            };
+            auto wait_v = [&](int t) {
+                const int g = kt_base + t;
+                wait(bar_vfull + g % kVStages, (unsigned)((g / kVStages) & 1));
+            };
+            for (int i = 0;; i++) {
+                // Take item i alone (the other lanes idle).  The slot is
+                // reported read only after this item's Q barrier has been
+                // waited for: the queue then cannot run two items ahead of
+                // this lane, so neither Q barrier can complete a phase that
+                // this lane has not yet waited for.
+                wait(bar_item_full + (i & 1), (unsigned)((i >> 1) & 1));
+                const ItemInfo it = item_info(p, item_slots[i & 1]);
+                if (!it.stop && !it.skip) wait_go(go_count);
+                pkv::tc::mbar_arrive(bar_item_empty + (i & 1));
+                if (it.stop) break;
+                if (!it.skip) {
+                    const int nkt = it.nkt;
+                    const int tb = q ? team_base1 : team_base0;  // this team's tiles before this item
+                    if (q < nkt) {
+                        wait_k(q);
+                        pkv::tc::fence_after_sync();
+                        issue_s(q);
+                    }
+                    for (int t = q; t < nkt; t += 2) {
+                        // PV(t) as soon as P(t) is stored; S(t+2) behind it once K(t+2)
+                        // has landed, so a late K tile never holds up a PV
+                        wait_v(t);
+                        for (int h = 0; h < 2; h++) {  // the first half runs while the team computes the second
+                            wait(bar_pfull + 2 * (t & 1) + h, (unsigned)((tb + (t >> 1)) & 1));
+                            pkv::tc::fence_after_sync();
+                            issue_pv_half(t, h);
+                        }
+                        if (t + 2 < nkt) {
+                            wait_k(t + 2);
+                            pkv::tc::fence_after_sync();
+                            issue_s(t + 2);
+                        }
+                    }
+                }
+                advance(it);
             }
-            for (int t = 0; t < nkt; t++) {
-                // operand tiles first, while the team is still computing P(t):
-                // each wait costs some hundreds of cycles even when already satisfied
-                wait_v(t);
-                if (t + 2 < nkt) wait_k(t + 2);
-                wait(bar_pfull + (t & 1), (unsigned)((t >> 1) & 1));  // P(t) stored
-                pkv::tc::fence_after_sync();
-                issue_pv(t);
-                if (t + 2 < nkt) issue_s(t + 2);
-            }
+            // every MMA of this lane has finished before TMEM is released
+            pkv::tc::mma_commit(bar_done + q);
+            if (!pkv::tc::mbar_wait(bar_done + q, 0, kWaitIters)) failed = true;
         }
         __syncwarp();
     } else {
@@ -322,139 +440,177 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t s_col = (uint32_t)team * BN, o_col = kOCol + (uint32_t)team * D;
-        const int R = tile * BM + row;
-        const int jrow = R / G;
-        const bool row_ok = jrow < n;
-        const int pos = row_ok ? prior + jrow : -1;
-        float m_used = -INFINITY, lsum = 0.f;
-
-        pkv::cp_async_wait<0>();  // this thread's Q copies
-        pkv::tc::fence_proxy_async_smem();
-        pkv::tc::mbar_arrive(bar_go);
-
-        for (int t = team; t < nkt; t += 2) {
-            // S(t) done; the team's PV(t-2), issued before it, is done too
-            wait(bar_s + team, (unsigned)((t >> 1) & 1));
-            pkv::tc::fence_after_sync();
-            const bool full_tile = t * BN + BN <= mask_from;
-            const int lim0 = pos - t * BN;  // keys i <= lim0 of this tile are visible
-
-            // all 128 raw scores of this row, masked
-            float sv[128];
-            pkv::tc::tmem_ld128(t_lane + s_col, sv);
-            if (!full_tile || !row_ok) {
-#pragma unroll
-                for (int i = 0; i < 128; i++) sv[i] = i <= lim0 ? sv[i] : -INFINITY;
+        const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
+        for (int i = 0;; i++) {
+            const ItemInfo it = take_item(i);
+            if (it.stop) break;
+            if (it.skip) {
+                advance(it);
+                continue;
             }
-            float mx[16];
+            const int nkt = it.nkt;
+            // Q tile: 128 rows x 16 chunks, 8 copies per softmax thread.  The
+            // previous item's S MMAs are all complete: this thread has been
+            // through that item's epilogue, which follows both teams' last PV.
 #pragma unroll
-            for (int i = 0; i < 16; i++)
-                mx[i] = fmaxf(fmaxf(fmaxf(sv[i], sv[i + 16]), fmaxf(sv[i + 32], sv[i + 48])),
-                              fmaxf(fmaxf(sv[i + 64], sv[i + 80]), fmaxf(sv[i + 96], sv[i + 112])));
-#pragma unroll
-            for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], mx[i + 8]);
-#pragma unroll
-            for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
-            float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            if (!row_ok) mraw = -INFINITY;
-            const float mt = mraw * p.scale_log2;  // scale > 0 commutes with max; -inf stays
-            const bool need = mt > m_used + 8.f;
-            float alpha = 1.f;
-            if (need) {
-                alpha = pkv::tc::ex2(m_used - mt);  // 0 when nothing was seen yet
-                lsum *= alpha;
-                m_used = mt;
+            for (int u = 0; u < 8; u++) {
+                const int e = tid + 2 * kTeamThreads * u;
+                const int r = e >> 4, c = e & 15;
+                const int R = it.tile * BM + r;
+                const int jr = R / G;
+                const bool ok = jr < it.n;
+                const __nv_bfloat16 *src =
+                    ok ? qg + ((size_t)(it.q0 + jr) * p.num_q_heads + it.kvh * G + (R - jr * G)) * D + c * 8 : qg;
+                pkv::cp_async16(smem + kOffQ + (c >> 3) * kHalf + sw128(r, c & 7), src, ok ? 16 : 0);
             }
-            if (t >= 2 && __any_sync(0xffffffffu, need)) {
+            pkv::cp_async_commit();
+            pkv::cp_async_wait<0>();
+            pkv::tc::fence_proxy_async_smem();
+            pkv::tc::mbar_arrive(bar_go + (go_count & 1));
+
+            const int R = it.tile * BM + row;
+            const int jrow = R / G;
+            const bool row_ok = jrow < it.n;
+            const int pos = row_ok ? it.L - it.n + jrow : -1;
+            float m_used = -INFINITY, lsum = 0.f;
+            const int tb = team ? team_base1 : team_base0;  // this team's tiles before this item
+
+            for (int t = team; t < nkt; t += 2) {
+                // S(t) done; the team's PV(t-2), issued before it, is done too
+                wait(bar_s + team, (unsigned)((tb + (t >> 1)) & 1));
+                pkv::tc::fence_after_sync();
+                const bool full_tile = t * BN + BN <= it.mask_from;
+                const int lim0 = pos - t * BN;  // keys i <= lim0 of this tile are visible
+                // The row's scores are read from TMEM twice, 64 at a time (for the
+                // maximum, then for the powers), so that only 64 stay live and the
+                // rest of the register file is free to overlap the exponentials.
+                const bool masked = !full_tile || !row_ok;
+                float mraw = -INFINITY;
+    #pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    float sv[64];
+                    pkv::tc::tmem_ld64(t_lane + s_col + h * 64, sv);
+                    if (masked) {
+    #pragma unroll
+                        for (int i = 0; i < 64; i++) sv[i] = h * 64 + i <= lim0 ? sv[i] : -INFINITY;
+                    }
+                    float mx[16];
+    #pragma unroll
+                    for (int i = 0; i < 16; i++)
+                        mx[i] = fmaxf(fmaxf(sv[i], sv[i + 16]), fmaxf(sv[i + 32], sv[i + 48]));
+    #pragma unroll
+                    for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], mx[i + 8]);
+    #pragma unroll
+                    for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
+                    mraw = fmaxf(mraw, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
+                }
+                if (!row_ok) mraw = -INFINITY;
+                const float mt = mraw * p.scale_log2;  // scale > 0 commutes with max; -inf stays
+                const bool need = mt > m_used + 8.f;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = pkv::tc::ex2(m_used - mt);  // 0 when nothing was seen yet
+                    lsum *= alpha;
+                    m_used = mt;
+                }
+                if (t >= 2 && __any_sync(0xffffffffu, need)) {
+    #pragma unroll 1
+                    for (int c = 0; c < D; c += 32) {
+                        float o[32];
+                        pkv::tc::tmem_ld32(t_lane + o_col + c, o);
+    #pragma unroll
+                        for (int i = 0; i < 32; i++) o[i] *= alpha;
+                        pkv::tc::tmem_st32(t_lane + o_col + c, o);
+                    }
+                }
+                // P = 2^(s * scale - m) as bf16 pairs over the first 64 columns;
+                // the scaling and the row sum run on paired fp32 instructions
+                const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+                const uint64_t sc2 = pkv::tc::f2(p.scale_log2, p.scale_log2), nb2 = pkv::tc::f2(nbase, nbase);
+                uint64_t acc2[2] = {pkv::tc::f2(0.f, 0.f), pkv::tc::f2(0.f, 0.f)};
+    #pragma unroll
+                for (int c = 0; c < BN; c += 64) {
+                    float sv[64];
+                    pkv::tc::tmem_ld64(t_lane + s_col + c, sv);
+                    if (masked) {
+    #pragma unroll
+                        for (int i = 0; i < 64; i++) sv[i] = c + i <= lim0 ? sv[i] : -INFINITY;
+                    }
+                    float pk[32];
+    #pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        float x0, x1, e0, e1;
+                        pkv::tc::unf2(pkv::tc::ffma2(pkv::tc::f2(sv[2 * i], sv[2 * i + 1]), sc2, nb2), x0, x1);
+                        // one pair in eight on the FMA pipe, the rest on the special-function
+                        // unit (about where the two take equally long)
+                        if ((i & 7) == 7) {
+                            pkv::tc::exp2_poly2(x0, x1, e0, e1);
+                        } else {
+                            e0 = pkv::tc::ex2(x0);
+                            e1 = pkv::tc::ex2(x1);
+                        }
+                        acc2[i & 1] = pkv::tc::fadd2(acc2[i & 1], pkv::tc::f2(e0, e1));
+                        pk[i] = __uint_as_float(pkv::pack_bf16(e0, e1));
+                    }
+                    // keys c .. c+63 -> P columns c/2 .. c/2+31, handed to the MMA lane
+                    pkv::tc::tmem_st32(t_lane + s_col + c / 2, pk);
+                    pkv::tc::fence_before_sync();
+                    pkv::tc::mbar_arrive(bar_pfull + 2 * team + c / 64);
+                }
+                {
+                    float a0, a1, b0, b1;
+                    pkv::tc::unf2(acc2[0], a0, a1);
+                    pkv::tc::unf2(acc2[1], b0, b1);
+                    lsum += (a0 + a1) + (b0 + b1);
+                }
+            }
+
+            // merge the two teams: exchange (m, l) with the partner thread of the same row
+            const int my_tiles = nkt > team ? (nkt - team + 1) / 2 : 0;
+            if (my_tiles > 0) {
+                wait(bar_o + team, (unsigned)((tb + my_tiles - 1) & 1));
+                pkv::tc::fence_after_sync();
+            }
+            red[(team * 2 + 0) * BM + row] = m_used;
+            red[(team * 2 + 1) * BM + row] = lsum;
+            asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
+            const float m0 = red[0 * BM + row], l0 = red[1 * BM + row];
+            const float m1 = red[2 * BM + row], l1 = red[3 * BM + row];
+            const float M = fmaxf(m0, m1);
+            const float f0 = M == -INFINITY ? 0.f : pkv::tc::ex2(m0 - M);
+            const float f1 = (M == -INFINITY || nkt < 2) ? 0.f : pkv::tc::ex2(m1 - M);
+            const float ltot = l0 * f0 + l1 * f1;
+            const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+            const float g0 = f0 * inv, g1 = f1 * inv;
+            // Output: each thread writes its half row (team 0 columns 0..63,
+            // team 1 columns 64..127) straight from registers, 16 bytes at a
+            // time; shared memory stays free for the next item's tiles.
+            OutT *orow = static_cast<OutT *>(p.out) +
+                         ((size_t)(it.q0 + (row_ok ? jrow : 0)) * p.num_q_heads + it.kvh * G + (R - jrow * G)) * D;
 #pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
-                    float o[32];
-                    pkv::tc::tmem_ld32(t_lane + o_col + c, o);
+            for (int c = 0; c < D / 2; c += 32) {
+                float a[32], b[32];
+                const uint32_t col = (uint32_t)(team * (D / 2) + c);
+                pkv::tc::tmem_ld32(t_lane + kOCol + col, a);
+                if (nkt >= 2) {
+                    pkv::tc::tmem_ld32(t_lane + kOCol + D + col, b);
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 32; i++) o[i] *= alpha;
-                    pkv::tc::tmem_st32(t_lane + o_col + c, o);
+                    for (int e = 0; e < 32; e++) b[e] = 0.f;
+                }
+                if (row_ok && !failed) {
+                    alignas(16) OutT v[32];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) pkv::store2(v + e, a[e] * g0 + b[e] * g1, a[e + 1] * g0 + b[e + 1] * g1);
+                    constexpr int kVec = 32 * (int)sizeof(OutT) / 16;
+#pragma unroll
+                    for (int k = 0; k < kVec; k++)
+                        reinterpret_cast<uint4 *>(orow + col)[k] = reinterpret_cast<const uint4 *>(v)[k];
                 }
             }
-            // P = 2^(s * scale - m) as bf16 pairs over the first 64 columns
-            const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < BN; c += 64) {
-                float pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    const float x0 = fmaf(sv[c + 2 * i], p.scale_log2, nbase);
-                    const float x1 = fmaf(sv[c + 2 * i + 1], p.scale_log2, nbase);
-                    // one pair in four on the FMA pipe, the rest on the special-function unit
-                    const float e0 = (i & 3) == 3 ? pkv::tc::exp2_poly(x0) : pkv::tc::ex2(x0);
-                    const float e1 = (i & 3) == 3 ? pkv::tc::exp2_poly(x1) : pkv::tc::ex2(x1);
-                    ls[(2 * i) & 3] += e0;
-                    ls[(2 * i + 1) & 3] += e1;
-                    pk[i] = __uint_as_float(pkv::pack_bf16(e0, e1));
-                }
-                // keys c .. c+63 -> P columns c/2 .. c/2+31
-                pkv::tc::tmem_st32(t_lane + s_col + c / 2, pk);
-            }
-            lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // the O reads are done before the next item's first PV may overwrite
             pkv::tc::fence_before_sync();
-            pkv::tc::mbar_arrive(bar_pfull + team);
-        }
-
-        // merge the two teams: exchange (m, l) with the partner thread of the same row
-        const int my_tiles = nkt > team ? (nkt - team + 1) / 2 : 0;
-        if (my_tiles > 0) {
-            const int last = team + 2 * (my_tiles - 1);
-            wait(bar_o + team, (unsigned)((last >> 1) & 1));
-            pkv::tc::fence_after_sync();
-        }
-        red[(team * 2 + 0) * BM + row] = m_used;
-        red[(team * 2 + 1) * BM + row] = lsum;
-        asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
-        const float m0 = red[0 * BM + row], l0 = red[1 * BM + row];
-        const float m1 = red[2 * BM + row], l1 = red[3 * BM + row];
-        const float M = fmaxf(m0, m1);
-        const float f0 = M == -INFINITY ? 0.f : pkv::tc::ex2(m0 - M);
-        const float f1 = (M == -INFINITY || nkt < 2) ? 0.f : pkv::tc::ex2(m1 - M);
-        const float ltot = l0 * f0 + l1 * f1;
-        const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
-        const float g0 = f0 * inv, g1 = f1 * inv;
-        // Output: each thread puts its half row (team 0 columns 0..63, team 1
-        // columns 64..127) into shared memory, and the 256 softmax threads
-        // then write whole rows with coalesced 16-byte stores.  The staging
-        // area is the Q and K region: every S has completed by now (the last
-        // one was issued before either team's last PV), whereas the other
-        // team's last PV may still be reading V.
-        constexpr int kRowBytes = D * (int)sizeof(OutT);
-        constexpr int kStride = kRowBytes + 16;  // padded rows
-        static_assert(BM * kStride <= kOffV, "output staging must not reach the V ring");
-        unsigned char *stage = smem + kOffQ;
-#pragma unroll 1
-        for (int c = 0; c < D / 2; c += 32) {
-            float a[32], b[32];
-            const uint32_t col = (uint32_t)(team * (D / 2) + c);
-            pkv::tc::tmem_ld32(t_lane + kOCol + col, a);
-            if (nkt >= 2) {
-                pkv::tc::tmem_ld32(t_lane + kOCol + D + col, b);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; i++) b[i] = 0.f;
-            }
-            OutT *srow = reinterpret_cast<OutT *>(stage + row * kStride) + col;
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) pkv::store2(srow + i, a[i] * g0 + b[i] * g1, a[i + 1] * g0 + b[i + 1] * g1);
-        }
-        asm volatile("bar.sync 6, %0;\n" ::"r"(2 * kTeamThreads) : "memory");
-        constexpr int kChunks = kRowBytes / 16;  // 16-byte chunks per row
-        for (int i = tid; i < BM * kChunks; i += 2 * kTeamThreads) {
-            const int r = i / kChunks, ch = i - r * kChunks;
-            const int Rr = tile * BM + r;
-            const int jr = Rr / G;
-            if (jr < n && !failed) {
-                unsigned char *dst = reinterpret_cast<unsigned char *>(static_cast<OutT *>(p.out)) +
-                                     ((size_t)(q0 + jr) * p.num_q_heads + kvh * G + (Rr - jr * G)) * kRowBytes +
-                                     ch * 16;
-                *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(stage + r * kStride + ch * 16);
-            }
+            advance(it);
         }
     }
 
@@ -530,12 +686,26 @@ int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaS
         if (e != cudaSuccess) return check_launch("prefill_tc: set shared memory size");
         attr_set[which][dev] = true;
     }
-    const int tiles = (p.max_q_len * p.group + BM - 1) / BM;
-    dim3 grid((unsigned)tiles, (unsigned)p.num_kv_heads, (unsigned)num_seqs);
+    PrefillParams pp = p;
+    pp.num_seqs = num_seqs;
+    pp.tiles_per_seq = (p.max_q_len * p.group + BM - 1) / BM;
+    const long long items = (long long)num_seqs * p.num_kv_heads * pp.tiles_per_seq;
+    if (items > 0x7fff0000LL) return fail(PKV_ERR_INVALID, "prefill: too many q tiles");
+    pp.num_items = (int)items;
+    cudaError_t me = cudaMemsetAsync(pp.item_counter, 0, sizeof(unsigned long long), st);
+    if (me != cudaSuccess) return fail(PKV_ERR_CUDA, "prefill: clear item counter: %s", cudaGetErrorString(me));
+    static int sms[64] = {0};
+    int nsm = 148;
+    if (dev >= 0 && dev < 64) {
+        if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (sms[dev] > 0) nsm = sms[dev];
+    }
+    // one persistent CTA per SM (its shared memory allows no second)
+    const unsigned grid = (unsigned)(pp.num_items < nsm ? pp.num_items : nsm);
     if (which == 0)
-        prefill_tc_kernel<float><<<grid, kThreads, kSmemBytes, st>>>(p, tk, tv);
+        prefill_tc_kernel<float><<<grid, kThreads, kSmemBytes, st>>>(pp, tk, tv);
     else
-        prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(p, tk, tv);
+        prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(pp, tk, tv);
     return check_launch("prefill_tc");
 }
 
