@@ -573,7 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             red[(team * 2 + 0) * BM + row] = m_used;
             red[(team * 2 + 1) * BM + row] = lsum;
+            // The fences order this thread's later reads of both teams' O
+            // after the completion its partner observed; without them the
+            // first tcgen05.ld waited microseconds.
+            pkv::tc::fence_before_sync();
             asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
+            pkv::tc::fence_after_sync();
             const float m0 = red[0 * BM + row], l0 = red[1 * BM + row];
             const float m1 = red[2 * BM + row], l1 = red[3 * BM + row];
             const float M = fmaxf(m0, m1);
