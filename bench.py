@@ -295,45 +295,71 @@ def time_device(step: Step, steps: int, warmup: int, world: int):
     return span_ms, serial_ms, per_call, wall
 
 
+def _pack(tensors, device):
+    """One uint8 buffer holding every tensor (each at a 256-byte aligned
+    offset) and views of it with the tensors' dtypes and shapes."""
+    offs, total = [], 0
+    for x in tensors:
+        offs.append(total)
+        total += (x.numel() * x.element_size() + 255) // 256 * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=device,
+                      pin_memory=(device == "cpu" and torch.cuda.is_available()))
+    views = [buf[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+             for o, x in zip(offs, tensors)]
+    return buf, views
+
+
 def time_e2e(step: Step, steps: int, warmup: int, world: int):
     """Same step through the public API with host buffers: each step copies its
-    inputs from pinned host memory and reads the outputs back."""
+    inputs from pinned host memory and reads the outputs back.  The inputs sit
+    in one pinned staging buffer (as a serving loop would assemble them) and
+    cross in one copy; the outputs come back in one copy."""
     b = step.b
     names = ["q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens"]
     if step.has_copy:
         names.append("copy_pairs")
     if step.pout is not None:
         names += ["prefill_q", "prefill_cu_q_lens", "prefill_block_tables", "prefill_context_lens"]
-    host = {n: getattr(b, n).pin_memory() for n in names}
-    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    pout_h = None if step.pout is None else torch.empty(step.pout.shape,
-                                                        dtype=step.pout.dtype).pin_memory()
-    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = out_h.numel() * out_h.element_size() + (
-        0 if pout_h is None else pout_h.numel() * pout_h.element_size())
+    src = [getattr(b, n).contiguous() for n in names]
+    hin, hviews = _pack(src, "cpu")
+    for v, x in zip(hviews, src):
+        v.copy_(x)
+    din, dviews = _pack(src, step.dev)
+    outs = [step.out] + ([] if step.pout is None else [step.pout])
+    dout, doviews = _pack(outs, step.dev)
+    hout = torch.empty(dout.numel(), dtype=torch.uint8).pin_memory()
+    saved = ({n: step.t[n] for n in names}, step.out, step.pout)
+    for n, v in zip(names, dviews):  # the calls read the packed device inputs
+        step.t[n] = v
+    step.out = doviews[0]
+    if step.pout is not None:
+        step.pout = doviews[1]
+    h2d = sum(x.numel() * x.element_size() for x in src)
+    d2h = sum(x.numel() * x.element_size() for x in outs)
     calls = step.calls()
 
     def one():
-        for n in names:
-            step.t[n].copy_(host[n], non_blocking=True)
+        din.copy_(hin, non_blocking=True)
         for _, fn in calls:
             fn()
-        out_h.copy_(step.out, non_blocking=True)
-        if pout_h is not None:
-            pout_h.copy_(step.pout, non_blocking=True)
+        hout.copy_(dout, non_blocking=True)
 
-    for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    try:
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    finally:
+        step.t.update(saved[0])
+        step.out, step.pout = saved[1], saved[2]
     return e0.elapsed_time(e1), h2d, d2h
 
 
