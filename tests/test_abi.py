@@ -53,6 +53,15 @@ def test_decode_workspace_sizes(lib):
     assert b"multiple of 16" in lib.pkv_last_error_string()
 
 
+def test_prefill_workspace_sizes(lib):
+    # head_dim 128 (the tcgen05 kernel): one 8-byte work-item counter,
+    # rounded to 256 bytes; head_dim 64 needs none
+    assert pkv.prefill_workspace_bytes(2, 1024, 32, 8, 128, 512, 3584) == 256
+    assert pkv.prefill_workspace_bytes(2, 1024, 8, 8, 64, 512, 3584) == 0
+    with pytest.raises(pkv.PkvError):
+        pkv.prefill_workspace_bytes(2, 1024, 32, 8, 96, 512, 3584)
+
+
 def test_decode_partition_choice(lib):
     assert pkv.decode_partition_size(64, 8, 4096, 256) == 256
     # adaptive: the largest partition that still leaves ~4 blocks per SM, for
