@@ -174,7 +174,8 @@ class ClockSampler:
 class Step:
     """Device-resident inputs and the calls of one step of the hot path."""
 
-    def __init__(self, batch: W.Batch, dev: str, partition: int = 0, unfused: bool = False):
+    def __init__(self, batch: W.Batch, dev: str, partition: int = 0, unfused: bool = False,
+                 no_cascade: bool = False):
         import paged_kv_cache_297_gb300 as pkv
         self.pkv = pkv
         self.b = batch
@@ -204,6 +205,14 @@ class Step:
         # decode-only steps whose new tokens are exactly one per sequence at
         # position L-1 take the fused append + decode call
         self.fused = (not unfused) and batch.prefill_q is None and self._one_token_per_seq()
+        # a batch over one shared prefix takes the cascade: the prefix once for
+        # all queries on the tensor cores, then each sequence's own tokens
+        self.prefix_len = 16 * int(batch.meta.get("prefix_blocks", 0))
+        self.cascade = (self.fused and not no_cascade and self.prefix_len > 0
+                        and batch.dtype == torch.bfloat16 and d == 128)
+        if self.cascade:
+            ws = pkv.decode_shared_prefix_workspace_bytes(S, Hq, d, self.max_ctx, self.prefix_len, partition)
+            self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
 
     def _one_token_per_seq(self) -> bool:
         b = self.b
@@ -216,7 +225,9 @@ class Step:
 
     def launches_per_step(self) -> int:
         n = 1 if self.fused else 2  # (append +) decode partitions
-        if self.max_ctx > self.part_used:
+        if self.cascade:
+            n += 2  # shared-prefix kernel, log-sum-exp merge
+        elif self.max_ctx > self.part_used:
             n += 1  # log-sum-exp reduce
         if self.has_copy:
             n += 1
@@ -231,6 +242,12 @@ class Step:
         if self.has_copy:
             out.append(("copy_blocks", lambda: pkv.copy_blocks(t["copy_pairs"], t["k_cache"],
                                                                t["v_cache"])))
+        if self.cascade:
+            out.append(("decode", lambda: pkv.decode_shared_prefix(
+                t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"], b.scale,
+                self.out, self.prefix_len, k_new=t["k_new"], v_new=t["v_new"],
+                max_context_len=self.max_ctx, partition_size=self.partition, workspace=self.ws)))
+            return out
         if self.fused:
             out.append(("decode", lambda: pkv.decode_step(
                 t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["block_tables"],
@@ -397,7 +414,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     batch = W.make_batch(args.workload, poison=False)
-    step = Step(batch, dev, args.partition, args.unfused)
+    step = Step(batch, dev, args.partition, args.unfused, args.no_cascade)
     peaks = read_peaks()
 
     clocks = ClockSampler(local)
@@ -421,10 +438,17 @@ def run_ours(args):
     # the fused call also writes the appended K and V rows (it reads them from
     # k_new/v_new instead of the cache, which the KV count already covers)
     dec_bytes = db["total"] + (2 * S * batch.spec.num_kv_heads * d * elem if step.fused else 0)
+    if step.cascade:
+        # the prefix's K/V are read once, not once per sequence: count them once
+        dec_bytes -= step.prefix_len * (S - 1) * 2 * batch.spec.num_kv_heads * d * elem
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
-    kname = "decode_step" if step.fused else "paged_attention_decode"
+    kname = ("decode_shared_prefix" if step.cascade else "decode_step" if step.fused
+             else "paged_attention_decode")
     traffic = recorded_traffic(kname, args.workload, DECODE_SOURCES)
-    roofline = {"kernel": ("decode_step (fused append + partition kernel + log-sum-exp reduce)"
+    roofline = {"kernel": ("decode_shared_prefix (fused append; shared-prefix tile on the tensor cores, "
+                           "partition kernel over each sequence's own tokens, log-sum-exp merge; bytes "
+                           "count the prefix once)" if step.cascade else
+                           "decode_step (fused append + partition kernel + log-sum-exp reduce)"
                            if step.fused else
                            "paged_attention_decode (partition kernel + log-sum-exp reduce)"),
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
@@ -537,6 +561,8 @@ def main(argv=None):
                     help="decode split-K partition in tokens (0: the library's adaptive choice)")
     ap.add_argument("--unfused", action="store_true",
                     help="separate append and decode calls even where the fused step applies")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="plain decode even where the batch shares a prefix")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -209,6 +209,48 @@ int pkv_paged_attention_decode_no_alloc(const void *q, const void *k_cache, cons
                                         int out_dtype, void *stream);
 
 /*
+ * Workspace (device bytes) that pkv_paged_attention_decode_shared_prefix
+ * needs with these sizes (head_dim 128; partition_size 0 covers every
+ * partition the call may choose).  *bytes is a host pointer.
+ */
+int pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                             int max_context_len, int prefix_len, int partition_size,
+                                             size_t *bytes);
+
+/*
+ * Decode of a batch whose sequences all begin with the same prefix_len tokens
+ * stored in the same physical blocks (a shared system prompt; ainews
+ * "PagedAttention": blocks of a common prefix are shared, copy-on-write on
+ * divergence).  Same result as pkv_decode_step (k_new, v_new given) or
+ * pkv_paged_attention_decode (both NULL) on these inputs, computed as a
+ * cascade:
+ *   1. the prefix once for every query of the batch: the S * Hq query rows
+ *      against the prefix keys of block_tables row 0 form a dense tile for
+ *      the tcgen05 tensor cores (the chunked-prefill kernel in a non-causal
+ *      mode), giving each row's (m, l, O) over the prefix;
+ *   2. each sequence's tokens [prefix_len, L_s) with the partitioned decode
+ *      kernel (and the fused append of the new token when k_new is given);
+ *   3. the log-sum-exp merge of 1 and 2 (chengxuchu #47 section 2.1: the
+ *      softmax over the union of the key sets).
+ * Contract, not checked: rows 0 .. prefix_len/16 - 1 of every block table
+ * are the same block ids.  Requirements: bf16 caches, head_dim 128, 1..16 q
+ * heads per kv head, prefix_len a positive multiple of 16 below the context
+ * bound, and every L_s > prefix_len (else PKV_STATUS_BAD_LENGTH and that
+ * sequence's output is undefined).  Other arguments as
+ * pkv_paged_attention_decode / pkv_decode_step; workspace of
+ * pkv_decode_shared_prefix_workspace_bytes(...) bytes, 256-byte aligned,
+ * needing no initialisation.
+ */
+int pkv_paged_attention_decode_shared_prefix(const void *q, const void *k_new, const void *v_new,
+                                             void *k_cache, void *v_cache, const int32_t *block_tables,
+                                             int max_blocks_per_seq, const int32_t *context_lens,
+                                             int num_seqs, int num_q_heads, int num_kv_heads,
+                                             int head_dim, int block_size, int num_blocks,
+                                             int max_context_len, int prefix_len, int partition_size,
+                                             float scale, void *out, int dtype, int out_dtype,
+                                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Workspace (device bytes) that pkv_paged_attention_prefill_chunk needs:
  * 256 for head_dim 128 (the bf16 kernel's work-item counter), else 0.
  */

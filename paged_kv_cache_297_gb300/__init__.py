@@ -27,7 +27,7 @@ import torch
 __all__ = [
     "BLOCK_SIZE", "DEFAULT_PARTITION", "PkvError", "load", "library_path", "kv_append",
     "copy_blocks", "decode_workspace_bytes", "decode_partition_size", "paged_attention_decode",
-    "decode_step",
+    "decode_step", "decode_shared_prefix_workspace_bytes", "decode_shared_prefix",
     "prefill_workspace_bytes", "paged_attention_prefill_chunk", "get_status", "STATUS_BITS",
     "EXPORTED",
 ]
@@ -42,6 +42,7 @@ STATUS_BITS = {"bad_slot": 1, "bad_block": 2, "bad_length": 4, "bad_qlen": 8, "i
 EXPORTED = (
     "pkv_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes", "pkv_decode_partition_size",
     "pkv_paged_attention_decode", "pkv_decode_step", "pkv_paged_attention_decode_no_alloc",
+    "pkv_decode_shared_prefix_workspace_bytes", "pkv_paged_attention_decode_shared_prefix",
     "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_last_error_string",
     "pkv_version",
@@ -83,6 +84,9 @@ def load():
     lib.pkv_decode_step.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I, I, P, SZ, P]
     lib.pkv_paged_attention_decode_no_alloc.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I,
                                                         I, F, P, I, I, P]
+    lib.pkv_decode_shared_prefix_workspace_bytes.argtypes = [I, I, I, I, I, I, ctypes.POINTER(SZ)]
+    lib.pkv_paged_attention_decode_shared_prefix.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I,
+                                                             I, F, P, I, I, P, SZ, P]
     lib.pkv_prefill_workspace_bytes.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
     lib.pkv_paged_attention_prefill_chunk.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, I,
                                                       I, F, P, I, I, P, SZ, P]
@@ -231,6 +235,52 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, s
         _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, d, bs, NB,
         int(max_context_len), int(partition_size), float(scale), _dev(out, "out"), _dt(q), _dt(out),
         ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def decode_shared_prefix_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
+                                         prefix_len, partition_size: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().pkv_decode_shared_prefix_workspace_bytes(
+        int(num_seqs), int(num_q_heads), int(head_dim), int(max_context_len), int(prefix_len),
+        int(partition_size), ctypes.byref(out)))
+    return int(out.value)
+
+
+def decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale, out, prefix_len: int,
+                         k_new=None, v_new=None, max_context_len: Optional[int] = None,
+                         partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """Decode of a batch whose sequences share their first ``prefix_len``
+    tokens (same physical blocks): the prefix once for all queries on the
+    tensor cores, each sequence's own tokens by the partitioned kernel, then a
+    log-sum-exp merge.  With ``k_new``/``v_new`` (``[S, Hkv, d]``) the new
+    tokens are appended at position L-1 first, as in :func:`decode_step`."""
+    NB, Hkv, bs, d = _cache_dims(k_cache, v_cache)
+    S, Hq, dq = q.shape
+    if dq != d or q.dtype != k_cache.dtype or out.shape != q.shape:
+        raise ValueError("q/out must be [S, Hq, head_dim] in the cache dtype")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None and (k_new.shape != (S, Hkv, d) or v_new.shape != k_new.shape
+                              or k_new.dtype != k_cache.dtype):
+        raise ValueError("k_new/v_new must be [S, num_kv_heads, head_dim] in the cache dtype")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks] and context_lens [S]")
+    mb = int(block_tables.shape[1])
+    if max_context_len is None:
+        max_context_len = mb * bs
+    need = decode_shared_prefix_workspace_bytes(S, Hq, d, max_context_len, prefix_len, partition_size)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(load().pkv_paged_attention_decode_shared_prefix(
+        _dev(q, "q"), None if k_new is None else _dev(k_new, "k_new"),
+        None if v_new is None else _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables", torch.int32), mb,
+        _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, d, bs, NB,
+        int(max_context_len), int(prefix_len), int(partition_size), float(scale), _dev(out, "out"),
+        _dt(q), _dt(out), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return out
 
 

@@ -16,6 +16,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "prefill_common.cuh"
 
 namespace {
 
@@ -50,7 +51,18 @@ struct DecodeParams {
     // written into the cache by the CTA(s) of the last partition, or nullptr
     const void *k_new;
     const void *v_new;
+    // shared prefix: tokens [0, prefix_len) of every sequence are handled
+    // elsewhere (their merged state is partial slot 0); the partitions here
+    // cover [prefix_len, L) and write slots 1, 2, ...  0 = no prefix.
+    int prefix_len;
 };
+
+// Partitions of the tokens this launch covers for a sequence of L tokens.
+__device__ __forceinline__ int own_parts(const DecodeParams &p, int L) {
+    if (p.prefix_len == 0) return L > 0 ? (L + p.partition - 1) / p.partition : 1;
+    const int suf = L - p.prefix_len;
+    return suf > 0 ? (suf + p.partition - 1) / p.partition : 0;
+}
 
 // Write the new token of sequence s, kv head kvh, at logical position L-1.
 // Called by every thread of a CTA that owns the partition holding L-1,
@@ -116,13 +128,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
 
     const int L = clamp_len(p.context_lens[s], p.len_cap, p.status,
                             part == 0 && blockIdx.x == 0 && threadIdx.x == 0);
-    const int nparts = L > 0 ? (L + p.partition - 1) / p.partition : 1;
+    if (p.prefix_len && L <= p.prefix_len && part == 0 && blockIdx.x == 0 && threadIdx.x == 0)
+        pkv::flag(p.status, PKV_STATUS_BAD_LENGTH);  // no private token after the shared prefix
+    const int nparts = own_parts(p, L);
     if (part >= nparts) return;
+    const int slot0 = p.prefix_len ? 1 : 0;  // partial slot 0 holds the shared prefix
+    const int nslots = slot0 + nparts;
 
     const int h0 = kvh * p.group + chunk * kRows;
     const int rows = min(kRows, p.group - chunk * kRows);
-    const int t_end = min(L, (part + 1) * p.partition);
-    const int blk_begin = (part * p.partition) / kBlock;
+    const int t_begin = p.prefix_len + part * p.partition;
+    const int t_end = min(L, t_begin + p.partition);
+    const int blk_begin = t_begin / kBlock;
     const int nblk = (t_end + kBlock - 1) / kBlock - blk_begin;
     const int wb = blk_begin + (nblk * warp) / kWarps;
     const int we = blk_begin + (nblk * (warp + 1)) / kWarps;
@@ -332,10 +349,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
             }
         }
         const size_t orow = (size_t)s * p.num_q_heads + h0 + r;
-        if (nparts == 1) {
+        if (nslots == 1) {
             pkv::store1(static_cast<OutT *>(p.out) + orow * D + c, lsum > 0.f ? acc / lsum : 0.f);
         } else {
-            const size_t prow = orow * p.max_parts + part;
+            const size_t prow = orow * p.max_parts + slot0 + part;
             p.part_o[prow * D + c] = acc;
             if (c == 0) {
                 p.part_ml[prow * 2] = M;
@@ -438,8 +455,10 @@ __global__ void __launch_bounds__(kThreads) decode_cuda_core_kernel(const Decode
     const int h = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
     const int L = clamp_len(p.context_lens[s], p.len_cap, p.status,
                             part == 0 && h == 0 && threadIdx.x == 0);
-    const int nparts = L > 0 ? (L + p.partition - 1) / p.partition : 1;
+    const int nparts = own_parts(p, L);
     if (part >= nparts) return;
+    const int slot0 = p.prefix_len ? 1 : 0;
+    const int nslots = slot0 + nparts;
     const int kvh = h / p.group;
     if (p.k_new && part == nparts - 1 && L > 0) {
         // every q head of the group writes the same bytes for its kv head
@@ -449,16 +468,16 @@ __global__ void __launch_bounds__(kThreads) decode_cuda_core_kernel(const Decode
     const T *qrow = static_cast<const T *>(p.q) + ((size_t)s * p.num_q_heads + h) * D;
     float m, l, acc;
     rows_cuda_core<T>(qrow, static_cast<const T *>(p.k_cache), static_cast<const T *>(p.v_cache),
-                      p.block_tables + (size_t)s * p.max_blocks, part * p.partition,
-                      min(L, (part + 1) * p.partition), p.num_blocks, p.num_kv_heads, kvh, D,
+                      p.block_tables + (size_t)s * p.max_blocks, p.prefix_len + part * p.partition,
+                      min(L, p.prefix_len + (part + 1) * p.partition), p.num_blocks, p.num_kv_heads, kvh, D,
                       p.scale_log2, p.status, sq, sp, sb, red, m, l, acc);
     const int c = threadIdx.x;
     if (c >= D) return;
     const size_t orow = (size_t)s * p.num_q_heads + h;
-    if (nparts == 1) {
+    if (nslots == 1) {
         pkv::store1(static_cast<OutT *>(p.out) + orow * D + c, l > 0.f ? acc / l : 0.f);
     } else {
-        const size_t prow = orow * p.max_parts + part;
+        const size_t prow = orow * p.max_parts + slot0 + part;
         p.part_o[prow * D + c] = acc;
         if (c == 0) {
             p.part_ml[prow * 2] = m;
@@ -483,7 +502,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
     if (row >= rows) return;
     const int s = row / p.num_q_heads;
     const int L = clamp_len(p.context_lens[s], p.len_cap, p.status, false);
-    const int nparts = L > 0 ? (L + p.partition - 1) / p.partition : 1;
+    const int nparts = (p.prefix_len ? 1 : 0) + own_parts(p, L);  // partial slots of this row
     if (nparts <= 1) return;
     const size_t prow = (size_t)row * p.max_parts;
     const float *ml = p.part_ml + prow * 2;
@@ -590,7 +609,9 @@ int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
             return pkv::check_launch("decode: set shared memory size");
         attr_set[dev] = true;
     }
-    dim3 grid((unsigned)(p.num_kv_heads * p.head_chunks), (unsigned)num_seqs, (unsigned)p.max_parts);
+    // (with a shared prefix, partial slot 0 comes from another kernel)
+    dim3 grid((unsigned)(p.num_kv_heads * p.head_chunks), (unsigned)num_seqs,
+              (unsigned)(p.max_parts - (p.prefix_len ? 1 : 0)));
     cudaError_t e = pkv::launch_dependent(decode_bf16_kernel<D, OutT>, grid, dim3(kThreads), bytes, st, p);
     if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "decode_bf16: %s", cudaGetErrorString(e));
     return pkv::check_launch("decode_bf16");
@@ -747,4 +768,137 @@ extern "C" int pkv_decode_step(const void *q, const void *k_new, const void *v_n
     return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len,
                        partition_size, scale, out, dtype, out_dtype, workspace, workspace_bytes, stream);
+}
+
+// ----------------------------------------------------------------------------
+// decode over a prefix shared by the whole batch (cascade)
+// ----------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t kCounterBytes = 256;  // the prefix kernel's work-item counter
+
+int shared_prefix_parts(int len_cap, int prefix_len, int partition) {
+    const int suf = len_cap - prefix_len;
+    return 1 + (suf > 0 ? (suf + partition - 1) / partition : 0);
+}
+
+}  // namespace
+
+extern "C" int pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                                        int max_context_len, int prefix_len, int partition_size,
+                                                        size_t *bytes) {
+    int part;
+    int rc = resolve_partition(partition_size, &part);
+    if (rc) return rc;
+    if (!bytes || num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || head_dim != 128 || prefix_len <= 0 ||
+        prefix_len % kBlock != 0 || prefix_len > max_context_len)
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix_workspace_bytes: bad argument");
+    // partition_size 0 may choose any adaptive size; 512 needs the most slots
+    *bytes = workspace_for(num_seqs, num_q_heads, head_dim, shared_prefix_parts(max_context_len, prefix_len, part)) +
+             kCounterBytes;
+    return PKV_OK;
+}
+
+extern "C" int pkv_paged_attention_decode_shared_prefix(
+    const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int num_blocks, int max_context_len, int prefix_len, int partition_size,
+    float scale, void *out, int dtype, int out_dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    int part;
+    int rc = resolve_partition(partition_size, &part);
+    if (rc) return rc;
+    if (block_size != kBlock) return pkv::fail(PKV_ERR_INVALID, "block_size must be 16 (got %d)", block_size);
+    if (dtype != PKV_BF16 || head_dim != 128)
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: bf16 caches with head_dim 128 only");
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
+        return pkv::fail(PKV_ERR_INVALID, "bad out_dtype %d", out_dtype);
+    if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0)
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: negative size");
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        num_q_heads / num_kv_heads > kRows)
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: num_q_heads must be 1..16 times num_kv_heads");
+    if (!(scale == scale)) return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: scale is NaN");
+    const long long cap = (long long)max_blocks_per_seq * kBlock;
+    const int len_cap = (int)(cap < max_context_len ? cap : max_context_len);
+    if (prefix_len <= 0 || prefix_len % kBlock != 0 || prefix_len >= len_cap)
+        return pkv::fail(PKV_ERR_INVALID,
+                         "decode_shared_prefix: prefix_len (%d) must be a positive multiple of 16 below the "
+                         "context bound (%d)", prefix_len, len_cap);
+    if (num_seqs == 0) return PKV_OK;
+    if (num_seqs > 65535) return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: at most 65535 sequences per call");
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: null pointer");
+    if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) || !pkv::aligned16(out))
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: q, caches and out must be 16-byte aligned");
+    if ((k_new || v_new) && (!k_new || !v_new || !pkv::aligned16(k_new) || !pkv::aligned16(v_new)))
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: k_new and v_new must both be 16-byte aligned");
+    if (partition_size == 0) part = adaptive_partition(num_seqs, num_kv_heads, len_cap - prefix_len);
+    const int max_parts = shared_prefix_parts(len_cap, prefix_len, part);
+    if (max_parts > 65535) return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: too many partitions");
+    const size_t rows = (size_t)num_seqs * num_q_heads * max_parts;
+    const size_t part_bytes = workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
+    if (!workspace || workspace_bytes < part_bytes + kCounterBytes)
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: workspace of %zu bytes needed, %zu given",
+                         part_bytes + kCounterBytes, workspace_bytes);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return pkv::fail(PKV_ERR_INVALID, "decode_shared_prefix: workspace must be 256-byte aligned");
+    char *ws = static_cast<char *>(workspace);
+    float *part_o = reinterpret_cast<float *>(ws);
+    float *part_ml = reinterpret_cast<float *>(ws + align256(rows * head_dim * sizeof(float)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // 1. the shared prefix, once for every query of the batch: a dense tile
+    //    on the tensor cores (partial slot 0 of every row)
+    pkv::PrefillParams pp{};
+    pp.q = q;
+    pp.k_cache = k_cache;
+    pp.v_cache = v_cache;
+    pp.block_tables = block_tables;  // row 0 holds the prefix blocks
+    pp.out = out;
+    pp.max_blocks = max_blocks_per_seq;
+    pp.num_q_heads = num_q_heads;
+    pp.num_kv_heads = num_kv_heads;
+    pp.group = num_q_heads / num_kv_heads;
+    pp.num_blocks = num_blocks;
+    pp.len_cap = len_cap;
+    pp.max_q_len = num_seqs;
+    pp.total_q = num_seqs;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+    pp.status = pkv::status_ptr();
+    pp.item_counter = reinterpret_cast<unsigned long long *>(ws + part_bytes);
+    pp.prefix_len = prefix_len;
+    pp.part_o = part_o;
+    pp.part_ml = part_ml;
+    pp.part_stride = max_parts;
+    rc = pkv::launch_prefill_tc(pp, 1, out_dtype, st);
+    if (rc) return rc;
+
+    // 2. each sequence's own tokens after the prefix (slots 1, 2, ...), with
+    //    the optional fused append, then 3. the log-sum-exp merge of all slots
+    DecodeParams p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = out;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_q_heads / num_kv_heads;
+    p.head_chunks = (p.group + kRows - 1) / kRows;
+    p.num_blocks = num_blocks;
+    p.len_cap = len_cap;
+    p.partition = part;
+    p.max_parts = max_parts;
+    p.scale_log2 = pp.scale_log2;
+    p.status = pp.status;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.prefix_len = prefix_len;
+    p.part_o = part_o;
+    p.part_ml = part_ml;
+    return out_dtype == PKV_F32 ? launch_decode<float>(p, num_seqs, head_dim, dtype, st)
+                                : launch_decode<__nv_bfloat16>(p, num_seqs, head_dim, dtype, st);
 }

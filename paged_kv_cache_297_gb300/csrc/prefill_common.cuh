@@ -30,6 +30,15 @@ struct PrefillParams {
     int tiles_per_seq;
     int num_items;
     unsigned long long *item_counter;
+    // shared-prefix mode (prefix_len > 0): the "chunk" is the batch's decode
+    // queries (one position per sequence, max_q_len = sequences), every one
+    // attends to keys [0, prefix_len) of block table row 0, and the result
+    // is written unnormalised as partial slot 0 of each decode row:
+    // part_o [rows][part_stride][D], part_ml [rows][part_stride][2]
+    int prefix_len;
+    float *part_o;
+    float *part_ml;
+    int part_stride;
 };
 
 // tcgen05 kernel (prefill_tc.cu): bf16 caches with head_dim 128.

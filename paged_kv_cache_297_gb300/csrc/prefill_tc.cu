@@ -139,11 +139,14 @@ __device__ __forceinline__ ItemInfo item_info(const PrefillParams &p, int4 v) {
     it.tile = p.tiles_per_seq - 1 - rem / p.num_kv_heads;
     it.kvh = rem - (rem / p.num_kv_heads) * p.num_kv_heads;
     it.bad_len = !it.stop && (it.L < 0 || it.L > p.len_cap);
-    it.bad_qlen = !it.stop && !it.bad_len &&
+    it.bad_qlen = !it.stop && !it.bad_len && !p.prefix_len &&
                   (it.q0 < 0 || it.n < 0 || it.n > it.L || it.n > p.max_q_len || it.q0 + it.n > p.total_q);
     it.skip = it.stop || it.bad_len || it.bad_qlen || it.tile * BM >= it.n * p.group;
     if (it.skip) {
         it.nkt = it.kv_end = it.mask_from = 0;
+    } else if (p.prefix_len) {  // every query sees the whole shared prefix, nothing after it
+        it.kv_end = it.mask_from = p.prefix_len;
+        it.nkt = (p.prefix_len + BN - 1) / BN;
     } else {
         const int prior = it.L - it.n;
         const int j_last = min(it.n - 1, (it.tile * BM + BM - 1) / p.group);
@@ -266,7 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int4 v = make_int4(item, 0, 0, 0);
                 if (lane == 0) {
                     if (i >= 2) wait(bar_item_empty + (i & 1), (unsigned)(((i >> 1) - 1) & 1));
-                    if (item < p.num_items) {
+                    if (item < p.num_items && p.prefix_len) {
+                        v.y = 0;                // the decode queries, one "position" per sequence
+                        v.z = p.max_q_len;
+                        v.w = p.prefix_len;
+                    } else if (item < p.num_items) {
                         const int s = p.num_seqs - 1 - item / (p.num_kv_heads * p.tiles_per_seq);
                         v.y = p.cu_q_lens[s];
                         v.z = p.cu_q_lens[s + 1] - v.y;
@@ -471,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int R = it.tile * BM + row;
             const int jrow = R / G;
             const bool row_ok = jrow < it.n;
-            const int pos = row_ok ? it.L - it.n + jrow : -1;
+            // last visible key: causal within the chunk, or the whole shared prefix
+            const int pos = !row_ok ? -1 : p.prefix_len ? p.prefix_len - 1 : it.L - it.n + jrow;
             float m_used = -INFINITY, lsum = 0.f;
             const int tb = team ? team_base1 : team_base0;  // this team's tiles before this item
 
@@ -603,7 +611,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; e++) b[e] = 0.f;
                 }
-                if (row_ok && !failed) {
+                if (row_ok && !failed && p.prefix_len) {
+                    // shared-prefix mode: the unnormalised state (M, L, O)
+                    // goes to partial slot 0 of the decode row (s = jrow)
+                    const size_t prow = ((size_t)jrow * p.num_q_heads + it.kvh * G + (R - jrow * G)) * p.part_stride;
+                    float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * D + col);
+#pragma unroll
+                    for (int k = 0; k < 8; k++)
+                        po[k] = make_float4(a[4 * k] * f0 + b[4 * k] * f1, a[4 * k + 1] * f0 + b[4 * k + 1] * f1,
+                                            a[4 * k + 2] * f0 + b[4 * k + 2] * f1, a[4 * k + 3] * f0 + b[4 * k + 3] * f1);
+                    if (team == 0 && c == 0) *reinterpret_cast<float2 *>(p.part_ml + prow * 2) = make_float2(M, ltot);
+                } else if (row_ok && !failed) {
                     alignas(16) OutT v[32];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) pkv::store2(v + e, a[e] * g0 + b[e] * g1, a[e + 1] * g0 + b[e + 1] * g1);

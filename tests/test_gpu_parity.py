@@ -314,3 +314,46 @@ def test_python_layer_rejects_bad_tensors():
     with pytest.raises(pkv.PkvError):
         pkv.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
                                    t["context_lens"], b.scale, out, partition_size=24)
+
+
+# ------------------------------------------------------------------ shared-prefix (cascade) decode
+
+def _cascade_step(b, prefix_len, out_dtype=torch.float32, fused=True, partition=0):
+    t = to_dev(b)
+    if t["copy_pairs"] is not None and t["copy_pairs"].numel():
+        pkv.copy_blocks(t["copy_pairs"], t["k_cache"], t["v_cache"])
+    if not fused:
+        pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"])
+    out = torch.empty(b.q.shape, dtype=out_dtype, device="cuda")
+    pkv.decode_shared_prefix(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
+                             b.scale, out, prefix_len, k_new=t["k_new"] if fused else None,
+                             v_new=t["v_new"] if fused else None, max_context_len=b.max_context_len,
+                             partition_size=partition)
+    torch.cuda.synchronize()
+    return t, out
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_shared_prefix_cascade_workload(out_dtype):
+    b = W.make_batch("shared_prefix_cow")
+    prefix_len = b.meta["prefix_blocks"] * 16
+    kc_o, vc_o, out_o, _ = oracle_step(b)
+    t, out = _cascade_step(b, prefix_len, out_dtype)
+    assert pkv.get_status() == 0
+    assert_bits_equal(t["k_cache"], kc_o, "k_cache")
+    assert_bits_equal(t["v_cache"], vc_o, "v_cache")
+    assert_parity(out, out_o, b.dtype, "cascade decode")
+
+
+@pytest.mark.parametrize("num_seqs,prefix_blocks,ctx,fused,partition", [
+    (40, 3, (16, 300), True, 0),      # 48-token prefix (one partial key tile), 160 query rows
+    (5, 9, (1, 40), False, 0),        # tiny suffixes, one row tile, append outside
+    (64, 20, (100, 2000), True, 256), # long suffixes split in 256-token partitions
+])
+def test_shared_prefix_cascade_shapes(num_seqs, prefix_blocks, ctx, fused, partition):
+    b = W.make_batch("shared_prefix_cow", num_seqs=num_seqs, ctx=ctx, prefix_blocks=prefix_blocks)
+    kc_o, vc_o, out_o, _ = oracle_step(b)
+    t, out = _cascade_step(b, prefix_blocks * 16, fused=fused, partition=partition)
+    assert pkv.get_status() == 0
+    assert_bits_equal(t["k_cache"], kc_o, "k_cache")
+    assert_parity(out, out_o, b.dtype, "cascade decode")
