@@ -55,6 +55,17 @@ struct DecodeParams {
     // elsewhere (their merged state is partial slot 0); the partitions here
     // cover [prefix_len, L) and write slots 1, 2, ...  0 = no prefix.
     int prefix_len;
+    // The launch before this one is the shared-prefix kernel, whose results
+    // this kernel does not read: do not wait for it at the start (run beside
+    // it). The grid's last CTA waits for it before exiting, so this grid
+    // completes after it, and the merge launch, which waits for this grid,
+    // also sees the prefix kernel's partials.
+    int overlap_prev;
+    // 1: each warp of a thread block streams the whole partition for its own
+    // (kv head, head chunk), four per block; 0: the four warps split one
+    // (kv head, chunk)'s partition and merge (set by the host, see
+    // use_head_warps)
+    int head_warps;
 };
 
 // Partitions of the tokens this launch covers for a sequence of L tokens.
@@ -65,18 +76,18 @@ __device__ __forceinline__ int own_parts(const DecodeParams &p, int L) {
 }
 
 // Write the new token of sequence s, kv head kvh, at logical position L-1.
-// Called by every thread of a CTA that owns the partition holding L-1,
-// followed by a CTA barrier before the partition is read.
+// Called by the threads [first, first + count) that own the partition holding
+// L-1, followed by a barrier over them before the partition is read.
 template <typename T>
 __device__ __forceinline__ void append_new_token(const DecodeParams &p, const int32_t *table, int s, int kvh,
-                                                 int L, int D) {
+                                                 int L, int D, int first, int count) {
     const int t = L - 1;
     const int phys = table[t / kBlock];
     if (phys < 0 || phys >= p.num_blocks) return;  // reported by the gather
     const int chunks = D * (int)sizeof(T) / 16;
     const size_t dst = (((size_t)phys * p.num_kv_heads + kvh) * kBlock + (t % kBlock)) * chunks;
     const size_t src = ((size_t)s * p.num_kv_heads + kvh) * chunks;
-    for (int i = threadIdx.x; i < 2 * chunks; i += blockDim.x) {
+    for (int i = first; i < 2 * chunks; i += count) {
         const bool is_v = i >= chunks;
         const int c = is_v ? i - chunks : i;
         const uint4 *from = static_cast<const uint4 *>(is_v ? p.v_new : p.k_new) + src + c;
@@ -110,7 +121,7 @@ struct DecodeSmem {
     static constexpr int kBytes = kStaging > kMerge ? kStaging : kMerge;
 };
 
-template <int D, typename OutT>
+template <int D, typename OutT, bool kHeadWarps>
 __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodeParams p) {
     using Sm = DecodeSmem<D>;
     constexpr int CH = D / 8;                 // 16-byte chunks per row
@@ -120,18 +131,37 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
 
     extern __shared__ __align__(128) unsigned char smem[];
     pkv::allow_dependents();
-    pkv::grid_dependency_wait();  // the appended tokens of the previous launch
+    if (!p.overlap_prev) pkv::grid_dependency_wait();  // the appended tokens of the previous launch
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gid = lane >> 2, tig = lane & 3;
-    const int kvh = blockIdx.x / p.head_chunks, chunk = blockIdx.x - kvh * p.head_chunks;
+    // the (kv head, head chunk) unit of this warp
+    const int unit = kHeadWarps ? blockIdx.x * kWarps + warp : blockIdx.x;
+    const bool idle = kHeadWarps && unit >= p.num_kv_heads * p.head_chunks;
+    const int kvh = unit / p.head_chunks, chunk = unit - kvh * p.head_chunks;
     const int s = blockIdx.y, part = blockIdx.z;
+    const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
+    const int blk_begin = (p.prefix_len + part * p.partition) / kBlock;
+    // The warp's blocks: a head warp takes every block of the partition; a
+    // split warp every fourth, starting at its own index.  The positions do
+    // not depend on the length, so the first 32 block ids are fetched now,
+    // alongside the length rather than after it, with one coalesced load;
+    // issuing a copy then never waits on a dependent block-table read.
+    const int bstride = kHeadWarps ? 1 : kWarps;
+    const int bfirst = blk_begin + (kHeadWarps ? 0 : warp);
+    int my_id = 0;
+    if (!idle && bfirst + bstride * lane < p.max_blocks) my_id = table[bfirst + bstride * lane];
 
     const int L = clamp_len(p.context_lens[s], p.len_cap, p.status,
                             part == 0 && blockIdx.x == 0 && threadIdx.x == 0);
     if (p.prefix_len && L <= p.prefix_len && part == 0 && blockIdx.x == 0 && threadIdx.x == 0)
         pkv::flag(p.status, PKV_STATUS_BAD_LENGTH);  // no private token after the shared prefix
     const int nparts = own_parts(p, L);
-    if (part >= nparts) return;
+    const bool tail_wait = p.overlap_prev && blockIdx.x == gridDim.x - 1 &&
+                           blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1;
+    if (part >= nparts || idle) {
+        if (tail_wait) pkv::grid_dependency_wait();
+        return;
+    }
     const int slot0 = p.prefix_len ? 1 : 0;  // partial slot 0 holds the shared prefix
     const int nslots = slot0 + nparts;
 
@@ -139,16 +169,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
     const int rows = min(kRows, p.group - chunk * kRows);
     const int t_begin = p.prefix_len + part * p.partition;
     const int t_end = min(L, t_begin + p.partition);
-    const int blk_begin = t_begin / kBlock;
     const int nblk = (t_end + kBlock - 1) / kBlock - blk_begin;
-    const int wb = blk_begin + (nblk * warp) / kWarps;
-    const int we = blk_begin + (nblk * (warp + 1)) / kWarps;
-    const int n = max(0, we - wb);
+    const int n = kHeadWarps ? nblk : max(0, (nblk - warp + kWarps - 1) / kWarps);
 
     const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
     const __nv_bfloat16 *kc = static_cast<const __nv_bfloat16 *>(p.k_cache);
     const __nv_bfloat16 *vc = static_cast<const __nv_bfloat16 *>(p.v_cache);
-    const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
 
     // query rows of this tile as mma A fragments (rows >= `rows` are zero)
     uint32_t qa[KSTEPS][4];
@@ -167,23 +193,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
     }
 
     if (p.k_new && part == nparts - 1 && L > 0) {
-        append_new_token<__nv_bfloat16>(p, table, s, kvh, L, D);
-        __syncthreads();  // the new row is read below through L2 by other threads
+        // the new row is read below through L2 by other threads
+        if (kHeadWarps) {
+            // (warps of other chunks of the same kv head write the same bytes)
+            append_new_token<__nv_bfloat16>(p, table, s, kvh, L, D, lane, 32);
+            __syncwarp();
+        } else {
+            append_new_token<__nv_bfloat16>(p, table, s, kvh, L, D, threadIdx.x, kThreads);
+            __syncthreads();
+        }
     }
 
     unsigned char *ring = smem + warp * Sm::kWarp;
 
-    // The warp's first 32 block ids, fetched with one coalesced load so that
-    // issuing a copy never waits on a dependent block-table read.
-    const int my_id = lane < n ? table[wb + lane] : 0;
     auto block_id = [&](int li) -> int {
-        return li < 32 ? __shfl_sync(0xffffffffu, my_id, li) : table[wb + li];
+        return li < 32 ? __shfl_sync(0xffffffffu, my_id, li) : table[bfirst + bstride * li];
     };
     // rows of the warp's li-th block that hold tokens of this partition (-1 for a bad id)
     auto block_rows = [&](int li, int &phys) -> int {
         phys = block_id(li);
         if (phys < 0 || phys >= p.num_blocks) return -1;
-        return min(kBlock, t_end - (wb + li) * kBlock);
+        return min(kBlock, t_end - (bfirst + bstride * li) * kBlock);
     };
 
     auto issue = [&](int li, int st) {
@@ -312,6 +342,34 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
     lB += __shfl_xor_sync(0xffffffffu, lB, 2);
 
     pkv::cp_async_wait<0>();
+    if (kHeadWarps) {
+        // the warp holds its rows' whole state for this partition
+        const size_t orow = (size_t)s * p.num_q_heads + h0 + gid;
+        const bool okA = gid < rows, okB = gid + 8 < rows;
+        if (nslots == 1) {
+            OutT *oa = static_cast<OutT *>(p.out) + orow * D;
+            OutT *ob = oa + 8 * D;
+            const float ia = lA > 0.f ? 1.f / lA : 0.f, ib = lB > 0.f ? 1.f / lB : 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                const int col = nt * 8 + tig * 2;
+                if (okA) pkv::store2(oa + col, o[nt][0] * ia, o[nt][1] * ia);
+                if (okB) pkv::store2(ob + col, o[nt][2] * ib, o[nt][3] * ib);
+            }
+        } else {
+            const size_t pa = orow * p.max_parts + slot0 + part, pb = pa + 8 * (size_t)p.max_parts;
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                const int col = nt * 8 + tig * 2;
+                if (okA) *reinterpret_cast<float2 *>(p.part_o + pa * D + col) = make_float2(o[nt][0], o[nt][1]);
+                if (okB) *reinterpret_cast<float2 *>(p.part_o + pb * D + col) = make_float2(o[nt][2], o[nt][3]);
+            }
+            if (tig == 0 && okA) *reinterpret_cast<float2 *>(p.part_ml + pa * 2) = make_float2(mA, lA);
+            if (tig == 0 && okB) *reinterpret_cast<float2 *>(p.part_ml + pb * 2) = make_float2(mB, lB);
+        }
+        if (tail_wait) pkv::grid_dependency_wait();
+        return;
+    }
     __syncthreads();  // every warp is done with its ring; reuse it for the merge
 
     float *mw = reinterpret_cast<float *>(smem) + warp * Sm::kMergeWarp;
@@ -360,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
             }
         }
     }
+    if (tail_wait) pkv::grid_dependency_wait();
 }
 
 // ----------------------------------------------------------------------------
@@ -462,7 +521,7 @@ __global__ void __launch_bounds__(kThreads) decode_cuda_core_kernel(const Decode
     const int kvh = h / p.group;
     if (p.k_new && part == nparts - 1 && L > 0) {
         // every q head of the group writes the same bytes for its kv head
-        append_new_token<T>(p, p.block_tables + (size_t)s * p.max_blocks, s, kvh, L, D);
+        append_new_token<T>(p, p.block_tables + (size_t)s * p.max_blocks, s, kvh, L, D, threadIdx.x, blockDim.x);
         __syncthreads();
     }
     const T *qrow = static_cast<const T *>(p.q) + ((size_t)s * p.num_q_heads + h) * D;
@@ -579,7 +638,8 @@ int resolve_partition(int partition_size, int *out) {
 // largest context, so a sequence is assumed to hold half of it.  Larger
 // partitions amortise each thread block's start-up and cut the split-K
 // partials; enough units keep every SM streaming.
-int adaptive_partition(int num_seqs, int num_kv_heads, int max_context_len) {
+// SM count of the current device (148 when there is none to ask)
+int device_sms() {
     static int sm_count[64] = {0};
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
@@ -588,7 +648,11 @@ int adaptive_partition(int num_seqs, int num_kv_heads, int max_context_len) {
         if (sm_count[dev] > 0) sms = sm_count[dev];
     }
     cudaGetLastError();
-    const long long target = 4LL * sms;
+    return sms;
+}
+
+int adaptive_partition(int num_seqs, int num_kv_heads, int max_context_len) {
+    const long long target = 4LL * device_sms();
     const int candidates[] = {3072, 2048, 1536, 1024};
     for (int c : candidates) {
         const long long per_seq = max(1, (max_context_len + 2 * c - 1) / (2 * c));
@@ -597,24 +661,47 @@ int adaptive_partition(int num_seqs, int num_kv_heads, int max_context_len) {
     return PKV_DEFAULT_PARTITION;
 }
 
-template <int D, typename OutT>
-int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
+// Head warps when a partition spans at most this many tokens (split four
+// ways it would give each warp at most 8 blocks, too few to amortise the
+// block's start: length, block ids, first copies, merge), provided the
+// launch still has two thread blocks per SM: a head-warp block covers four
+// (kv head, chunk) units, so it cuts the block count fourfold.
+constexpr int kHeadWarpTokens = 512;
+
+// own_max: the most tokens one launch covers for a sequence (the context
+// minus any shared prefix); units: kv heads x head chunks.
+bool use_head_warps(int num_seqs, int units, int own_max, int partition) {
+    if ((own_max < partition ? own_max : partition) > kHeadWarpTokens) return false;
+    const long long parts = own_max > 0 ? (own_max + partition - 1) / partition : 1;
+    return (long long)num_seqs * ((units + kWarps - 1) / kWarps) * parts >= 2LL * device_sms();
+}
+
+template <int D, typename OutT, bool kHeadWarps>
+int launch_bf16_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
     constexpr int bytes = DecodeSmem<D>::kBytes;
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(decode_bf16_kernel<D, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 bytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
             return pkv::check_launch("decode: set shared memory size");
         attr_set[dev] = true;
     }
+    const int units = p.num_kv_heads * p.head_chunks;
     // (with a shared prefix, partial slot 0 comes from another kernel)
-    dim3 grid((unsigned)(p.num_kv_heads * p.head_chunks), (unsigned)num_seqs,
+    dim3 grid((unsigned)(kHeadWarps ? (units + kWarps - 1) / kWarps : units), (unsigned)num_seqs,
               (unsigned)(p.max_parts - (p.prefix_len ? 1 : 0)));
-    cudaError_t e = pkv::launch_dependent(decode_bf16_kernel<D, OutT>, grid, dim3(kThreads), bytes, st, p);
+    cudaError_t e =
+        pkv::launch_dependent(decode_bf16_kernel<D, OutT, kHeadWarps>, grid, dim3(kThreads), bytes, st, p);
     if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "decode_bf16: %s", cudaGetErrorString(e));
     return pkv::check_launch("decode_bf16");
+}
+
+template <int D, typename OutT>
+int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
+    return p.head_warps ? launch_bf16_variant<D, OutT, true>(p, num_seqs, st)
+                        : launch_bf16_variant<D, OutT, false>(p, num_seqs, st);
 }
 
 template <typename T, typename OutT>
@@ -721,6 +808,7 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
     p.status = pkv::status_ptr();
     p.k_new = k_new;
     p.v_new = v_new;
+    p.head_warps = use_head_warps(num_seqs, num_kv_heads * p.head_chunks, p.len_cap, part);
     if ((k_new || v_new) && (!k_new || !v_new || !pkv::aligned16(k_new) || !pkv::aligned16(v_new)))
         return pkv::fail(PKV_ERR_INVALID, "decode_step: k_new and v_new must both be 16-byte aligned device pointers");
 
@@ -897,6 +985,8 @@ extern "C" int pkv_paged_attention_decode_shared_prefix(
     p.k_new = k_new;
     p.v_new = v_new;
     p.prefix_len = prefix_len;
+    p.overlap_prev = 1;  // the partitions run beside the prefix kernel
+    p.head_warps = use_head_warps(num_seqs, num_kv_heads * p.head_chunks, len_cap - prefix_len, part);
     p.part_o = part_o;
     p.part_ml = part_ml;
     return out_dtype == PKV_F32 ? launch_decode<float>(p, num_seqs, head_dim, dtype, st)

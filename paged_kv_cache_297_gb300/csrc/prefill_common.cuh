@@ -30,6 +30,11 @@ struct PrefillParams {
     int tiles_per_seq;
     int num_items;
     unsigned long long *item_counter;
+    // set by the launch: 1 when the q tiles are loaded by TMA (the group
+    // divides the 128-row tile), 0 when the softmax threads copy them
+    int q_tma;
+    // set by the launch: 1 when the output is 32-byte aligned (32-byte stores)
+    int out_v8;
     // shared-prefix mode (prefix_len > 0): the "chunk" is the batch's decode
     // queries (one position per sequence, max_q_len = sequences), every one
     // attends to keys [0, prefix_len) of block table row 0, and the result

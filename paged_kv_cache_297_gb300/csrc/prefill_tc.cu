@@ -64,6 +64,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <string.h>
 
 #include "common.cuh"
 #include "prefill_common.cuh"
@@ -92,13 +93,16 @@ constexpr int kOffK = kOffQ + kTile;                     // 32768
 constexpr int kOffV = kOffK + kKStages * kTile;          // 131072
 constexpr int kOffBar = kOffV + kVStages * kTile;        // 229376
 // barriers: per team s, o (4); per team and half of P (4); K full/empty; V
-// full/empty; go (2); item queue full/empty (4); per team MMA drain (2)
-constexpr int kNumBars = 8 + 2 * kKStages + 2 * kVStages + 2 + 4 + 2;
+// full/empty; go (2); item queue full/empty (4); per team MMA drain (2); Q
+// buffer free (1)
+constexpr int kNumBars = 8 + 2 * kKStages + 2 * kVStages + 2 + 4 + 2 + 1;
 constexpr int kItemReaders = 1 + 2 + 8;  // item queue readers: V loader, MMA lanes, softmax warps
 constexpr int kOffSlots = (kOffBar + kNumBars * 8 + 15) & ~15;  // TMEM address (16 B), two item slots (int4)
 static_assert(kOffSlots % 16 == 0, "item slots are 16-byte vectors");
-constexpr int kOffRed = kOffSlots + 16 + 2 * 16;
+constexpr int kOffSeen = kOffSlots + 16 + 2 * 16;         // phases seen per K and V stage (ints)
+constexpr int kOffRed = kOffSeen + 16 * 4;
 constexpr int kSmemBytes = kOffRed + 2 * 2 * BM * 4;     // [team][m, l][row]
+static_assert(kKStages + kVStages <= 16, "phase counters");
 static_assert(kSmemBytes <= 232448, "more shared memory than a CTA may have");
 constexpr unsigned kWaitIters = 1u << 24;
 
@@ -160,8 +164,11 @@ __device__ __forceinline__ ItemInfo item_info(const PrefillParams &p, int4 v) {
 template <typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v) {
+                      const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_q) {
     extern __shared__ __align__(1024) unsigned char smem[];
+    // a dependent launch (the decode partitions beside the shared-prefix
+    // mode) may start as soon as every CTA of this one has
+    pkv::allow_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = p.group;
     const uint32_t sbase = pkv::smem_u32(smem);
@@ -182,9 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar_item_full = bar_go + 2;          // [slot] item published
     uint64_t *bar_item_empty = bar_item_full + 2;  // [slot] every role has read it
     uint64_t *bar_done = bar_item_empty + 2;       // [team] all of the team's MMAs finished
+    uint64_t *bar_qfree = bar_done + 2;            // every S of the k-th item with work finished (2 arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffSlots);
     int4 *item_slots = reinterpret_cast<int4 *>(smem + kOffSlots + 16);
     float *red = reinterpret_cast<float *>(smem + kOffRed);  // [team][m, l][row]
+    // [K stages][V stages]: how many phases of each stage's "full" barrier an
+    // MMA lane has seen complete (see wait_full)
+    volatile int *seen = reinterpret_cast<volatile int *>(smem + kOffSeen);
 
     if (tid == 0) {
         for (int t = 0; t < 2; t++) {
@@ -196,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pkv::tc::mbar_init(bar_item_empty + t, kItemReaders);
             pkv::tc::mbar_init(bar_done + t, 1);
         }
+        pkv::tc::mbar_init(bar_qfree, 2);
         for (int st = 0; st < kKStages; st++) {
             pkv::tc::mbar_init(bar_kfull + st, 1);
             pkv::tc::mbar_init(bar_kempty + st, 1);
@@ -204,8 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             pkv::tc::mbar_init(bar_vfull + st, 1);
             pkv::tc::mbar_init(bar_vempty + st, 1);
         }
-        pkv::tc::mbar_init(bar_go, 2 * kTeamThreads);
-        pkv::tc::mbar_init(bar_go + 1, 2 * kTeamThreads);
+        // Q lands by TMA (one arrival with its bytes) or by the softmax threads' copies
+        for (int i = 0; i < kKStages + kVStages; i++) seen[i] = 0;
+        pkv::tc::mbar_init(bar_go, p.q_tma ? 1 : 2 * kTeamThreads);
+        pkv::tc::mbar_init(bar_go + 1, p.q_tma ? 1 : 2 * kTeamThreads);
         pkv::tc::fence_mbar_init();
     }
     __syncthreads();  // barriers initialised: the loaders can start right away
@@ -295,62 +309,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                 it = take_item(i);
             }
             if (it.stop) break;
+            if (is_k && p.q_tma && !it.skip) {
+                // This item's q tile, as soon as the previous one's S MMAs are
+                // done with the buffer: it lands while that item finishes.  Row
+                // r = j * G + h of the tile is query q0 + tile*128/G + j, head
+                // kvh*G + h: one 3-D box {64 columns, G heads, 128/G queries}
+                // per half.  Rows past the chunk read other queries or zeros
+                // and are masked.
+                if (go_count > 0) wait(bar_qfree, (unsigned)((go_count - 1) & 1));
+                if (lane == 0) {
+                    uint64_t *go = bar_go + (go_count & 1);
+                    pkv::tc::mbar_arrive_expect_tx(go, kTile);
+                    const int z = it.q0 + it.tile * (BM / G);
+#pragma unroll
+                    for (int h = 0; h < 2; h++)
+                        pkv::tc::tma_load_3d(smem + kOffQ + h * kHalf, &tmap_q, h * 64, it.kvh * G, z, go);
+                }
+            }
             const int32_t *table = p.block_tables + (size_t)(it.skip ? 0 : it.s) * p.max_blocks;
             for (int t = 0; t < it.nkt; t++) {
                 const int g = kt_base + t;  // ring position across items
                 const int st = g % nst;
                 if (g >= nst) wait(empty + st, (unsigned)((g / nst - 1) & 1));
                 unsigned char *dst = smem + (is_k ? kOffK : kOffV) + st * kTile;
-                // physical ids of the 8 blocks holding keys [t*128, t*128 + 128)
+                // Keys [t*128, t*128 + 128) sit in 8 blocks, each loaded with two
+                // 16-row x 64-column TMA boxes.  Blocks past the keys are not
+                // loaded: K rows there are masked out of S whatever they hold, V
+                // rows are zeroed in place (P = 0 times a NaN would poison O).
+                // A V block that the keys end inside is copied with zero fill.
+                const int tile_keys = min(BN, it.kv_end - t * BN);
+                const int nbk = (tile_keys + kBlock - 1) / kBlock;
+                const int cpq = (!is_k && (tile_keys % kBlock)) ? tile_keys / kBlock : -1;
+                const int ntma = cpq >= 0 ? nbk - 1 : nbk;  // blocks 0 .. ntma-1 by TMA
                 int my_id = 0;
-                if (lane < 8 && t * BN + lane * kBlock < it.kv_end) my_id = table[t * 8 + lane];
-                if ((t + 1) * BN <= it.kv_end) {
-                    // eight whole blocks: TMA
-                    int y = box_rows;  // out of range: the box reads as zeros
-                    if (lane < 8) {
-                        if (my_id >= 0 && my_id < p.num_blocks)
-                            y = (my_id * p.num_kv_heads + it.kvh) * kBlock;
-                        else
-                            pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
-                    }
-                    int ys[8];
+                if (lane < nbk) my_id = table[t * 8 + lane];
+                int y = box_rows;
+                if (lane < ntma) {
+                    if (my_id >= 0 && my_id < p.num_blocks)
+                        y = (my_id * p.num_kv_heads + it.kvh) * kBlock;
+                    else
+                        pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                }
+                int ys[8];
 #pragma unroll
-                    for (int q = 0; q < 8; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
-                    if (lane == 0) {
-                        pkv::tc::mbar_arrive_expect_tx(full + st, kTile);
-#pragma unroll
-                        for (int q = 0; q < 8; q++) {
-#pragma unroll
-                            for (int h = 0; h < 2; h++)
-                                pkv::tc::tma_load_2d(dst + h * kHalf + q * 2048, tmap, h * 64, ys[q], full + st);
+                for (int q = 0; q < 8; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
+                const bool extra = cpq >= 0 || (!is_k && nbk < 8);
+                if (extra) {
+                    // generic-proxy part of the V tile: the partial block's live
+                    // rows by zero-filling copies, every other row past the keys
+                    // zeroed with stores
+                    const int phys = cpq >= 0 ? __shfl_sync(0xffffffffu, my_id, cpq) : 0;
+                    const bool ok = phys >= 0 && phys < p.num_blocks;
+                    if (cpq >= 0 && !ok && lane == 0) pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                    for (int e = lane + 256 * ntma; e < 16 * 128; e += 32) {
+                        const int r = e >> 4, c = e & 15;
+                        unsigned char *d = dst + (c >> 3) * kHalf + sw128(r, c & 7);
+                        if (r < tile_keys) {
+                            const int rb = r % kBlock;
+                            const size_t go = ok ? ((((size_t)phys * p.num_kv_heads + it.kvh) * kBlock + rb) * D) * 2 + c * 16 : 0;
+                            pkv::cp_async16(d, cache + go, ok ? 16 : 0);
+                        } else {
+                            *reinterpret_cast<uint4 *>(d) = make_uint4(0u, 0u, 0u, 0u);
                         }
-                    }
-                } else {
-                    // the last tile may end inside a block: zero-filling copies
-#pragma unroll 4
-                    for (int u = 0; u < 64; u++) {
-                        const int e = lane + 32 * u;
-                        const int r = e >> 4, c = e & 15;  // r >> 4 == u >> 3
-                        const int key = t * BN + r;
-                        const int phys = __shfl_sync(0xffffffffu, my_id, u >> 3);
-                        int nb = 0;
-                        size_t go = 0;
-                        if (key < it.kv_end) {
-                            if (phys >= 0 && phys < p.num_blocks) {
-                                nb = 16;
-                                go = ((((size_t)phys * p.num_kv_heads + it.kvh) * kBlock + (key % kBlock)) * D) * 2 +
-                                     c * 16;
-                            } else if (c == 0 && (key % kBlock) == 0) {
-                                pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
-                            }
-                        }
-                        pkv::cp_async16(dst + (c >> 3) * kHalf + sw128(r, c & 7), cache + go, nb);
                     }
                     pkv::cp_async_commit();
                     pkv::cp_async_wait<0>();
                     pkv::tc::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) pkv::tc::mbar_arrive(full + st);
+                }
+                if (lane == 0) {
+                    pkv::tc::mbar_arrive_expect_tx(full + st, (uint32_t)(ntma * 2 * 2048));
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        if (q >= ntma) break;
+#pragma unroll
+                        for (int h = 0; h < 2; h++)
+                            pkv::tc::tma_load_2d(dst + h * kHalf + q * 2048, tmap, h * 64, ys[q], full + st);
+                    }
                 }
             }
             advance(it);
@@ -363,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issue: lane 0 of warp 8 + q issues team q's tiles
         const int q = warp - kMmaWarp;
         if (lane == 0) {
+            int nkt_cur = 0;  // key tiles of the item being issued
             auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into the S/P buffer of team t & 1 (K(t) landed)
                 const uint32_t qa = sbase + kOffQ;
                 const uint32_t kb = sbase + kOffK + ((kt_base + t) % kKStages) * kTile;
@@ -374,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 pkv::tc::mma_commit(bar_kempty + ((kt_base + t) % kKStages));
                 pkv::tc::mma_commit(bar_s + (t & 1));
+                if (t + 2 >= nkt_cur) pkv::tc::mma_commit(bar_qfree);  // this lane's last read of Q
             };
             // O(team t & 1) (+)= P(t) V(t) over keys 64h .. 64h+63 (V(t) landed,
             // that half of P(t) stored)
@@ -391,14 +428,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pkv::tc::mma_commit(bar_o + (t & 1));
                 }
             };
-            auto wait_k = [&](int t) {
-                const int g = kt_base + t;
-                wait(bar_kfull + g % kKStages, (unsigned)((g / kKStages) & 1));
+            // A ring stage's consecutive tiles can belong to different teams,
+            // hence to different MMA lanes.  A lane must not wait on a phase
+            // of a stage's "full" barrier before the previous phase has been
+            // seen complete: a parity wait cannot tell "phase k done" from
+            // "phase k-1 still running".  So each wait first lets the
+            // stage's count of seen phases reach this phase's index (the
+            // other lane moves it), then waits, then counts this phase.
+            auto wait_full = [&](uint64_t *full, volatile int *cnt, int g, int nst) {
+                const int s = g % nst, ph = g / nst;
+                unsigned n = 0;
+                while (!failed && cnt[s] < ph) {
+                    if (++n > kWaitIters) failed = true;
+                }
+                wait(full + s, (unsigned)(ph & 1));
+                cnt[s] = ph + 1;
             };
-            auto wait_v = [&](int t) {
-                const int g = kt_base + t;
-                wait(bar_vfull + g % kVStages, (unsigned)((g / kVStages) & 1));
-            };
+            auto wait_k = [&](int t) { wait_full(bar_kfull, seen, kt_base + t, kKStages); };
+            auto wait_v = [&](int t) { wait_full(bar_vfull, seen + kKStages, kt_base + t, kVStages); };
             for (int i = 0;; i++) {
                 // Take item i alone (the other lanes idle).  The slot is
                 // reported read only after this item's Q barrier has been
@@ -412,7 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it.stop) break;
                 if (!it.skip) {
                     const int nkt = it.nkt;
+                    nkt_cur = nkt;
                     const int tb = q ? team_base1 : team_base0;  // this team's tiles before this item
+                    if (q >= nkt) pkv::tc::mbar_arrive(bar_qfree);  // no S of this lane reads this Q
                     if (q < nkt) {
                         wait_k(q);
                         pkv::tc::fence_after_sync();
@@ -456,11 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             const int nkt = it.nkt;
-            // Q tile: 128 rows x 16 chunks, 8 copies per softmax thread.  The
-            // previous item's S MMAs are all complete: this thread has been
-            // through that item's epilogue, which follows both teams' last PV.
+            // Without TMA, the Q tile: 128 rows x 16 chunks, 8 copies per
+            // softmax thread.  The previous item's S MMAs are all complete:
+            // this thread has been through that item's epilogue, which
+            // follows both teams' last PV.
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
+            for (int u = 0; u < 8 && !p.q_tma; u++) {
                 const int e = tid + 2 * kTeamThreads * u;
                 const int r = e >> 4, c = e & 15;
                 const int R = it.tile * BM + r;
@@ -470,10 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok ? qg + ((size_t)(it.q0 + jr) * p.num_q_heads + it.kvh * G + (R - jr * G)) * D + c * 8 : qg;
                 pkv::cp_async16(smem + kOffQ + (c >> 3) * kHalf + sw128(r, c & 7), src, ok ? 16 : 0);
             }
-            pkv::cp_async_commit();
-            pkv::cp_async_wait<0>();
-            pkv::tc::fence_proxy_async_smem();
-            pkv::tc::mbar_arrive(bar_go + (go_count & 1));
+            if (!p.q_tma) {
+                pkv::cp_async_commit();
+                pkv::cp_async_wait<0>();
+                pkv::tc::fence_proxy_async_smem();
+                pkv::tc::mbar_arrive(bar_go + (go_count & 1));
+            }
 
             const int R = it.tile * BM + row;
             const int jrow = R / G;
@@ -492,25 +544,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The row's scores are read from TMEM twice, 64 at a time (for the
                 // maximum, then for the powers), so that only 64 stay live and the
                 // rest of the register file is free to overlap the exponentials.
+                // Unmasked, the first read's own reduction gives the maximum.
                 const bool masked = !full_tile || !row_ok;
                 float mraw = -INFINITY;
     #pragma unroll
                 for (int h = 0; h < 2; h++) {
-                    float sv[64];
-                    pkv::tc::tmem_ld64(t_lane + s_col + h * 64, sv);
+                    float sv[64], hmax;
+                    pkv::tc::tmem_ld64_max(t_lane + s_col + h * 64, sv, hmax);
                     if (masked) {
     #pragma unroll
                         for (int i = 0; i < 64; i++) sv[i] = h * 64 + i <= lim0 ? sv[i] : -INFINITY;
+                        float mx[16];
+    #pragma unroll
+                        for (int i = 0; i < 16; i++)
+                            mx[i] = fmaxf(fmaxf(sv[i], sv[i + 16]), fmaxf(sv[i + 32], sv[i + 48]));
+    #pragma unroll
+                        for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], mx[i + 8]);
+    #pragma unroll
+                        for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
+                        hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                     }
-                    float mx[16];
-    #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        mx[i] = fmaxf(fmaxf(sv[i], sv[i + 16]), fmaxf(sv[i + 32], sv[i + 48]));
-    #pragma unroll
-                    for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], mx[i + 8]);
-    #pragma unroll
-                    for (int i = 0; i < 4; i++) mx[i] = fmaxf(mx[i], mx[i + 4]);
-                    mraw = fmaxf(mraw, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
+                    mraw = fmaxf(mraw, hmax);
                 }
                 if (!row_ok) mraw = -INFINITY;
                 const float mt = mraw * p.scale_log2;  // scale > 0 commutes with max; -inf stays
@@ -625,10 +679,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     alignas(16) OutT v[32];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) pkv::store2(v + e, a[e] * g0 + b[e] * g1, a[e + 1] * g0 + b[e + 1] * g1);
-                    constexpr int kVec = 32 * (int)sizeof(OutT) / 16;
+                    if (p.out_v8) {
+                        // 32 bytes per store: each fills whole sectors of the row
+                        constexpr int kVec = 32 * (int)sizeof(OutT) / 32;
 #pragma unroll
-                    for (int k = 0; k < kVec; k++)
-                        reinterpret_cast<uint4 *>(orow + col)[k] = reinterpret_cast<const uint4 *>(v)[k];
+                        for (int k = 0; k < kVec; k++)
+                            pkv::tc::st_global_32B(orow + col + k * (32 / (int)sizeof(OutT)),
+                                                   reinterpret_cast<const uint4 *>(v) + 2 * k);
+                    } else {
+                        constexpr int kVec = 32 * (int)sizeof(OutT) / 16;
+#pragma unroll
+                        for (int k = 0; k < kVec; k++)
+                            reinterpret_cast<uint4 *>(orow + col)[k] = reinterpret_cast<const uint4 *>(v)[k];
+                    }
                 }
             }
             // the O reads are done before the next item's first PV may overwrite
@@ -684,6 +747,20 @@ int make_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int num_
     return PKV_OK;
 }
 
+// 3-D view of the queries [total_q][Hq][128] bf16: boxes of {64 columns, G
+// heads, 128/G queries}, the 128 packed rows of one q tile, 128-byte swizzle.
+int make_q_map(CUtensorMap *map, const void *q, int num_q_heads, int total_q, int group) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)num_q_heads * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(BM / group)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return pkv::fail(PKV_ERR_CUDA, "prefill: cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -696,6 +773,14 @@ int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaS
     if (rc) return rc;
     rc = make_cache_map(&tv, p.v_cache, p.num_blocks, p.num_kv_heads);
     if (rc) return rc;
+    // q tiles by TMA when a tile is whole queries (G divides 128)
+    CUtensorMap tq;
+    memset(&tq, 0, sizeof(tq));
+    const bool q_tma = p.group <= BM && BM % p.group == 0 && p.total_q > 0;
+    if (q_tma) {
+        rc = make_q_map(&tq, p.q, p.num_q_heads, p.total_q, p.group);
+        if (rc) return rc;
+    }
     static bool attr_set[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -710,6 +795,8 @@ int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaS
         attr_set[which][dev] = true;
     }
     PrefillParams pp = p;
+    pp.q_tma = q_tma ? 1 : 0;
+    pp.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0 ? 1 : 0;
     pp.num_seqs = num_seqs;
     pp.tiles_per_seq = (p.max_q_len * p.group + BM - 1) / BM;
     const long long items = (long long)num_seqs * p.num_kv_heads * pp.tiles_per_seq;
@@ -726,9 +813,9 @@ int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaS
     // one persistent CTA per SM (its shared memory allows no second)
     const unsigned grid = (unsigned)(pp.num_items < nsm ? pp.num_items : nsm);
     if (which == 0)
-        prefill_tc_kernel<float><<<grid, kThreads, kSmemBytes, st>>>(pp, tk, tv);
+        prefill_tc_kernel<float><<<grid, kThreads, kSmemBytes, st>>>(pp, tk, tv, tq);
     else
-        prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(pp, tk, tv);
+        prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(pp, tk, tv, tq);
     return check_launch("prefill_tc");
 }
 

@@ -96,6 +96,19 @@ def test_split_matches_unsplit():
     assert float((split - whole).abs().max()) <= 2e-3
 
 
+def test_head_warps_match_split_warps():
+    # partitions of at most 512 tokens give each warp a whole (kv head,
+    # partition); larger ones split a (kv head, partition) over four warps
+    # (160 sequences: enough thread blocks for the head-warp schedule)
+    lens = [1, 40, 500, 512, 513, 1000, 1023] * 23
+    b = W.custom_batch("bf16", len(lens), 40, 5, 128, lens, seed=207)
+    _, _, heads, _ = gpu_step(b, partition_size=512)
+    _, _, split, _ = gpu_step(b, partition_size=1024)
+    assert float((heads - split).abs().max()) <= 2e-3
+    _check_step(b, partition_size=512)
+    _check_step(b, partition_size=1024)
+
+
 def test_default_matches_unsplit():
     lens = [3000, 4096, 777, 2049]
     b = W.custom_batch("bf16", len(lens), 32, 8, 128, lens, seed=206)
@@ -144,10 +157,38 @@ def test_outlier_rows_long_mixed_lengths():
     ([0, 3072], [512, 512], 64, 8, 128),
     ([7, 0], [130, 33], 8, 8, 64),
     ([1000], [1], 16, 1, 128),
+    # q tiles by TMA for groups that divide the 128-row tile (1, 32), copied
+    # by the softmax threads otherwise (12)
+    ([50, 0], [200, 129], 8, 8, 128),
+    ([0, 900], [40, 300], 32, 1, 128),
+    ([0, 300], [77, 260], 24, 2, 128),
 ])
 def test_prefill_edges(priors, chunks, hq, hkv, d):
     b = W.custom_prefill("bf16", hq, hkv, d, priors, chunks, seed=301 + sum(chunks))
     _check_step(b)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_prefill_output_only_16_byte_aligned(out_dtype):
+    # the epilogue writes 32 bytes per store only to a 32-byte aligned output
+    b = W.custom_prefill("bf16", 32, 8, 128, [0, 700], [300, 200], seed=311)
+    t = to_dev(b)
+    pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"])
+    n = b.prefill_q.numel()
+    shift = 16 // torch.empty(0, dtype=out_dtype).element_size()
+    buf = torch.empty(n + shift, dtype=out_dtype, device="cuda")
+    outs = [buf[:n].view(b.prefill_q.shape), buf[shift:].view(b.prefill_q.shape)]
+    assert outs[1].data_ptr() % 32 == 16
+    res = []
+    for out in outs:
+        out.fill_(float("nan"))
+        pkv.paged_attention_prefill_chunk(t["prefill_q"], t["prefill_cu_q_lens"], t["k_cache"], t["v_cache"],
+                                          t["prefill_block_tables"], t["prefill_context_lens"], b.scale, out,
+                                          max_q_len=300, max_context_len=900)
+        torch.cuda.synchronize()
+        res.append(out.clone())
+    assert pkv.get_status() == 0
+    assert torch.equal(res[0], res[1])
 
 
 def test_prefill_fp32():
@@ -162,6 +203,12 @@ def test_prefill_fp32():
     ("bf16", 32, 8, 128, [1, 16, 17, 512, 513, 1024, 1025, 3000], 512),
     ("bf16", 64, 2, 64, [5, 40, 700], 0),
     ("f32", 16, 4, 128, [1, 33, 600], 256),
+    # head-warp schedule (partitions of at most 512 tokens and at least two
+    # thread blocks per SM): two chunks of a 24-head group append the same
+    # row; three kv heads leave a warp idle
+    ("bf16", 48, 2, 128, [1, 17, 300, 512] * 80, 0),
+    ("bf16", 12, 3, 128, [5, 200, 600, 1500] * 80, 512),
+    ("bf16", 32, 8, 128, [3, 16, 17, 300, 511, 900] * 4, 128),
 ])
 def test_decode_step_equals_append_then_decode(dtype, hq, hkv, d, lens, partition):
     b = W.custom_batch(dtype, len(lens), hq, hkv, d, lens, seed=501 + d + hq)
@@ -349,6 +396,7 @@ def test_shared_prefix_cascade_workload(out_dtype):
     (40, 3, (16, 300), True, 0),      # 48-token prefix (one partial key tile), 160 query rows
     (5, 9, (1, 40), False, 0),        # tiny suffixes, one row tile, append outside
     (64, 20, (100, 2000), True, 256), # long suffixes split in 256-token partitions
+    (160, 4, (16, 600), True, 256),   # head-warp suffix partitions with partials
 ])
 def test_shared_prefix_cascade_shapes(num_seqs, prefix_blocks, ctx, fused, partition):
     b = W.make_batch("shared_prefix_cow", num_seqs=num_seqs, ctx=ctx, prefix_blocks=prefix_blocks)
