@@ -27,13 +27,18 @@
 //     S/P buffer, O accumulator and running (m, l); the two partial results
 //     are merged by log-sum-exp at the end.  The teams run independently, so
 //     one team's softmax overlaps the other team's MMAs.
-//   * two MMA warps, one per team, whose first lane issues, per tile t of its
-//     team, PV(t) (half by half as P(t) is stored) and then S(t+2) into the
-//     same buffer.  tcgen05.mma operations issued by one thread execute in
-//     order, so S(t+2) cannot overwrite P(t) before PV(t) has read it, and a
-//     team that sees S(t) complete also knows its previous PV is done.  Two
-//     issuing threads halve the issue overhead (barrier waits, descriptors,
-//     commits) that a single thread would serialise across both teams.
+//   * one MMA-issuing thread (lane 0 of warp 8) for both teams, tiles in
+//     order: PV(t) (half by half as P(t) is stored) and then S(t+2) into
+//     the same buffer.  tcgen05.mma operations issued by one thread execute
+//     in order, so S(t+2) cannot overwrite P(t) before PV(t) has read it,
+//     and a team that sees S(t) complete also knows its previous PV is
+//     done.  The pipe then runs PV(t), S(t+2), PV(t+1), S(t+3), ...: each
+//     team's next S completes a unit before the other team's, so the teams'
+//     softmax phases stay apart.  One thread also waits on every ring phase
+//     in order: with a stage's consecutive tiles going to different
+//     waiters, a parity wait could not tell "phase k done" from "phase k-1
+//     still running".  (Two issuing threads, one per team, measured the
+//     same once their waits were ordered.)
 //   * two loader warps, one for K and one for V, that gather tiles through
 //     the block table: a tile of whole blocks with 2-D TMA boxes (one
 //     16-row x 64-column box per block and half; the cache is viewed as
@@ -79,7 +84,7 @@ constexpr int D = 128;
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int kTeamThreads = 128;
-constexpr int kMmaWarp = 8;  // warps 8 and 9: MMA issue for team 0 and team 1
+constexpr int kMmaWarp = 8;  // warp 8: MMA issue (warp 9 only takes part in the TMEM allocation)
 constexpr int kKLoadWarp = 10, kVLoadWarp = 11;
 constexpr int kThreads = 12 * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -93,16 +98,14 @@ constexpr int kOffK = kOffQ + kTile;                     // 32768
 constexpr int kOffV = kOffK + kKStages * kTile;          // 131072
 constexpr int kOffBar = kOffV + kVStages * kTile;        // 229376
 // barriers: per team s, o (4); per team and half of P (4); K full/empty; V
-// full/empty; go (2); item queue full/empty (4); per team MMA drain (2); Q
-// buffer free (1)
-constexpr int kNumBars = 8 + 2 * kKStages + 2 * kVStages + 2 + 4 + 2 + 1;
-constexpr int kItemReaders = 1 + 2 + 8;  // item queue readers: V loader, MMA lanes, softmax warps
+// full/empty; go (2); item queue full/empty (4); MMA drain (1); Q buffer
+// free (1)
+constexpr int kNumBars = 8 + 2 * kKStages + 2 * kVStages + 2 + 4 + 1 + 1;
+constexpr int kItemReaders = 1 + 1 + 8;  // item queue readers: V loader, MMA lane, softmax warps
 constexpr int kOffSlots = (kOffBar + kNumBars * 8 + 15) & ~15;  // TMEM address (16 B), two item slots (int4)
 static_assert(kOffSlots % 16 == 0, "item slots are 16-byte vectors");
-constexpr int kOffSeen = kOffSlots + 16 + 2 * 16;         // phases seen per K and V stage (ints)
-constexpr int kOffRed = kOffSeen + 16 * 4;
+constexpr int kOffRed = kOffSlots + 16 + 2 * 16;
 constexpr int kSmemBytes = kOffRed + 2 * 2 * BM * 4;     // [team][m, l][row]
-static_assert(kKStages + kVStages <= 16, "phase counters");
 static_assert(kSmemBytes <= 232448, "more shared memory than a CTA may have");
 constexpr unsigned kWaitIters = 1u << 24;
 
@@ -188,14 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar_go = bar_vempty + kVStages;      // [k & 1] Q of the k-th item with work landed (256 arrivals)
     uint64_t *bar_item_full = bar_go + 2;          // [slot] item published
     uint64_t *bar_item_empty = bar_item_full + 2;  // [slot] every role has read it
-    uint64_t *bar_done = bar_item_empty + 2;       // [team] all of the team's MMAs finished
-    uint64_t *bar_qfree = bar_done + 2;            // every S of the k-th item with work finished (2 arrivals)
+    uint64_t *bar_done = bar_item_empty + 2;       // all MMAs finished
+    uint64_t *bar_qfree = bar_done + 1;            // every S of the k-th item with work finished (2 arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffSlots);
     int4 *item_slots = reinterpret_cast<int4 *>(smem + kOffSlots + 16);
     float *red = reinterpret_cast<float *>(smem + kOffRed);  // [team][m, l][row]
-    // [K stages][V stages]: how many phases of each stage's "full" barrier an
-    // MMA lane has seen complete (see wait_full)
-    volatile int *seen = reinterpret_cast<volatile int *>(smem + kOffSeen);
 
     if (tid == 0) {
         for (int t = 0; t < 2; t++) {
@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pkv::tc::mbar_init(bar_pfull + 2 * t + 1, kTeamThreads);
             pkv::tc::mbar_init(bar_item_full + t, 1);
             pkv::tc::mbar_init(bar_item_empty + t, kItemReaders);
-            pkv::tc::mbar_init(bar_done + t, 1);
         }
+        pkv::tc::mbar_init(bar_done, 1);
         pkv::tc::mbar_init(bar_qfree, 2);
         for (int st = 0; st < kKStages; st++) {
             pkv::tc::mbar_init(bar_kfull + st, 1);
@@ -217,7 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             pkv::tc::mbar_init(bar_vempty + st, 1);
         }
         // Q lands by TMA (one arrival with its bytes) or by the softmax threads' copies
-        for (int i = 0; i < kKStages + kVStages; i++) seen[i] = 0;
         pkv::tc::mbar_init(bar_go, p.q_tma ? 1 : 2 * kTeamThreads);
         pkv::tc::mbar_init(bar_go + 1, p.q_tma ? 1 : 2 * kTeamThreads);
         pkv::tc::fence_mbar_init();
@@ -395,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        // ---------------- MMA issue: lane 0 of warp 8 + q issues team q's tiles
-        const int q = warp - kMmaWarp;
-        if (lane == 0) {
+        // ---------------- MMA issue: lane 0 of warp 8 issues every tile of both
+        // teams; warp 9 has no role after the TMEM allocation
+        if (warp == kMmaWarp && lane == 0) {
             int nkt_cur = 0;  // key tiles of the item being issued
             auto issue_s = [&](int t) {  // S(t) = Q K(t)^T into the S/P buffer of team t & 1 (K(t) landed)
                 const uint32_t qa = sbase + kOffQ;
@@ -410,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 pkv::tc::mma_commit(bar_kempty + ((kt_base + t) % kKStages));
                 pkv::tc::mma_commit(bar_s + (t & 1));
-                if (t + 2 >= nkt_cur) pkv::tc::mma_commit(bar_qfree);  // this lane's last read of Q
+                // the item's last two S are the last reads of Q: the Q barrier
+                // expects two arrivals per item
+                if (t + 2 >= nkt_cur) pkv::tc::mma_commit(bar_qfree);
             };
             // O(team t & 1) (+)= P(t) V(t) over keys 64h .. 64h+63 (V(t) landed,
             // that half of P(t) stored)
@@ -428,24 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pkv::tc::mma_commit(bar_o + (t & 1));
                 }
             };
-            // A ring stage's consecutive tiles can belong to different teams,
-            // hence to different MMA lanes.  A lane must not wait on a phase
-            // of a stage's "full" barrier before the previous phase has been
-            // seen complete: a parity wait cannot tell "phase k done" from
-            // "phase k-1 still running".  So each wait first lets the
-            // stage's count of seen phases reach this phase's index (the
-            // other lane moves it), then waits, then counts this phase.
-            auto wait_full = [&](uint64_t *full, volatile int *cnt, int g, int nst) {
-                const int s = g % nst, ph = g / nst;
-                unsigned n = 0;
-                while (!failed && cnt[s] < ph) {
-                    if (++n > kWaitIters) failed = true;
-                }
-                wait(full + s, (unsigned)(ph & 1));
-                cnt[s] = ph + 1;
+            auto wait_k = [&](int t) {
+                const int g = kt_base + t;
+                wait(bar_kfull + g % kKStages, (unsigned)((g / kKStages) & 1));
             };
-            auto wait_k = [&](int t) { wait_full(bar_kfull, seen, kt_base + t, kKStages); };
-            auto wait_v = [&](int t) { wait_full(bar_vfull, seen + kKStages, kt_base + t, kVStages); };
+            auto wait_v = [&](int t) {
+                const int g = kt_base + t;
+                wait(bar_vfull + g % kVStages, (unsigned)((g / kVStages) & 1));
+            };
             for (int i = 0;; i++) {
                 // Take item i alone (the other lanes idle).  The slot is
                 // reported read only after this item's Q barrier has been
@@ -460,18 +451,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!it.skip) {
                     const int nkt = it.nkt;
                     nkt_cur = nkt;
-                    const int tb = q ? team_base1 : team_base0;  // this team's tiles before this item
-                    if (q >= nkt) pkv::tc::mbar_arrive(bar_qfree);  // no S of this lane reads this Q
-                    if (q < nkt) {
-                        wait_k(q);
+                    if (nkt == 1) pkv::tc::mbar_arrive(bar_qfree);  // one S reads this Q
+                    for (int t = 0; t < nkt && t < 2; t++) {
+                        wait_k(t);
                         pkv::tc::fence_after_sync();
-                        issue_s(q);
+                        issue_s(t);
                     }
-                    for (int t = q; t < nkt; t += 2) {
-                        // PV(t) as soon as P(t) is stored; S(t+2) behind it once K(t+2)
-                        // has landed, so a late K tile never holds up a PV
+                    // One issuing thread, tiles in order: the tensor pipe runs PV(t),
+                    // S(t+2), PV(t+1), S(t+3), ...  Each team's next S is queued right
+                    // behind its own PV, a whole unit before the other team's, which
+                    // keeps the two teams' softmax phases apart.  PV(t) goes half by
+                    // half as P(t) is stored (the first half runs while the team
+                    // computes the second); S(t+2) follows once K(t+2) has landed.
+                    for (int t = 0; t < nkt; t++) {
+                        const int tb = (t & 1) ? team_base1 : team_base0;  // the team's tiles before this item
                         wait_v(t);
-                        for (int h = 0; h < 2; h++) {  // the first half runs while the team computes the second
+                        for (int h = 0; h < 2; h++) {
                             wait(bar_pfull + 2 * (t & 1) + h, (unsigned)((tb + (t >> 1)) & 1));
                             pkv::tc::fence_after_sync();
                             issue_pv_half(t, h);
@@ -485,9 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 advance(it);
             }
-            // every MMA of this lane has finished before TMEM is released
-            pkv::tc::mma_commit(bar_done + q);
-            if (!pkv::tc::mbar_wait(bar_done + q, 0, kWaitIters)) failed = true;
+            // every MMA has finished before TMEM is released
+            pkv::tc::mma_commit(bar_done);
+            if (!pkv::tc::mbar_wait(bar_done, 0, kWaitIters)) failed = true;
         }
         __syncwarp();
     } else {
