@@ -287,6 +287,89 @@ int pkv_paged_attention_prefill_chunk(const void *q, const int32_t *cu_q_lens,
                                       int out_dtype, void *workspace, size_t workspace_bytes,
                                       void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Host block manager (host memory only; no CUDA call).
+ *
+ * Keeps the mapping the kernels above consume: which physical cache blocks
+ * hold each sequence's tokens (its block table), which blocks are shared and
+ * how often (reference counts), and which full blocks hold a known token
+ * prefix so that a later prompt starting with the same tokens reuses them.
+ * Source: ainews "PagedAttention" (logical blocks mapped to physical blocks,
+ * allocated on demand, shared between sequences, copy-on-write when a shared
+ * block must change); #47 §5.2 (block table); runtime "Paging" and "Prefix
+ * caching" (reuse of cached prefix blocks, least-recently-used eviction).
+ *
+ * Blocks hold PKV_BLOCK_SIZE tokens.  A block is
+ *   - free (in no table, content unknown),
+ *   - in use (reference count >= 1: the number of sequences whose table
+ *     holds it), or
+ *   - cached (reference count 0 but full, with its token content and prefix
+ *     registered; reusable by a matching prompt, evicted least recently
+ *     used first when no free block is left).
+ * Only full blocks are registered.  A block's identity in the prefix index
+ * is a 64-bit chain hash of its 16 token ids and the hash of the block
+ * before it; a hit also compares the stored token ids.
+ *
+ * The manager is not thread-safe.  Sequence ids are the caller's (any
+ * int64).  Errors: PKV_ERR_INVALID for bad arguments or unknown / duplicate
+ * sequence ids, PKV_ERR_OOB when the blocks needed are not available (the
+ * call then changes nothing).
+ * ------------------------------------------------------------------------- */
+
+/* *bm: a new manager over blocks [0, num_blocks); tables are at most
+ * max_blocks_per_seq blocks wide.  prefix_cache 0 disables the prefix index
+ * (every block is freed when its last sequence ends). */
+int pkv_bm_create(int num_blocks, int max_blocks_per_seq, int prefix_cache, void **bm);
+
+/* Releases the manager. */
+int pkv_bm_destroy(void *bm);
+
+/* *free_blocks: blocks a new allocation could take (free + cached);
+ * *cached_blocks: those of them that are cached (may be NULL). */
+int pkv_bm_num_free_blocks(void *bm, int *free_blocks, int *cached_blocks);
+
+/* A new sequence holding the prompt tokens[0 .. num_tokens).  Its leading
+ * full blocks are taken from the prefix index while their token content and
+ * prefix match; *num_cached_tokens (may be NULL) receives how many leading
+ * tokens were found there (their K/V are already in the cache).  The other
+ * tokens get new blocks (the caller writes their K/V, e.g. by a prefill of
+ * tokens [*num_cached_tokens, num_tokens)); new full blocks are registered
+ * in the prefix index at once, so the caller must write them before any
+ * reader of a later prompt uses them. */
+int pkv_bm_add_sequence(void *bm, int64_t seq_id, const int32_t *tokens, int num_tokens,
+                        int *num_cached_tokens);
+
+/* Sequence `child` starts as a copy of `parent`: the same table, every block
+ * shared (reference count + 1).  The first append to either side of a
+ * shared, partly filled last block copies it (see pkv_bm_append_tokens). */
+int pkv_bm_fork(void *bm, int64_t parent, int64_t child);
+
+/* Reserve the slot of one new token for each of seq_ids[0 .. n) (n host
+ * int64 ids; tokens: their token ids, for the prefix index).  The last
+ * block is used when it has room and this sequence alone holds it; a full
+ * last block gets a new block after it; a shared, partly filled last block
+ * is replaced by a new block, and the pair (old, new) is appended to
+ * copy_pairs (host int64 [2 * n] at most) for pkv_copy_blocks, which must
+ * run before the tokens' K/V are written.  slot_mapping (host int64 [n])
+ * receives block * 16 + offset for each token, *num_pairs the number of
+ * pairs.  A block that becomes full is registered in the prefix index. */
+int pkv_bm_append_tokens(void *bm, const int64_t *seq_ids, int n, const int32_t *tokens,
+                         int64_t *slot_mapping, int64_t *copy_pairs, int *num_pairs);
+
+/* Slots of tokens [first, first + n) of a sequence (host int64 [n]), e.g.
+ * the prompt tokens a prefill writes. */
+int pkv_bm_slots(void *bm, int64_t seq_id, int first, int n, int64_t *slots);
+
+/* The sequence ends: every block's reference count drops by one; a block
+ * left unreferenced becomes cached if it is registered, else free. */
+int pkv_bm_free_sequence(void *bm, int64_t seq_id);
+
+/* Block tables and lengths for seq_ids[0 .. n): tables is host int32
+ * [n][max_blocks] (unused entries -1), context_lens host int32 [n] (may be
+ * NULL).  Fails if a table is wider than max_blocks. */
+int pkv_bm_block_tables(void *bm, const int64_t *seq_ids, int n, int32_t *tables, int max_blocks,
+                        int32_t *context_lens);
+
 /*
  * Synchronises `stream`, then reads and clears the status word of the current
  * device.  *flags (host pointer, may be NULL) receives the PKV_STATUS_* bits.

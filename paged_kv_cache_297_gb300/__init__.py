@@ -46,6 +46,8 @@ EXPORTED = (
     "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_last_error_string",
     "pkv_version",
+    "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free_blocks", "pkv_bm_add_sequence", "pkv_bm_fork",
+    "pkv_bm_append_tokens", "pkv_bm_slots", "pkv_bm_free_sequence", "pkv_bm_block_tables",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -93,6 +95,16 @@ def load():
     lib.pkv_get_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
     lib.pkv_last_error_string.argtypes = []
     lib.pkv_version.argtypes = []
+    L = ctypes.c_int64
+    lib.pkv_bm_create.argtypes = [I, I, I, ctypes.POINTER(P)]
+    lib.pkv_bm_destroy.argtypes = [P]
+    lib.pkv_bm_num_free_blocks.argtypes = [P, ctypes.POINTER(I), ctypes.POINTER(I)]
+    lib.pkv_bm_add_sequence.argtypes = [P, L, P, I, ctypes.POINTER(I)]
+    lib.pkv_bm_fork.argtypes = [P, L, L]
+    lib.pkv_bm_append_tokens.argtypes = [P, P, I, P, P, P, ctypes.POINTER(I)]
+    lib.pkv_bm_slots.argtypes = [P, L, I, I, P]
+    lib.pkv_bm_free_sequence.argtypes = [P, L]
+    lib.pkv_bm_block_tables.argtypes = [P, P, I, P, I, P]
     for name in EXPORTED:
         getattr(lib, name).restype = I
     lib.pkv_last_error_string.restype = ctypes.c_char_p
@@ -332,3 +344,81 @@ def get_status(stream=None) -> int:
     if rc == ERR_CUDA:
         _check(rc)
     return int(flags.value)
+
+
+class BlockManager:
+    """Host block manager (``pkv_bm_*``): physical block allocation with
+    reference counts, copy-on-write and a prefix index over full blocks.
+    Produces the block tables, context lengths, slot mappings and copy pairs
+    that the kernels take.  Host memory only; returns CPU tensors."""
+
+    def __init__(self, num_blocks: int, max_blocks_per_seq: int, prefix_cache: bool = True):
+        h = ctypes.c_void_p()
+        _check(load().pkv_bm_create(int(num_blocks), int(max_blocks_per_seq), int(bool(prefix_cache)),
+                                    ctypes.byref(h)))
+        self._h = h
+        self.max_blocks_per_seq = int(max_blocks_per_seq)
+
+    def close(self) -> None:
+        if self._h:
+            _check(load().pkv_bm_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free_blocks(self):
+        """(blocks a new allocation could take, of which cached)"""
+        f, c = ctypes.c_int(0), ctypes.c_int(0)
+        _check(load().pkv_bm_num_free_blocks(self._h, ctypes.byref(f), ctypes.byref(c)))
+        return f.value, c.value
+
+    def add_sequence(self, seq_id: int, tokens) -> int:
+        """New sequence with prompt ``tokens``; returns how many leading
+        tokens were found in the prefix index."""
+        t = torch.as_tensor(tokens, dtype=torch.int32).contiguous()
+        n = ctypes.c_int(0)
+        _check(load().pkv_bm_add_sequence(self._h, int(seq_id), t.data_ptr() if t.numel() else None,
+                                          t.numel(), ctypes.byref(n)))
+        return n.value
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(load().pkv_bm_fork(self._h, int(parent), int(child)))
+
+    def append_tokens(self, seq_ids, tokens):
+        """One new token per sequence: returns (slot_mapping int64 [n],
+        copy pairs int64 [p, 2]) for copy_blocks then kv_append."""
+        ids = torch.as_tensor(seq_ids, dtype=torch.int64).contiguous()
+        tok = torch.as_tensor(tokens, dtype=torch.int32).contiguous()
+        if ids.shape != tok.shape or ids.dim() != 1:
+            raise ValueError("seq_ids and tokens must be 1-D of the same length")
+        n = ids.numel()
+        slots = torch.empty(n, dtype=torch.int64)
+        pairs = torch.empty(max(1, 2 * n), dtype=torch.int64)
+        np_ = ctypes.c_int(0)
+        _check(load().pkv_bm_append_tokens(self._h, ids.data_ptr() if n else None, n,
+                                           tok.data_ptr() if n else None, slots.data_ptr(),
+                                           pairs.data_ptr(), ctypes.byref(np_)))
+        return slots, pairs[: 2 * np_.value].view(-1, 2).clone()
+
+    def slots(self, seq_id: int, first: int, n: int) -> torch.Tensor:
+        out = torch.empty(max(1, n), dtype=torch.int64)
+        _check(load().pkv_bm_slots(self._h, int(seq_id), int(first), int(n), out.data_ptr()))
+        return out[:n]
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check(load().pkv_bm_free_sequence(self._h, int(seq_id)))
+
+    def block_tables(self, seq_ids, max_blocks: Optional[int] = None):
+        """(block tables int32 [n, max_blocks], context lengths int32 [n])"""
+        ids = torch.as_tensor(seq_ids, dtype=torch.int64).contiguous()
+        w = int(max_blocks or self.max_blocks_per_seq)
+        n = ids.numel()
+        tables = torch.empty((max(1, n), w), dtype=torch.int32)
+        lens = torch.empty(max(1, n), dtype=torch.int32)
+        _check(load().pkv_bm_block_tables(self._h, ids.data_ptr() if n else None, n, tables.data_ptr(), w,
+                                          lens.data_ptr()))
+        return tables[:n], lens[:n]

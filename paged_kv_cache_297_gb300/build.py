@@ -1,6 +1,6 @@
 """Build ``libpkv.so`` in-tree with nvcc for sm_103a (GB300).
 
-Each ``csrc/*.cu`` is compiled to an object in parallel, then linked into one
+Each ``csrc/*.cu`` (and host-only ``*.cpp``) is compiled to an object in parallel, then linked into one
 shared library next to this file.  Objects are rebuilt only when their source
 or a header changed.  ``python -m paged_kv_cache_297_gb300.build`` runs it.
 """
@@ -41,13 +41,13 @@ def _newer(target: str, deps: list[str]) -> bool:
 
 def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     cc = nvcc()
     extra = list(extra or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         if _newer(obj, [src] + headers) or extra:
             cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
             if verbose:
