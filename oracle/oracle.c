@@ -31,7 +31,13 @@
  * in logical order.  A sequence with L = 0 gets an all-zero output row.
  *
  * Element types: 0 = IEEE binary32, 1 = bfloat16 (the upper 16 bits of a
- * binary32).  Every value is widened exactly to double before use.
+ * binary32), 2 = fp8 E4M3 (quantised cache, chengxuchu #47 / the runtime
+ * page on KV-cache memory, section 2.4: 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; exponent 0 is subnormal, m * 2^-9; the code
+ * S.1111.111 is NaN and there is no infinity, so the largest finite value
+ * is 448).  An fp8 cache stores K / scale and V / scale with one scale per
+ * kv head; reading multiplies back.  Every value is widened exactly to
+ * double before use.
  */
 #include <math.h>
 #include <stdint.h>
@@ -45,7 +51,44 @@
 #define ORC_BAD_ARG -1
 #define ORC_BAD_INDEX -2
 
+/* Value of an E4M3 code, from the format's definition. */
+static double e4m3_value(uint8_t c) {
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+double oracle_e4m3_decode(uint8_t c) { return e4m3_value(c); }
+
+/*
+ * E4M3 code of a binary32 value: the nearest finite code, ties to the code
+ * with an even mantissa (round to nearest even), magnitudes beyond 448 to
+ * 448 (saturation); NaN to the NaN code.  Found by trying every code, the
+ * plainest correct way.
+ */
+uint8_t oracle_e4m3_encode(float f) {
+    if (isnan(f)) return 0x7F;
+    uint8_t sign = signbit(f) ? 0x80 : 0;
+    double a = fabs((double)f);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c < 127; c++) { /* every finite non-negative code */
+        double err = fabs(e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
 static double widen(const void *base, int64_t i, int dtype) {
+    if (dtype == 2) return e4m3_value(((const uint8_t *)base)[i]);
     if (dtype == 0) {
         float f;
         memcpy(&f, (const char *)base + 4 * i, 4);
@@ -61,7 +104,7 @@ static double widen(const void *base, int64_t i, int dtype) {
     }
 }
 
-static int elem_bytes(int dtype) { return dtype == 0 ? 4 : 2; }
+static int elem_bytes(int dtype) { return dtype == 0 ? 4 : dtype == 1 ? 2 : 1; }
 
 int oracle_threads(void) {
 #ifdef _OPENMP
@@ -92,6 +135,34 @@ int oracle_kv_append(const void *k, const void *v, const int64_t *slot_mapping, 
     return ORC_OK;
 }
 
+/*
+ * Append into an fp8 E4M3 cache: each element x of token i, kv head g is
+ * stored as the code of the binary32 quotient x / scale[g] (k_scale for K,
+ * v_scale for V), x widened from in_dtype (0 binary32, 1 bfloat16).
+ * Negative slots are skipped, as in oracle_kv_append.
+ */
+int oracle_kv_append_fp8(const void *k, const void *v, int in_dtype, const int64_t *slot_mapping,
+                         int num_tokens, uint8_t *k_cache, uint8_t *v_cache, int num_blocks,
+                         int num_kv_heads, int block_size, int head_dim, const float *k_scale,
+                         const float *v_scale) {
+    for (int i = 0; i < num_tokens; i++) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_blocks * block_size) return ORC_BAD_INDEX;
+        int64_t blk = slot / block_size, r = slot % block_size;
+        for (int g = 0; g < num_kv_heads; g++) {
+            int64_t src = ((int64_t)i * num_kv_heads + g) * head_dim;
+            int64_t dst = (((int64_t)blk * num_kv_heads + g) * block_size + r) * head_dim;
+            for (int j = 0; j < head_dim; j++) {
+                float xk = (float)widen(k, src + j, in_dtype), xv = (float)widen(v, src + j, in_dtype);
+                k_cache[dst + j] = oracle_e4m3_encode(xk / k_scale[g]);
+                v_cache[dst + j] = oracle_e4m3_encode(xv / v_scale[g]);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
 /* Copy whole blocks (every kv head, every row) from src to dst, K and V. */
 int oracle_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
                        int num_blocks, int num_kv_heads, int block_size, int head_dim, int dtype) {
@@ -116,7 +187,8 @@ int oracle_paged_attention(const void *q, int q_dtype, const void *k_cache, cons
                            int kv_dtype, const int32_t *block_tables, int max_blocks,
                            const int32_t *context_lens, const int32_t *cu_q_lens, int num_seqs,
                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                           int num_blocks, double scale, double *out) {
+                           int num_blocks, double scale, const float *k_scale, const float *v_scale,
+                           double *out) {
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || block_size <= 0) return ORC_BAD_ARG;
     int group = num_q_heads / num_kv_heads;
     int rows = cu_q_lens ? cu_q_lens[num_seqs] : num_seqs;
@@ -150,6 +222,8 @@ int oracle_paged_attention(const void *q, int q_dtype, const void *k_cache, cons
         for (int j = 0; j < head_dim; j++) o[j] = 0.0;
         if (ntok <= 0) continue;
         double *x = (double *)malloc(sizeof(double) * ntok);
+        /* per kv head dequantisation scales of an fp8 cache (1 otherwise) */
+        const double ks = k_scale ? (double)k_scale[g] : 1.0, vs = v_scale ? (double)v_scale[g] : 1.0;
         const int32_t *table = block_tables + (size_t)s * max_blocks;
         int64_t qbase = ((int64_t)r * num_q_heads + h) * head_dim;
         /* logits x_t = scale * <q, K_t> */
@@ -164,7 +238,7 @@ int oracle_paged_attention(const void *q, int q_dtype, const void *k_cache, cons
             int64_t kbase = (((int64_t)b * num_kv_heads + g) * block_size + t % block_size) * head_dim;
             double acc = 0.0;
             for (int j = 0; j < head_dim; j++)
-                acc += widen(q, qbase + j, q_dtype) * widen(k_cache, kbase + j, kv_dtype);
+                acc += widen(q, qbase + j, q_dtype) * (widen(k_cache, kbase + j, kv_dtype) * ks);
             x[t] = scale * acc;
             if (x[t] > m) m = x[t];
         }
@@ -176,7 +250,7 @@ int oracle_paged_attention(const void *q, int q_dtype, const void *k_cache, cons
             double w = exp(x[t] - m);
             den += w;
             int64_t vbase = (((int64_t)b * num_kv_heads + g) * block_size + t % block_size) * head_dim;
-            for (int j = 0; j < head_dim; j++) o[j] += w * widen(v_cache, vbase + j, kv_dtype);
+            for (int j = 0; j < head_dim; j++) o[j] += w * (widen(v_cache, vbase + j, kv_dtype) * vs);
         }
         for (int j = 0; j < head_dim; j++) o[j] /= den;
         free(x);

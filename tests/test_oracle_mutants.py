@@ -26,11 +26,18 @@ MUTANTS = {
     "scale_dropped": ("x[t] = scale * acc;", "x[t] = acc;"),
     "max_not_subtracted": ("double w = exp(x[t] - m);", "double w = exp(x[t]);"),
     "no_normalisation": ("o[j] /= den;", "o[j] /= (den > 0 ? 1.0 : 1.0);"),
-    "values_from_keys": ("o[j] += w * widen(v_cache,", "o[j] += w * widen(k_cache,"),
+    "values_from_keys": ("o[j] += w * (widen(v_cache,", "o[j] += w * (widen(k_cache,"),
     "append_wrong_head": ("size_t src = ((size_t)i * num_kv_heads + g) * row;",
                           "size_t src = ((size_t)i * num_kv_heads + (num_kv_heads - 1 - g)) * row;"),
     "copy_only_keys": ("memmove((char *)v_cache + dst * blk", "if (0) memmove((char *)v_cache + dst * blk"),
     "bf16_wrong_half": ("bits = ((uint32_t)h) << 16;", "bits = ((uint32_t)h) << 15;"),
+    "e4m3_ties_to_odd": ("(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    "e4m3_max_code_missing": ("for (int c = 0; c < 127; c++)", "for (int c = 0; c < 126; c++)"),
+    "e4m3_subnormal_exponent": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    "e4m3_bias_off_by_one": ("v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "fp8_append_scale_ignored": ("oracle_e4m3_encode(xk / k_scale[g]);", "oracle_e4m3_encode(xk);"),
+    "fp8_value_scale_dropped": ("* (widen(v_cache, vbase + j, kv_dtype) * vs);",
+                                "* (widen(v_cache, vbase + j, kv_dtype) * 1.0);"),
 }
 
 

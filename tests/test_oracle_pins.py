@@ -303,3 +303,81 @@ def test_block_table_example_gathers_in_table_order():
             kk[ids[t // BS], 0, t % BS, 2] = 1000.0
             out = oracle.decode(q, kk, vc, bt, torch.tensor([L], dtype=torch.int32), 1.0)[0, 0]
             assert round(float(out[0])) == ids[t // BS] and round(float(out[1])) == t % BS
+
+
+# ------------------------------------------------------------------ fp8 (E4M3) cache
+
+def test_e4m3_codes_decode_like_the_library_format():
+    """Every one of the 256 codes widens to torch's float8_e4m3fn value;
+    S.1111.111 is NaN (the format has no infinity)."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    got = oracle.e4m3_decode(codes)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64)
+    nan = ref.isnan()
+    assert nan.nonzero().flatten().tolist() == [127, 255]
+    assert got[nan].isnan().all() and torch.equal(got[~nan], ref[~nan])
+    assert float(got[0x7E]) == 448.0 and float(got[0x01]) == 2.0 ** -9 and float(got[0x38]) == 1.0
+
+
+def test_e4m3_encoding_round_trips_and_matches_the_library_in_range():
+    codes = torch.tensor([c for c in range(256) if c not in (127, 255)], dtype=torch.uint8)
+    vals = oracle.e4m3_decode(codes).to(torch.float32)
+    assert torch.equal(oracle.e4m3_encode(vals), codes)          # -0 -> 0x80 included
+    g = torch.Generator().manual_seed(17)
+    x = torch.cat([torch.randn(4000, generator=g) * s for s in (1e-3, 0.05, 1.0, 30.0, 150.0)])
+    x = x[x.abs() <= 448]
+    assert torch.equal(oracle.e4m3_encode(x), x.to(torch.float8_e4m3fn).view(torch.uint8))
+
+
+def test_e4m3_rounds_ties_to_even_and_saturates():
+    # 1.0625 lies halfway between 1.0 (mantissa 000) and 1.125 (001): even wins;
+    # 1.1875 halfway between 1.125 (001) and 1.25 (010); 2^-10 halfway
+    # between 0 and the smallest subnormal
+    x = torch.tensor([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 449.0, 1e6, -1e6, 464.0])
+    assert oracle.e4m3_encode(x).tolist() == [0x38, 0x3A, 0x00, 0x02, 0x7E, 0x7E, 0xFE, 0x7E]
+
+
+def test_fp8_append_stores_codes_of_the_scaled_rows():
+    NB, H, d = 4, 2, 16
+    g = torch.Generator().manual_seed(3)
+    k = (torch.randn(5, H, d, generator=g) * 40).to(torch.bfloat16)
+    v = (torch.randn(5, H, d, generator=g) * 3).to(torch.bfloat16)
+    ks, vs = torch.tensor([0.25, 3.0]), torch.tensor([0.125, 0.01])
+    slots = torch.tensor([0, 17, -1, 63, 5], dtype=torch.int64)
+    kc = torch.full((NB, H, BS, d), 0x55, dtype=torch.uint8)
+    vc = kc.clone()
+    oracle.kv_append_fp8(k, v, slots, kc, vc, ks, vs)
+    touched = torch.zeros(NB * BS, dtype=torch.bool)
+    def want(x):  # torch's cast in range; beyond 448 the saturated code
+        c = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        return torch.where(x.abs() > 448, torch.where(x > 0, 0x7E, 0xFE).to(torch.uint8), c)
+
+    for i, s in enumerate(slots.tolist()):
+        if s < 0:
+            continue
+        touched[s] = True
+        for h in range(H):
+            assert torch.equal(kc[s // BS, h, s % BS], want(k[i, h].float() / ks[h]))
+            assert torch.equal(vc[s // BS, h, s % BS], want(v[i, h].float() / vs[h]))
+    rest = ~touched.view(NB, BS)
+    assert (kc.permute(0, 2, 1, 3)[rest] == 0x55).all() and (vc.permute(0, 2, 1, 3)[rest] == 0x55).all()
+
+
+def test_fp8_attention_multiplies_the_per_head_scales_back():
+    """An fp8 cache read with per-head power-of-two scales equals the binary32
+    cache holding code value x scale exactly."""
+    NB, Hkv, Hq, d = 6, 2, 4, 16
+    g = torch.Generator().manual_seed(9)
+    kc = torch.randint(0, 256, (NB, Hkv, BS, d), dtype=torch.uint8, generator=g)
+    vc = torch.randint(0, 256, (NB, Hkv, BS, d), dtype=torch.uint8, generator=g)
+    kc[(kc & 0x7F) == 0x7F] = 0x10                           # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0x22
+    ks, vs = torch.tensor([0.5, 4.0]), torch.tensor([2.0 ** -3, 8.0])
+    kf = (oracle.e4m3_decode(kc) * ks.double().view(1, Hkv, 1, 1)).float()
+    vf = (oracle.e4m3_decode(vc) * vs.double().view(1, Hkv, 1, 1)).float()
+    bt = torch.tensor([[3, 1, 5], [0, 2, 4]], dtype=torch.int32)
+    cl = torch.tensor([40, 33], dtype=torch.int32)
+    q = torch.randn(2, Hq, d, generator=g) * 0.05
+    a = oracle.decode(q, kc, vc, bt, cl, 0.3, ks, vs)
+    b = oracle.decode(q, kf, vf, bt, cl, 0.3)
+    assert torch.equal(a, b)
