@@ -208,6 +208,11 @@ class Step:
         # a batch over one shared prefix takes the cascade: the prefix once for
         # all queries on the tensor cores, then each sequence's own tokens
         self.prefix_len = 16 * int(batch.meta.get("prefix_blocks", 0))
+        # fp8 E4M3 caches: the quantising append, then the fp8 decode
+        self.fp8 = batch.k_scale is not None
+        if self.fp8:
+            t["k_scale"], t["v_scale"] = batch.k_scale.to(dev), batch.v_scale.to(dev)
+            self.fused = False
         self.cascade = (self.fused and not no_cascade and self.prefix_len > 0
                         and batch.dtype == torch.bfloat16 and d == 128)
         if self.cascade:
@@ -242,6 +247,15 @@ class Step:
         if self.has_copy:
             out.append(("copy_blocks", lambda: pkv.copy_blocks(t["copy_pairs"], t["k_cache"],
                                                                t["v_cache"])))
+        if self.fp8:
+            out.append(("kv_append", lambda: pkv.kv_append_fp8(t["k_new"], t["v_new"], t["slot_mapping"],
+                                                               t["k_cache"], t["v_cache"], t["k_scale"],
+                                                               t["v_scale"])))
+            out.append(("decode", lambda: pkv.paged_attention_decode_fp8(
+                t["q"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"], t["block_tables"],
+                t["context_lens"], b.scale, self.out, max_context_len=self.max_ctx,
+                partition_size=self.partition, workspace=self.ws)))
+            return out
         if self.cascade:
             out.append(("decode", lambda: pkv.decode_shared_prefix(
                 t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"], b.scale,
@@ -390,8 +404,13 @@ def cpu_baseline(batch: W.Batch, budget_s: float = 12.0):
     while True:
         if batch.copy_pairs is not None and batch.copy_pairs.numel():
             oracle.copy_blocks(kc, vc, batch.copy_pairs)
-        oracle.kv_append(batch.k_new, batch.v_new, batch.slot_mapping, kc, vc)
-        oracle.decode(batch.q, kc, vc, batch.block_tables, batch.context_lens, batch.scale)
+        if batch.k_scale is not None:
+            oracle.kv_append_fp8(batch.k_new, batch.v_new, batch.slot_mapping, kc, vc, batch.k_scale,
+                                 batch.v_scale)
+        else:
+            oracle.kv_append(batch.k_new, batch.v_new, batch.slot_mapping, kc, vc)
+        oracle.decode(batch.q, kc, vc, batch.block_tables, batch.context_lens, batch.scale, batch.k_scale,
+                      batch.v_scale)
         if batch.prefill_q is not None:
             oracle.prefill_chunk(batch.prefill_q, batch.prefill_cu_q_lens, kc, vc,
                                  batch.prefill_block_tables, batch.prefill_context_lens,
@@ -414,6 +433,10 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     batch = W.make_batch(args.workload, poison=False)
+    if args.kv_dtype == "fp8":
+        if batch.prefill_q is not None or batch.spec.head_dim != 128 or batch.dtype != torch.bfloat16:
+            raise SystemExit("--kv-dtype fp8 needs a bf16, head_dim 128, decode-only workload")
+        batch = W.fp8_batch(batch)
     step = Step(batch, dev, args.partition, args.unfused, args.no_cascade)
     peaks = read_peaks()
 
@@ -431,8 +454,9 @@ def run_ours(args):
     value = world * seqs_per_step * args.steps / (span_ms / 1e3)
     S, Hq, d = batch.q.shape
     elem = batch.q.element_size()
+    kv_elem = batch.k_cache.element_size()  # 1 for fp8 caches
     # context lengths the decode call sees (after this step's append)
-    db = accounting.decode_bytes(batch.context_lens, Hq, batch.spec.num_kv_heads, d, elem, elem)
+    db = accounting.decode_bytes(batch.context_lens, Hq, batch.spec.num_kv_heads, d, kv_elem, elem, elem)
     ab = accounting.append_bytes(int(batch.slot_mapping.numel()), batch.spec.num_kv_heads, d, elem)
     dec_ms = per_call["decode"]
     # the fused call also writes the appended K and V rows (it reads them from
@@ -443,13 +467,15 @@ def run_ours(args):
         dec_bytes -= step.prefix_len * (S - 1) * 2 * batch.spec.num_kv_heads * d * elem
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
     kname = ("decode_shared_prefix" if step.cascade else "decode_step" if step.fused
-             else "paged_attention_decode")
+             else "paged_attention_decode_fp8" if step.fp8 else "paged_attention_decode")
     traffic = recorded_traffic(kname, args.workload, DECODE_SOURCES)
     roofline = {"kernel": ("decode_shared_prefix (fused append; shared-prefix tile on the tensor cores, "
                            "partition kernel over each sequence's own tokens, log-sum-exp merge; bytes "
                            "count the prefix once)" if step.cascade else
                            "decode_step (fused append + partition kernel + log-sum-exp reduce)"
                            if step.fused else
+                           "paged_attention_decode_fp8 (fp8 E4M3 cache converted in shared memory, "
+                           "fp16 tile products; partition kernel + log-sum-exp reduce)" if step.fp8 else
                            "paged_attention_decode (partition kernel + log-sum-exp reduce)"),
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
@@ -472,9 +498,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "seq-steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if step.fp8 else "bf16"
         if batch.dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "seqs": S, "q_heads": Hq,
+        "config": {"workload": args.workload + ("_fp8" if step.fp8 else ""), "seqs": S, "q_heads": Hq,
                    "kv_heads": batch.spec.num_kv_heads, "head_dim": d, "block_size": 16,
                    "max_context_len": batch.max_context_len,
                    "mean_context_len": round(float(batch.context_lens.float().mean()), 1),
@@ -563,6 +589,8 @@ def main(argv=None):
                     help="separate append and decode calls even where the fused step applies")
     ap.add_argument("--no-cascade", action="store_true",
                     help="plain decode even where the batch shares a prefix")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="fp8: the same step over fp8 E4M3 caches (decode-only workloads)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -57,6 +57,7 @@ extern "C" {
 /* element types */
 #define PKV_F32 0
 #define PKV_BF16 1
+#define PKV_FP8_E4M3 2  /* cache element: fp8 E4M3 code of value / scale (per kv head); 1 byte */
 
 /* status-word bits (pkv_get_status) */
 #define PKV_STATUS_BAD_SLOT 1u       /* kv_append: slot >= num_blocks * block_size */
@@ -86,6 +87,22 @@ int pkv_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int
                   int block_size, int dtype, void *stream);
 
 /*
+ * KV append into an fp8 E4M3 cache (quantised KV cache; the runtime page on
+ * KV-cache memory, section 2.4).  As pkv_kv_append, except that each element
+ * x of kv head g is stored as the E4M3 code of the binary32 quotient
+ * x / k_scale[g] (K) or x / v_scale[g] (V): round to nearest even, magnitudes
+ * beyond 448 saturated to 448, NaN to the NaN code.
+ *   k, v          [num_tokens][num_kv_heads][head_dim], in_dtype (PKV_F32 or
+ *                 PKV_BF16), 16-byte aligned
+ *   k_cache, v_cache  [num_blocks][num_kv_heads][16][head_dim] bytes
+ *   k_scale, v_scale  [num_kv_heads] float32 device arrays, positive
+ */
+int pkv_kv_append_fp8(const void *k, const void *v, int in_dtype, const int64_t *slot_mapping,
+                      int num_tokens, void *k_cache, void *v_cache, const float *k_scale,
+                      const float *v_scale, int num_blocks, int num_kv_heads, int head_dim,
+                      int block_size, void *stream);
+
+/*
  * Copy-on-write block copy.  ainews article, "PagedAttention": when requests
  * sharing prefix blocks diverge, only the forked block is copied.
  *   src_dst_pairs  [num_pairs][2] int64 (src, dst): block dst of both caches
@@ -93,6 +110,7 @@ int pkv_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int
  *                  Destinations must be distinct and must not be sources of
  *                  the same call (caller contract).  An id outside
  *                  [0, num_blocks) skips the pair and sets PKV_STATUS_BAD_BLOCK.
+ *   dtype          PKV_F32, PKV_BF16 or PKV_FP8_E4M3 (bytes are copied).
  */
 int pkv_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, int num_pairs,
                     int num_blocks, int num_kv_heads, int head_dim, int block_size, int dtype,
@@ -152,6 +170,28 @@ int pkv_paged_attention_decode(const void *q, const void *k_cache, const void *v
                                int max_context_len, int partition_size, float scale, void *out,
                                int dtype, int out_dtype, void *workspace, size_t workspace_bytes,
                                void *stream);
+
+/*
+ * Decode over fp8 E4M3 caches (written by pkv_kv_append_fp8): as
+ * pkv_paged_attention_decode with bf16 queries, where cached element x of kv
+ * head g stands for x * k_scale[g] (K) or x * v_scale[g] (V).  head_dim must
+ * be 128.  The workspace is sized by pkv_decode_workspace_bytes.
+ *   q             [num_seqs][num_q_heads][128] bf16
+ *   k_cache, v_cache  [num_blocks][num_kv_heads][16][128] bytes
+ *   k_scale, v_scale  [num_kv_heads] float32 device arrays
+ *   out           [num_seqs][num_q_heads][128], out_dtype
+ * Precision: codes widen to fp16 exactly; q is rounded to fp16 once (a
+ * query beyond the fp16 range, 65504, overflows); the softmax weights enter
+ * the value product as fp16; accumulation is fp32.
+ */
+int pkv_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   int max_context_len, int partition_size, float scale, void *out,
+                                   int out_dtype, void *workspace, size_t workspace_bytes,
+                                   void *stream);
 
 /*
  * One decode step: append, then attend, in one launch.  Equivalent to

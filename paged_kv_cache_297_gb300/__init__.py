@@ -35,7 +35,7 @@ __all__ = [
 BLOCK_SIZE = 16
 DEFAULT_PARTITION = 512
 OK, ERR_INVALID, ERR_CUDA, ERR_OOB = 0, 1, 2, 3
-F32, BF16 = 0, 1
+F32, BF16, FP8_E4M3 = 0, 1, 2  # FP8_E4M3: a uint8 tensor of E4M3 codes
 STATUS_BITS = {"bad_slot": 1, "bad_block": 2, "bad_length": 4, "bad_qlen": 8, "internal": 16}
 
 # every entry point declared in include/pkv.h
@@ -46,6 +46,7 @@ EXPORTED = (
     "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_last_error_string",
     "pkv_version",
+    "pkv_kv_append_fp8", "pkv_paged_attention_decode_fp8",
     "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free_blocks", "pkv_bm_add_sequence", "pkv_bm_fork",
     "pkv_bm_append_tokens", "pkv_bm_slots", "pkv_bm_free_sequence", "pkv_bm_block_tables",
 )
@@ -95,6 +96,9 @@ def load():
     lib.pkv_get_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
     lib.pkv_last_error_string.argtypes = []
     lib.pkv_version.argtypes = []
+    lib.pkv_kv_append_fp8.argtypes = [P, P, I, P, I, P, P, P, P, I, I, I, I, P]
+    lib.pkv_paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I, P,
+                                                   SZ, P]
     L = ctypes.c_int64
     lib.pkv_bm_create.argtypes = [I, I, I, ctypes.POINTER(P)]
     lib.pkv_bm_destroy.argtypes = [P]
@@ -123,6 +127,8 @@ def _dt(t: torch.Tensor) -> int:
         return F32
     if t.dtype == torch.bfloat16:
         return BF16
+    if t.dtype == torch.uint8:
+        return FP8_E4M3
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -216,6 +222,54 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         _dev(block_tables, "block_tables", torch.int32), mb,
         _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, d, bs, NB,
         int(max_context_len), int(partition_size), float(scale), _dev(out, "out"), _dt(q),
+        _dt(out), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def kv_append_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None) -> None:
+    """Append into fp8 E4M3 caches (uint8 tensors): element x of kv head g is
+    stored as the code of x / scale[g] (nearest even, saturated at 448)."""
+    NB, H, bs, d = _cache_dims(k_cache, v_cache)
+    if k_cache.dtype != torch.uint8:
+        raise TypeError("fp8 caches are uint8 tensors of E4M3 codes")
+    if k.dim() != 3 or k.shape[1:] != (H, d) or v.shape != k.shape or k.dtype != v.dtype:
+        raise ValueError("k/v must be [num_tokens, num_kv_heads, head_dim]")
+    for sc, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if sc.shape != (H,):
+            raise ValueError(f"{name} must be [num_kv_heads]")
+    _check(load().pkv_kv_append_fp8(
+        _dev(k, "k"), _dev(v, "v"), _dt(k), _dev(slot_mapping, "slot_mapping", torch.int64), int(k.shape[0]),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(k_scale, "k_scale", torch.float32),
+        _dev(v_scale, "v_scale", torch.float32), NB, H, d, bs, _stream(stream)))
+
+
+def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+                               max_context_len: Optional[int] = None, partition_size: int = 0,
+                               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode with bf16 queries over fp8 E4M3 caches (uint8), cached element x
+    of kv head g standing for x * scale[g]."""
+    NB, Hkv, bs, d = _cache_dims(k_cache, v_cache)
+    S, Hq, dq = q.shape
+    if k_cache.dtype != torch.uint8 or q.dtype != torch.bfloat16 or dq != d:
+        raise ValueError("q must be bf16 [S, Hq, head_dim] over uint8 (E4M3) caches")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks] and context_lens [S]")
+    mb = int(block_tables.shape[1])
+    if max_context_len is None:
+        max_context_len = mb * bs
+    need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pkv_paged_attention_decode_fp8(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+        _dev(block_tables, "block_tables", torch.int32), mb,
+        _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, d, bs, NB,
+        int(max_context_len), int(partition_size), float(scale), _dev(out, "out"),
         _dt(out), ws_ptr, ws_bytes, _stream(stream)))
     return out
 

@@ -22,18 +22,21 @@ def kv_cache_bytes(layers: int, batch: int, kv_heads: int, seq_len: int, head_di
 
 
 def decode_bytes(context_lens: torch.Tensor, num_q_heads: int, num_kv_heads: int,
-                 head_dim: int, elem: int, out_elem: int) -> dict:
+                 head_dim: int, elem: int, out_elem: int, q_elem: int | None = None) -> dict:
     """Bytes one decode launch must move at minimum.
 
-    KV: every cached token of every sequence, K and V, each kv head once.
-    Plus the query and output rows, each sequence's used block-table entries
-    and its context length.  Split-K partials are overhead and not counted.
+    KV: every cached token of every sequence, K and V, each kv head once
+    (``elem`` bytes per cached element: 1 for an fp8 cache).  Plus the query
+    (``q_elem``, default ``elem``) and output rows, each sequence's used
+    block-table entries and its context length.  Split-K partials are
+    overhead and not counted.
     """
+    q_elem = elem if q_elem is None else q_elem
     L = context_lens.to(torch.int64)
     tokens = int(L.sum())
     kv = kv_cache_bytes(1, 1, num_kv_heads, tokens, head_dim, elem)
     S = int(L.numel())
-    qo = S * num_q_heads * head_dim * (elem + out_elem)
+    qo = S * num_q_heads * head_dim * (q_elem + out_elem)
     tables = int(((L + BLOCK_SIZE - 1) // BLOCK_SIZE).sum()) * 4 + S * 4
     return {"kv": kv, "q_out": qo, "tables": tables, "total": kv + qo + tables}
 

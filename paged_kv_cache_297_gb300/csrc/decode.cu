@@ -66,6 +66,9 @@ struct DecodeParams {
     // (kv head, chunk)'s partition and merge (set by the host, see
     // use_head_warps)
     int head_warps;
+    // fp8 E4M3 caches: per kv head scales (stored = value / scale), else null
+    const float *k_scale;
+    const float *v_scale;
 };
 
 // Partitions of the tokens this launch covers for a sequence of L tokens.
@@ -108,12 +111,15 @@ __device__ __forceinline__ int clamp_len(int L, int cap, unsigned *status, bool 
 // bf16 tensor-core decode
 // ----------------------------------------------------------------------------
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct DecodeSmem {
-    static constexpr int kRowBytes = D * 2;
+    // ring depth in blocks: an fp8 block is half the bytes, so twice the
+    // blocks keep as many bytes in flight (what an HBM-bound warp needs)
+    static constexpr int kRing = kFp8 ? 2 * kStages : kStages;
+    static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);   // one cached row
     static constexpr int kTile = kBlock * kRowBytes;      // one block of one kv head
     static constexpr int kStage = 2 * kTile;               // K + V
-    static constexpr int kWarp = kStages * kStage;
+    static constexpr int kWarp = kRing * kStage;
     static constexpr int kStaging = kWarps * kWarp;
     static constexpr int kMergeStride = D + 8;             // floats per merged row
     static constexpr int kMergeWarp = kRows * kMergeStride + 2 * kRows;
@@ -121,10 +127,24 @@ struct DecodeSmem {
     static constexpr int kBytes = kStaging > kMerge ? kStaging : kMerge;
 };
 
-template <int D, typename OutT, bool kHeadWarps>
+// kFp8: the cache holds fp8 E4M3 codes of value / scale (per kv head).  The
+// codes go from the shared-memory ring straight into mma.sync fragments,
+// widened to fp16 (exact) in registers: fp16 tile products with fp32
+// accumulation (the query rounded to fp16 once, P as one fp16 operand), the
+// K scale folded into the softmax scale, the V scale applied to the output.
+// Two permutations let whole 4-byte words feed the fragments:
+//  - S = q.K^T sums over d, so any order of d serves if q and K agree:
+//    in k-step kk, thread (gid, tig) supplies d = 32 tig + 4 kk + {0,1} as
+//    fragment positions {2 tig, 2 tig + 1} and + {2, 3} as {2 tig + 8,
+//    2 tig + 9}; its 32 K codes of a token are one 32-byte run.
+//  - O = P.V is computed in a permuted d order, undone at the store:
+//    column n of n-tile 4 m + j is d = 32 m + 4 n + j, so one 4-byte word
+//    of a token row serves four n-tiles, and two rows' words, byte-permuted,
+//    give the (token, token + 1) pairs of the B fragments.
+template <int D, typename OutT, bool kHeadWarps, bool kFp8 = false>
 __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodeParams p) {
-    using Sm = DecodeSmem<D>;
-    constexpr int CH = D / 8;                 // 16-byte chunks per row
+    using Sm = DecodeSmem<D, kFp8>;
+    constexpr int CH = Sm::kRowBytes / 16;    // 16-byte chunks per cached row
     constexpr int PER_LANE = kBlock * CH / 32;
     constexpr int KSTEPS = D / 16;
     constexpr int NT = D / 8;                 // n-tiles of the output
@@ -173,8 +193,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
     const int n = kHeadWarps ? nblk : max(0, (nblk - warp + kWarps - 1) / kWarps);
 
     const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
-    const __nv_bfloat16 *kc = static_cast<const __nv_bfloat16 *>(p.k_cache);
-    const __nv_bfloat16 *vc = static_cast<const __nv_bfloat16 *>(p.v_cache);
+    const unsigned char *kc = static_cast<const unsigned char *>(p.k_cache);
+    const unsigned char *vc = static_cast<const unsigned char *>(p.v_cache);
 
     // query rows of this tile as mma A fragments (rows >= `rows` are zero)
     uint32_t qa[KSTEPS][4];
@@ -189,10 +209,26 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
             qa[kk][1] = vb ? *reinterpret_cast<const uint32_t *>(qb_row + col) : 0u;
             qa[kk][2] = va ? *reinterpret_cast<const uint32_t *>(qa_row + col + 8) : 0u;
             qa[kk][3] = vb ? *reinterpret_cast<const uint32_t *>(qb_row + col + 8) : 0u;
+            if constexpr (kFp8) {
+                // the permuted d order (see above), as fp16 pairs
+                const int pcol = 32 * tig + 4 * kk;
+                const uint2 ra = va ? *reinterpret_cast<const uint2 *>(qa_row + pcol) : make_uint2(0u, 0u);
+                const uint2 rb = vb ? *reinterpret_cast<const uint2 *>(qb_row + pcol) : make_uint2(0u, 0u);
+                const uint32_t w[4] = {ra.x, rb.x, ra.y, rb.y};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
+                    qa[kk][e] = pkv::pack_f16(__low2float(h2), __high2float(h2));
+                }
+            }
         }
     }
+    // softmax scale in base-2 units (fp8: times the kv head's K scale) and
+    // the output factor (fp8: the V scale)
+    const float sl2 = kFp8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
+    const float vsc = kFp8 ? p.v_scale[kvh] : 1.f;
 
-    if (p.k_new && part == nparts - 1 && L > 0) {
+    if (!kFp8 && p.k_new && part == nparts - 1 && L > 0) {
         // the new row is read below through L2 by other threads
         if (kHeadWarps) {
             // (warps of other chunks of the same kv head write the same bytes)
@@ -224,9 +260,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
             valid = 0;
             phys = 0;
         }
-        const size_t base = ((size_t)phys * p.num_kv_heads + kvh) * kBlock * D;
-        const unsigned char *kg = reinterpret_cast<const unsigned char *>(kc + base);
-        const unsigned char *vg = reinterpret_cast<const unsigned char *>(vc + base);
+        const size_t base = ((size_t)phys * p.num_kv_heads + kvh) * kBlock * Sm::kRowBytes;
+        const unsigned char *kg = kc + base;
+        const unsigned char *vg = vc + base;
         unsigned char *ks = ring + st * Sm::kStage;
         unsigned char *vs = ks + Sm::kTile;
 #pragma unroll
@@ -246,37 +282,55 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
 
 #pragma unroll
-    for (int st = 0; st < kStages - 1; st++) {
+    for (int st = 0; st < Sm::kRing - 1; st++) {
         if (st < n) issue(st, st);
         pkv::cp_async_commit();
     }
 
     for (int i = 0; i < n; i++) {
         {
-            const int nx = i + kStages - 1;
-            if (nx < n) issue(nx, nx % kStages);
+            const int nx = i + Sm::kRing - 1;
+            if (nx < n) issue(nx, nx % Sm::kRing);
             pkv::cp_async_commit();
         }
-        pkv::cp_async_wait<kStages - 1>();
+        pkv::cp_async_wait<Sm::kRing - 1>();
         __syncwarp();
 
-        const int st = i % kStages;
+        const int st = i % Sm::kRing;
         const unsigned char *ks = ring + st * Sm::kStage;
         const unsigned char *vs = ks + Sm::kTile;
+
         int phys;
         int valid = block_rows(i, phys);
         if (valid < 0) valid = 0;
 
         // S = q . K^T for the block's 16 tokens (two n-tiles of 8 tokens)
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (kFp8) {
+            // tokens gid and gid + 8: their codes d = 32 tig .. 32 tig + 31
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid, 2 * tig, Sm::kRowBytes));
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid, 2 * tig + 1, Sm::kRowBytes));
+            const uint4 c0 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid + 8, 2 * tig, Sm::kRowBytes));
+            const uint4 c1 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid + 8, 2 * tig + 1, Sm::kRowBytes));
+            const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t wc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-        for (int kk = 0; kk < KSTEPS; kk++) {
-            uint32_t b0, b1, b2, b3;
-            const int tok = ((lane >> 4) << 3) + (lane & 7);
-            const int ch = kk * 2 + ((lane >> 3) & 1);
-            pkv::ldsm_x4(b0, b1, b2, b3, ks + pkv::swz(tok, ch, Sm::kRowBytes));
-            pkv::mma_bf16(s0, qa[kk], b0, b1);
-            pkv::mma_bf16(s1, qa[kk], b2, b3);
+            for (int kk = 0; kk < KSTEPS; kk++) {
+                pkv::mma_f16(s0, qa[kk], pkv::e4m3x2_to_f16x2((uint16_t)(wa[kk] & 0xffffu)),
+                             pkv::e4m3x2_to_f16x2((uint16_t)(wa[kk] >> 16)));
+                pkv::mma_f16(s1, qa[kk], pkv::e4m3x2_to_f16x2((uint16_t)(wc[kk] & 0xffffu)),
+                             pkv::e4m3x2_to_f16x2((uint16_t)(wc[kk] >> 16)));
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; kk++) {
+                uint32_t b0, b1, b2, b3;
+                const int tok = ((lane >> 4) << 3) + (lane & 7);
+                const int ch = kk * 2 + ((lane >> 3) & 1);
+                pkv::ldsm_x4(b0, b1, b2, b3, ks + pkv::swz(tok, ch, D * 2));
+                pkv::mma_bf16(s0, qa[kk], b0, b1);
+                pkv::mma_bf16(s1, qa[kk], b2, b3);
+            }
         }
         // scale to base-2 units and mask rows past the context
         const int t0 = tig * 2;
@@ -284,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
         const int tk[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
 #pragma unroll
         for (int e = 0; e < 8; e++) {
-            x[e] = tk[e & 3] < valid ? x[e] * p.scale_log2 : -INFINITY;
+            x[e] = tk[e & 3] < valid ? x[e] * sl2 : -INFINITY;
         }
         float mxA = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
         float mxB = fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]));
@@ -312,26 +366,55 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
             o[nt][2] *= alB;
             o[nt][3] *= alB;
         }
-        // P as two bf16 A fragments, hi + lo, so P keeps ~16 significant bits
-        float hi[8], lo[8];
+        if constexpr (kFp8) {
+            // P as one fp16 A fragment (11 significant bits; P <= 1)
+            const uint32_t ph[4] = {pkv::pack_f16(pr[0], pr[1]), pkv::pack_f16(pr[4], pr[5]),
+                                    pkv::pack_f16(pr[2], pr[3]), pkv::pack_f16(pr[6], pr[7])};
+            // O += P . V in the permuted column order: rows 2 tig, 2 tig + 1,
+            // 2 tig + 8, 2 tig + 9 (the fragment's token pairs), bytes
+            // 32 m + 4 gid .. + 3 of each
+            auto word = [&](int row, int m) {
+                const int cb = 32 * m + 4 * gid;
+                return *reinterpret_cast<const uint32_t *>(vs + pkv::swz(row, cb >> 4, Sm::kRowBytes) + (cb & 15));
+            };
 #pragma unroll
-        for (int e = 0; e < 8; e++) pkv::split_bf16(pr[e], hi[e], lo[e]);
-        const uint32_t ph[4] = {pkv::pack_bf16(hi[0], hi[1]), pkv::pack_bf16(hi[4], hi[5]),
-                                pkv::pack_bf16(hi[2], hi[3]), pkv::pack_bf16(hi[6], hi[7])};
-        const uint32_t pl[4] = {pkv::pack_bf16(lo[0], lo[1]), pkv::pack_bf16(lo[4], lo[5]),
-                                pkv::pack_bf16(lo[2], lo[3]), pkv::pack_bf16(lo[6], lo[7])};
-        // O += P . V
+            for (int m = 0; m < D / 32; m++) {
+                const uint32_t wa = word(2 * tig, m), wb = word(2 * tig + 1, m);
+                const uint32_t wc = word(2 * tig + 8, m), wd = word(2 * tig + 9, m);
+                // (token, token + 1) code pairs for columns j = 0 .. 3
+                const uint32_t p01 = __byte_perm(wa, wb, 0x5140), p23 = __byte_perm(wa, wb, 0x7362);
+                const uint32_t q01 = __byte_perm(wc, wd, 0x5140), q23 = __byte_perm(wc, wd, 0x7362);
+                pkv::mma_f16(o[4 * m], ph, pkv::e4m3x2_to_f16x2((uint16_t)(p01 & 0xffffu)),
+                             pkv::e4m3x2_to_f16x2((uint16_t)(q01 & 0xffffu)));
+                pkv::mma_f16(o[4 * m + 1], ph, pkv::e4m3x2_to_f16x2((uint16_t)(p01 >> 16)),
+                             pkv::e4m3x2_to_f16x2((uint16_t)(q01 >> 16)));
+                pkv::mma_f16(o[4 * m + 2], ph, pkv::e4m3x2_to_f16x2((uint16_t)(p23 & 0xffffu)),
+                             pkv::e4m3x2_to_f16x2((uint16_t)(q23 & 0xffffu)));
+                pkv::mma_f16(o[4 * m + 3], ph, pkv::e4m3x2_to_f16x2((uint16_t)(p23 >> 16)),
+                             pkv::e4m3x2_to_f16x2((uint16_t)(q23 >> 16)));
+            }
+        } else {
+            // P as two bf16 A fragments, hi + lo, so P keeps ~16 significant bits
+            float hi[8], lo[8];
 #pragma unroll
-        for (int nn = 0; nn < D / 16; nn++) {
-            uint32_t v0, v1, v2, v3;
-            const int j = lane >> 3;
-            const int tok = ((j & 1) << 3) + (lane & 7);
-            const int ch = nn * 2 + (j >> 1);
-            pkv::ldsm_x4_t(v0, v1, v2, v3, vs + pkv::swz(tok, ch, Sm::kRowBytes));
-            pkv::mma_bf16(o[2 * nn], ph, v0, v1);
-            pkv::mma_bf16(o[2 * nn], pl, v0, v1);
-            pkv::mma_bf16(o[2 * nn + 1], ph, v2, v3);
-            pkv::mma_bf16(o[2 * nn + 1], pl, v2, v3);
+            for (int e = 0; e < 8; e++) pkv::split_bf16(pr[e], hi[e], lo[e]);
+            const uint32_t ph[4] = {pkv::pack_bf16(hi[0], hi[1]), pkv::pack_bf16(hi[4], hi[5]),
+                                    pkv::pack_bf16(hi[2], hi[3]), pkv::pack_bf16(hi[6], hi[7])};
+            const uint32_t pl[4] = {pkv::pack_bf16(lo[0], lo[1]), pkv::pack_bf16(lo[4], lo[5]),
+                                    pkv::pack_bf16(lo[2], lo[3]), pkv::pack_bf16(lo[6], lo[7])};
+            // O += P . V
+#pragma unroll
+            for (int nn = 0; nn < D / 16; nn++) {
+                uint32_t v0, v1, v2, v3;
+                const int j = lane >> 3;
+                const int tok = ((j & 1) << 3) + (lane & 7);
+                const int ch = nn * 2 + (j >> 1);
+                pkv::ldsm_x4_t(v0, v1, v2, v3, vs + pkv::swz(tok, ch, D * 2));
+                pkv::mma_bf16(o[2 * nn], ph, v0, v1);
+                pkv::mma_bf16(o[2 * nn], pl, v0, v1);
+                pkv::mma_bf16(o[2 * nn + 1], ph, v2, v3);
+                pkv::mma_bf16(o[2 * nn + 1], pl, v2, v3);
+            }
         }
         __syncwarp();
     }
@@ -342,6 +425,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
     lB += __shfl_xor_sync(0xffffffffu, lB, 2);
 
     pkv::cp_async_wait<0>();
+    // The accumulator as pairs of adjacent output columns: slot k holds, for
+    // row gid (hi = 0) or gid + 8 (hi = 1), the values of columns col and
+    // col + 1 (fp8: in the permuted order of the value product, undone here).
+    auto out_pair = [&](int k, int hi, float &x0, float &x1) -> int {
+        if constexpr (kFp8) {
+            const int m = k >> 2, e = (k >> 1) & 1, j = (k & 1) * 2;
+            x0 = o[4 * m + j][2 * hi + e];
+            x1 = o[4 * m + j + 1][2 * hi + e];
+            return 32 * m + 8 * tig + 4 * e + j;
+        } else {
+            x0 = o[k][2 * hi];
+            x1 = o[k][2 * hi + 1];
+            return k * 8 + tig * 2;
+        }
+    };
     if (kHeadWarps) {
         // the warp holds its rows' whole state for this partition
         const size_t orow = (size_t)s * p.num_q_heads + h0 + gid;
@@ -349,20 +447,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
         if (nslots == 1) {
             OutT *oa = static_cast<OutT *>(p.out) + orow * D;
             OutT *ob = oa + 8 * D;
-            const float ia = lA > 0.f ? 1.f / lA : 0.f, ib = lB > 0.f ? 1.f / lB : 0.f;
+            const float ia = lA > 0.f ? vsc / lA : 0.f, ib = lB > 0.f ? vsc / lB : 0.f;
 #pragma unroll
-            for (int nt = 0; nt < NT; nt++) {
-                const int col = nt * 8 + tig * 2;
-                if (okA) pkv::store2(oa + col, o[nt][0] * ia, o[nt][1] * ia);
-                if (okB) pkv::store2(ob + col, o[nt][2] * ib, o[nt][3] * ib);
+            for (int k = 0; k < NT; k++) {
+                float x0, x1, y0, y1;
+                const int col = out_pair(k, 0, x0, x1);
+                out_pair(k, 1, y0, y1);
+                if (okA) pkv::store2(oa + col, x0 * ia, x1 * ia);
+                if (okB) pkv::store2(ob + col, y0 * ib, y1 * ib);
             }
         } else {
             const size_t pa = orow * p.max_parts + slot0 + part, pb = pa + 8 * (size_t)p.max_parts;
 #pragma unroll
-            for (int nt = 0; nt < NT; nt++) {
-                const int col = nt * 8 + tig * 2;
-                if (okA) *reinterpret_cast<float2 *>(p.part_o + pa * D + col) = make_float2(o[nt][0], o[nt][1]);
-                if (okB) *reinterpret_cast<float2 *>(p.part_o + pb * D + col) = make_float2(o[nt][2], o[nt][3]);
+            for (int k = 0; k < NT; k++) {
+                float x0, x1, y0, y1;
+                const int col = out_pair(k, 0, x0, x1);
+                out_pair(k, 1, y0, y1);
+                if (okA) *reinterpret_cast<float2 *>(p.part_o + pa * D + col) = make_float2(x0 * vsc, x1 * vsc);
+                if (okB) *reinterpret_cast<float2 *>(p.part_o + pb * D + col) = make_float2(y0 * vsc, y1 * vsc);
             }
             if (tig == 0 && okA) *reinterpret_cast<float2 *>(p.part_ml + pa * 2) = make_float2(mA, lA);
             if (tig == 0 && okB) *reinterpret_cast<float2 *>(p.part_ml + pb * 2) = make_float2(mB, lB);
@@ -382,11 +484,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
         ll[gid + 8] = lB;
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; nt++) {
-        const int col = nt * 8 + tig * 2;
-        *reinterpret_cast<float2 *>(mw + gid * Sm::kMergeStride + col) = make_float2(o[nt][0], o[nt][1]);
-        *reinterpret_cast<float2 *>(mw + (gid + 8) * Sm::kMergeStride + col) =
-            make_float2(o[nt][2], o[nt][3]);
+    for (int k = 0; k < NT; k++) {
+        float x0, x1, y0, y1;
+        const int col = out_pair(k, 0, x0, x1);
+        out_pair(k, 1, y0, y1);
+        *reinterpret_cast<float2 *>(mw + gid * Sm::kMergeStride + col) = make_float2(x0, x1);
+        *reinterpret_cast<float2 *>(mw + (gid + 8) * Sm::kMergeStride + col) = make_float2(y0, y1);
     }
     __syncthreads();
 
@@ -408,10 +511,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
         }
         const size_t orow = (size_t)s * p.num_q_heads + h0 + r;
         if (nslots == 1) {
-            pkv::store1(static_cast<OutT *>(p.out) + orow * D + c, lsum > 0.f ? acc / lsum : 0.f);
+            pkv::store1(static_cast<OutT *>(p.out) + orow * D + c, lsum > 0.f ? acc * vsc / lsum : 0.f);
         } else {
             const size_t prow = orow * p.max_parts + slot0 + part;
-            p.part_o[prow * D + c] = acc;
+            p.part_o[prow * D + c] = acc * vsc;
             if (c == 0) {
                 p.part_ml[prow * 2] = M;
                 p.part_ml[prow * 2 + 1] = lsum;
@@ -676,15 +779,19 @@ bool use_head_warps(int num_seqs, int units, int own_max, int partition) {
     return (long long)num_seqs * ((units + kWarps - 1) / kWarps) * parts >= 2LL * device_sms();
 }
 
-template <int D, typename OutT, bool kHeadWarps>
+template <int D, typename OutT, bool kHeadWarps, bool kFp8>
 int launch_bf16_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
-    constexpr int bytes = DecodeSmem<D>::kBytes;
+    constexpr int bytes = DecodeSmem<D, kFp8>::kBytes;
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        // two thread blocks per SM: the largest shared-memory carve-out
+        if (cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps, kFp8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+            cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps, kFp8>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return pkv::check_launch("decode: set shared memory size");
         attr_set[dev] = true;
     }
@@ -693,15 +800,15 @@ int launch_bf16_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
     dim3 grid((unsigned)(kHeadWarps ? (units + kWarps - 1) / kWarps : units), (unsigned)num_seqs,
               (unsigned)(p.max_parts - (p.prefix_len ? 1 : 0)));
     cudaError_t e =
-        pkv::launch_dependent(decode_bf16_kernel<D, OutT, kHeadWarps>, grid, dim3(kThreads), bytes, st, p);
+        pkv::launch_dependent(decode_bf16_kernel<D, OutT, kHeadWarps, kFp8>, grid, dim3(kThreads), bytes, st, p);
     if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "decode_bf16: %s", cudaGetErrorString(e));
     return pkv::check_launch("decode_bf16");
 }
 
-template <int D, typename OutT>
+template <int D, typename OutT, bool kFp8 = false>
 int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
-    return p.head_warps ? launch_bf16_variant<D, OutT, true>(p, num_seqs, st)
-                        : launch_bf16_variant<D, OutT, false>(p, num_seqs, st);
+    return p.head_warps ? launch_bf16_variant<D, OutT, true, kFp8>(p, num_seqs, st)
+                        : launch_bf16_variant<D, OutT, false, kFp8>(p, num_seqs, st);
 }
 
 template <typename T, typename OutT>
@@ -716,6 +823,8 @@ int launch_decode(const DecodeParams &p, int num_seqs, int D, int dtype, cudaStr
     int rc;
     if (dtype == PKV_BF16) {
         rc = D == 128 ? launch_bf16<128, OutT>(p, num_seqs, st) : launch_bf16<64, OutT>(p, num_seqs, st);
+    } else if (dtype == PKV_FP8_E4M3) {
+        rc = launch_bf16<128, OutT, true>(p, num_seqs, st);
     } else {
         rc = launch_core<float, OutT>(p, num_seqs, D, st);
     }
@@ -762,14 +871,21 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
                 const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                 int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
                 int max_context_len, int partition_size, float scale, void *out, int dtype, int out_dtype,
-                void *workspace, size_t workspace_bytes, void *stream) {
+                void *workspace, size_t workspace_bytes, void *stream, const float *k_scale = nullptr,
+                const float *v_scale = nullptr) {
     int part;
     int rc = resolve_partition(partition_size, &part);
     if (rc) return rc;
     if (block_size != kBlock) return pkv::fail(PKV_ERR_INVALID, "block_size must be 16 (got %d)", block_size);
     if (head_dim != 64 && head_dim != 128)
         return pkv::fail(PKV_ERR_INVALID, "head_dim must be 64 or 128 (got %d)", head_dim);
-    if (dtype != PKV_F32 && dtype != PKV_BF16) return pkv::fail(PKV_ERR_INVALID, "bad dtype %d", dtype);
+    if (dtype != PKV_F32 && dtype != PKV_BF16 && dtype != PKV_FP8_E4M3)
+        return pkv::fail(PKV_ERR_INVALID, "bad dtype %d", dtype);
+    if (dtype == PKV_FP8_E4M3) {  // bf16 queries over an fp8 cache
+        if (head_dim != 128) return pkv::fail(PKV_ERR_INVALID, "fp8 decode: head_dim must be 128");
+        if (!k_scale || !v_scale) return pkv::fail(PKV_ERR_INVALID, "fp8 decode: null scales");
+        if (k_new || v_new) return pkv::fail(PKV_ERR_INVALID, "fp8 decode: no fused append");
+    }
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return pkv::fail(PKV_ERR_INVALID, "bad out_dtype %d", out_dtype);
     if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0)
@@ -809,6 +925,8 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
     p.k_new = k_new;
     p.v_new = v_new;
     p.head_warps = use_head_warps(num_seqs, num_kv_heads * p.head_chunks, p.len_cap, part);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     if ((k_new || v_new) && (!k_new || !v_new || !pkv::aligned16(k_new) || !pkv::aligned16(v_new)))
         return pkv::fail(PKV_ERR_INVALID, "decode_step: k_new and v_new must both be 16-byte aligned device pointers");
 
@@ -842,6 +960,20 @@ extern "C" int pkv_paged_attention_decode(const void *q, const void *k_cache, co
     return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len,
                        partition_size, scale, out, dtype, out_dtype, workspace, workspace_bytes, stream);
+}
+
+extern "C" int pkv_paged_attention_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                              const float *k_scale, const float *v_scale,
+                                              const int32_t *block_tables, int max_blocks_per_seq,
+                                              const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                              int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                              int max_context_len, int partition_size, float scale, void *out,
+                                              int out_dtype, void *workspace, size_t workspace_bytes,
+                                              void *stream) {
+    return decode_impl(q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len,
+                       partition_size, scale, out, PKV_FP8_E4M3, out_dtype, workspace, workspace_bytes, stream,
+                       k_scale, v_scale);
 }
 
 extern "C" int pkv_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,

@@ -109,6 +109,9 @@ class Batch:
     prefill_cu_q_lens: Optional[torch.Tensor] = None    # [P+1] int32
     prefill_block_tables: Optional[torch.Tensor] = None  # [P, max_blocks] int32
     prefill_context_lens: Optional[torch.Tensor] = None  # [P] int32
+    # fp8 E4M3 caches (k_cache / v_cache are uint8 codes): per kv head scales
+    k_scale: Optional[torch.Tensor] = None               # [Hkv] float32
+    v_scale: Optional[torch.Tensor] = None
     meta: dict = field(default_factory=dict)
 
     @property
@@ -470,3 +473,29 @@ def custom_prefill(dtype: str, num_q_heads: int, num_kv_heads: int, head_dim: in
         prefill_block_tables=_tables(prow, width),
         prefill_context_lens=torch.from_numpy(plens.astype(np.int32)),
         meta={"pool_need": need})
+
+
+def fp8_batch(base: Batch, seed: int = 97) -> Batch:
+    """The same step over fp8 E4M3 caches: random codes in place of the cache
+    values (drawn directly as codes: random sign, exponent field uniform in
+    [4, 10], mantissa uniform, so magnitudes 2^-3 .. 2^4 before scaling),
+    the NaN code (0x7F) in every row the base batch poisons, and per kv head
+    scales 2^-4 (1 + g/8) for K and 2^-3 (1 + g/16) for V.  Queries and the
+    new tokens stay bf16 (the append quantises them)."""
+    g = torch.Generator().manual_seed(seed)
+    NB, H, bs, d = base.k_cache.shape
+
+    def codes(src):
+        sign = torch.randint(0, 2, src.shape, generator=g, dtype=torch.int32) << 7
+        ex = torch.randint(4, 11, src.shape, generator=g, dtype=torch.int32) << 3
+        man = torch.randint(0, 8, src.shape, generator=g, dtype=torch.int32)
+        c = (sign | ex | man).to(torch.uint8)
+        c[src.isnan()] = 0x7F
+        return c
+
+    out = Batch(**{f.name: getattr(base, f.name) for f in base.__dataclass_fields__.values()})
+    out.k_cache, out.v_cache = codes(base.k_cache), codes(base.v_cache)
+    out.k_scale = 2.0 ** -4 * (1 + torch.arange(H, dtype=torch.float32) / 8)
+    out.v_scale = 2.0 ** -3 * (1 + torch.arange(H, dtype=torch.float32) / 16)
+    out.meta = dict(base.meta, fp8=True)
+    return out
