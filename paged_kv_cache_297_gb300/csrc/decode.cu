@@ -115,7 +115,7 @@ template <int D, bool kFp8 = false>
 struct DecodeSmem {
     // ring depth in blocks: an fp8 block is half the bytes, so twice the
     // blocks keep as many bytes in flight (what an HBM-bound warp needs)
-    static constexpr int kRing = kFp8 ? 2 * kStages : kStages;
+    static constexpr int kRing = kFp8 ? 4 : kStages;
     static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);   // one cached row
     static constexpr int kTile = kBlock * kRowBytes;      // one block of one kv head
     static constexpr int kStage = 2 * kTile;               // K + V
@@ -142,7 +142,7 @@ struct DecodeSmem {
 //    of a token row serves four n-tiles, and two rows' words, byte-permuted,
 //    give the (token, token + 1) pairs of the B fragments.
 template <int D, typename OutT, bool kHeadWarps, bool kFp8 = false>
-__global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(const DecodeParams p) {
     using Sm = DecodeSmem<D, kFp8>;
     constexpr int CH = Sm::kRowBytes / 16;    // 16-byte chunks per cached row
     constexpr int PER_LANE = kBlock * CH / 32;
