@@ -282,6 +282,8 @@ class Step:
 
 
 DECODE_SOURCES = ("common.cuh", "decode.cu")
+# the shared-prefix call also runs the tcgen05 kernel on the prefix
+CASCADE_SOURCES = DECODE_SOURCES + ("prefill_common.cuh", "prefill_tc.cu", "tcgen05.cuh")
 
 
 def time_device(step: Step, steps: int, warmup: int, world: int):
@@ -468,7 +470,7 @@ def run_ours(args):
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
     kname = ("decode_shared_prefix" if step.cascade else "decode_step" if step.fused
              else "paged_attention_decode_fp8" if step.fp8 else "paged_attention_decode")
-    traffic = recorded_traffic(kname, args.workload, DECODE_SOURCES)
+    traffic = recorded_traffic(kname, args.workload, CASCADE_SOURCES if step.cascade else DECODE_SOURCES)
     roofline = {"kernel": ("decode_shared_prefix (fused append; shared-prefix tile on the tensor cores, "
                            "partition kernel over each sequence's own tokens, log-sum-exp merge; bytes "
                            "count the prefix once)" if step.cascade else
