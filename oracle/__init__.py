@@ -57,6 +57,8 @@ def _load():
         lib.oracle_e4m3_decode.restype = ctypes.c_double
         lib.oracle_kv_append_fp8.argtypes = [P, P, I, P, I, P, P, I, I, I, I, P, P]
         lib.oracle_threads.restype = I
+        lib.oracle_set_threads.argtypes = [I]
+        lib.oracle_set_threads.restype = None
         _lib = lib
     return _lib
 
@@ -73,6 +75,11 @@ def _ptr(t: torch.Tensor | None):
 
 def threads() -> int:
     return _load().oracle_threads()
+
+
+def set_threads(n: int) -> None:
+    """Threads for later calls (OpenMP)."""
+    _load().oracle_set_threads(int(n))
 
 
 def kv_append(k, v, slot_mapping, k_cache, v_cache) -> None:

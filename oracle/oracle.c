@@ -114,6 +114,15 @@ int oracle_threads(void) {
 #endif
 }
 
+/* Threads for the parallel loops that follow (n >= 1). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Write new tokens' K and V rows into their slots; slot < 0 is skipped. */
 int oracle_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int num_tokens,
                      void *k_cache, void *v_cache, int num_blocks, int num_kv_heads,

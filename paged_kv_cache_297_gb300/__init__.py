@@ -168,11 +168,27 @@ def kv_append(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
         _dt(k_cache), _stream(stream)))
 
 
-def copy_blocks(src_dst_pairs, k_cache, v_cache, stream=None) -> None:
-    """Copy-on-write: block dst of both caches becomes a copy of block src."""
+def check_copy_pairs(src_dst_pairs) -> None:
+    """The copy_blocks caller contract, checked on a host copy: destinations
+    distinct and none of them a source of the same call (the blocks of one
+    call are copied concurrently)."""
+    p = src_dst_pairs.detach().to("cpu", torch.int64).view(-1, 2)
+    dst = p[:, 1].tolist()
+    if len(set(dst)) != len(dst):
+        raise ValueError("copy_blocks: a destination block appears twice")
+    if set(dst) & set(p[:, 0].tolist()):
+        raise ValueError("copy_blocks: a destination block is also a source")
+
+
+def copy_blocks(src_dst_pairs, k_cache, v_cache, stream=None, check: Optional[bool] = None) -> None:
+    """Copy-on-write: block dst of both caches becomes a copy of block src.
+    ``check`` (default: the PKV_CHECK_PAIRS environment variable) validates
+    the caller contract on a host copy first (a device-to-host copy)."""
     NB, H, bs, d = _cache_dims(k_cache, v_cache)
     if src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
         raise ValueError("src_dst_pairs must be [n, 2]")
+    if check if check is not None else os.environ.get("PKV_CHECK_PAIRS", "") not in ("", "0"):
+        check_copy_pairs(src_dst_pairs)
     _check(load().pkv_copy_blocks(
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(src_dst_pairs, "src_dst_pairs", torch.int64), int(src_dst_pairs.shape[0]), NB, H, d,

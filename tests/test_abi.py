@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import paged_kv_cache_297_gb300 as pkv
 from paged_kv_cache_297_gb300 import build as pkv_build
@@ -133,3 +134,11 @@ def test_zero_sized_calls_launch_nothing(lib):
     assert lib.pkv_paged_attention_decode(None, None, None, None, 0, None, 0, 32, 8, 128, 16, 0, 0,
                                           0, ctypes.c_float(1.0), None, pkv.BF16, pkv.F32, None, 0,
                                           None) == 0
+
+
+def test_copy_pair_contract_check_on_the_host():
+    pkv.check_copy_pairs(torch.tensor([[1, 5], [2, 6], [1, 7]]))
+    with pytest.raises(ValueError):
+        pkv.check_copy_pairs(torch.tensor([[1, 5], [2, 5]]))   # duplicate destination
+    with pytest.raises(ValueError):
+        pkv.check_copy_pairs(torch.tensor([[1, 5], [5, 6]]))   # destination also a source

@@ -273,6 +273,29 @@ def test_block_relabelling_is_bitwise_invariant_on_gpu():
     assert torch.equal(out_a.cpu(), out_b.cpu())
 
 
+def test_append_to_another_slot_is_bitwise_invariant_on_gpu():
+    # each sequence's last block moves to a spare block before the step: its
+    # rows are copied there (copy_blocks), the table points at the copy and
+    # the new token is appended into the copy; the output must not change
+    b = W.make_batch("llama3_8b_decode", num_seqs=16)
+    _, _, out_a, _ = gpu_step(b)
+    S = b.num_seqs
+    L = b.context_lens.long()
+    last = (L - 1) // 16
+    old = b.block_tables.long().gather(1, last.unsqueeze(1)).squeeze(1)
+    used = set(b.block_tables[b.block_tables >= 0].tolist())
+    spare = torch.tensor([x for x in range(b.num_blocks) if x not in used][:S], dtype=torch.int64)
+    assert spare.numel() == S
+    b.copy_pairs = torch.stack([old, spare], dim=1)
+    bt = b.block_tables.clone()
+    bt[torch.arange(S), last] = spare.to(torch.int32)
+    b.block_tables = bt
+    b.slot_mapping = spare * 16 + (L - 1) % 16
+    _, _, out_b, _ = gpu_step(b)
+    assert pkv.get_status() == 0
+    assert torch.equal(out_a.cpu(), out_b.cpu())
+
+
 def test_shared_prefix_equals_private_copies_on_gpu():
     b = W.make_batch("shared_prefix_cow", num_seqs=32)
     _, _, shared, _ = gpu_step(b)

@@ -181,6 +181,28 @@ def test_block_relabelling_is_bitwise_invariant():
     assert torch.equal(a, b)
 
 
+def test_append_to_another_slot_is_bitwise_invariant():
+    """The new token written into a copy of the last block (table updated)
+    gives the same output as writing it in place."""
+    g = torch.Generator().manual_seed(13)
+    Hkv, d, NB = 2, 8, 10
+    kc = torch.randn(NB, Hkv, BS, d, generator=g)
+    vc = torch.randn(NB, Hkv, BS, d, generator=g)
+    k = torch.randn(1, Hkv, d, generator=g)
+    v = torch.randn(1, Hkv, d, generator=g)
+    q = torch.randn(1, 4, d, generator=g)
+    bt = torch.tensor([[2, 6, 4]], dtype=torch.int32)
+    cl = torch.tensor([40], dtype=torch.int32)               # token 39: block 4, row 7
+    kc_a, vc_a = kc.clone(), vc.clone()
+    oracle.kv_append(k, v, torch.tensor([4 * BS + 7]), kc_a, vc_a)
+    a = oracle.decode(q, kc_a, vc_a, bt, cl, 0.3)
+    kc_b, vc_b = kc.clone(), vc.clone()
+    oracle.copy_blocks(kc_b, vc_b, torch.tensor([[4, 9]]))
+    oracle.kv_append(k, v, torch.tensor([9 * BS + 7]), kc_b, vc_b)
+    b = oracle.decode(q, kc_b, vc_b, torch.tensor([[2, 6, 9]], dtype=torch.int32), cl, 0.3)
+    assert torch.equal(a, b)
+
+
 def test_shared_prefix_equals_private_copies():
     g = torch.Generator().manual_seed(9)
     Hkv, d, NB = 2, 8, 12
