@@ -449,12 +449,18 @@ def cpu_baseline(batch: W.Batch, budget_s: float = 12.0):
             "single_thread": one}
 
 
+# Arm "CPU part" codes of the server cores this may run on
+ARM_PARTS = {"0xd0c": "Neoverse N1", "0xd40": "Neoverse V1", "0xd49": "Neoverse N2", "0xd4f": "Neoverse V2",
+             "0xd83": "Neoverse V3", "0xd84": "Neoverse V3AE", "0xd8e": "Neoverse N3"}
+
+
 def cpu_model() -> str:
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
                 if line.lower().startswith(("model name", "cpu part", "hardware")):
-                    return line.split(":", 1)[1].strip()
+                    v = line.split(":", 1)[1].strip()
+                    return f"Arm {ARM_PARTS[v]} ({v})" if v in ARM_PARTS else v
     except OSError:
         pass
     import platform
