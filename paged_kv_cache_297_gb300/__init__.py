@@ -11,9 +11,15 @@ Calls (names follow the C ABI without the ``pkv_`` prefix):
   copy_blocks(src_dst_pairs, k_cache, v_cache)
   paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out)
   decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out)
+  decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                       prefix_len)
   paged_attention_prefill_chunk(q, cu_q_lens, k_cache, v_cache, block_tables,
                                 context_lens, scale, out)
+  kv_append_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale)
+  paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                             context_lens, scale, out)
   get_status()
+  BlockManager(num_blocks, max_blocks_per_seq)   (host block allocator, pkv_bm_*)
 """
 
 from __future__ import annotations
@@ -29,7 +35,8 @@ __all__ = [
     "copy_blocks", "decode_workspace_bytes", "decode_partition_size", "paged_attention_decode",
     "decode_step", "decode_shared_prefix_workspace_bytes", "decode_shared_prefix",
     "prefill_workspace_bytes", "paged_attention_prefill_chunk", "get_status", "STATUS_BITS",
-    "EXPORTED",
+    "EXPORTED", "kv_append_fp8", "paged_attention_decode_fp8", "check_copy_pairs", "BlockManager",
+    "FP8_E4M3",
 ]
 
 BLOCK_SIZE = 16
@@ -133,7 +140,7 @@ def _dt(t: torch.Tensor) -> int:
 
 
 def _dev(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None) -> int:
-    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -142,8 +149,15 @@ def _dev(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None) -> int
     return t.data_ptr()
 
 
+# the current stream's handle without building a Stream object (a few
+# microseconds less host time per call)
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        if _RAW_STREAM is not None:
+            return _RAW_STREAM(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -228,9 +242,9 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
     mb = int(block_tables.shape[1])
     if max_context_len is None:
         max_context_len = mb * bs
-    need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().pkv_paged_attention_decode(
@@ -275,9 +289,9 @@ def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     mb = int(block_tables.shape[1])
     if max_context_len is None:
         max_context_len = mb * bs
-    need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().pkv_paged_attention_decode_fp8(
@@ -306,9 +320,9 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, s
     mb = int(block_tables.shape[1])
     if max_context_len is None:
         max_context_len = mb * bs
-    need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().pkv_decode_step(
@@ -352,8 +366,8 @@ def decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale,
     mb = int(block_tables.shape[1])
     if max_context_len is None:
         max_context_len = mb * bs
-    need = decode_shared_prefix_workspace_bytes(S, Hq, d, max_context_len, prefix_len, partition_size)
-    if workspace is None:
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        need = decode_shared_prefix_workspace_bytes(S, Hq, d, max_context_len, prefix_len, partition_size)
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(load().pkv_paged_attention_decode_shared_prefix(
         _dev(q, "q"), None if k_new is None else _dev(k_new, "k_new"),
@@ -393,9 +407,9 @@ def paged_attention_prefill_chunk(q, cu_q_lens, k_cache, v_cache, block_tables, 
         max_q_len = total_q
     if max_context_len is None:
         max_context_len = mb * bs
-    need = prefill_workspace_bytes(S, total_q, Hq, Hkv, d, max_q_len, max_context_len)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        need = prefill_workspace_bytes(S, total_q, Hq, Hkv, d, max_q_len, max_context_len)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().pkv_paged_attention_prefill_chunk(
