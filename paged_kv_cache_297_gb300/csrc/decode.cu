@@ -14,6 +14,7 @@
 //   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p 2^(m_p - M) O_p / L.
 // Logits are kept in base-2 units (scale * log2 e folded into one multiply).
 #include <math.h>
+#include <type_traits>
 
 #include "common.cuh"
 #include "prefill_common.cuh"
@@ -113,8 +114,10 @@ __device__ __forceinline__ int clamp_len(int L, int cap, unsigned *status, bool 
 
 template <int D, bool kFp8 = false>
 struct DecodeSmem {
-    // ring depth in blocks: an fp8 block is half the bytes, so twice the
-    // blocks keep as many bytes in flight (what an HBM-bound warp needs)
+    // ring depth in blocks: an fp8 block is half the bytes, and the fp8
+    // kernel runs three thread blocks per SM, so 4 stages of 4 KB per warp
+    // keep the bf16 kernel's bytes in flight per SM (2 blocks x 4 warps x
+    // 3 stages x 8 KB = 192 KB), which is what an HBM-bound SM needs
     static constexpr int kRing = kFp8 ? 4 : kStages;
     static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);   // one cached row
     static constexpr int kTile = kBlock * kRowBytes;      // one block of one kv head
@@ -652,63 +655,103 @@ __global__ void __launch_bounds__(kThreads) decode_cuda_core_kernel(const Decode
 // log-sum-exp merge of the partitions of each (sequence, q head)
 // ----------------------------------------------------------------------------
 
-// One warp per (sequence, q head); each lane owns D/32 output columns.  The
-// partition weights 2^(m_p - M) are computed lane-parallel and broadcast by
-// shuffles, and four partitions' loads are kept in flight.
+// One warp per (sequence, q head); each lane owns D/32 output columns.
+// Rows of at most kEager partitions (the common case) issue every load at
+// once: the slots' addresses do not depend on the length, so the length, the
+// first kEager slots' (m, l) and this lane's columns of their O rows travel
+// in one round trip, and the slots past the row's count are dropped
+// afterwards.  Longer rows compute the weights 2^(m_p - M) lane-parallel,
+// broadcast them by shuffles and keep four partitions' loads in flight.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p, int rows) {
     constexpr int VEC = D / 32;
+    constexpr int kEager = 4;
+    using VecT = typename std::conditional<VEC == 4, float4, float2>::type;
     pkv::grid_dependency_wait();  // the partials of the partition launch
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int s = row / p.num_q_heads;
-    const int L = clamp_len(p.context_lens[s], p.len_cap, p.status, false);
-    const int nparts = (p.prefix_len ? 1 : 0) + own_parts(p, L);  // partial slots of this row
-    if (nparts <= 1) return;
     const size_t prow = (size_t)row * p.max_parts;
     const float *ml = p.part_ml + prow * 2;
-    float M = -INFINITY;
-    for (int q = lane; q < nparts; q += 32) M = fmaxf(M, ml[2 * q]);
+    const float *po = p.part_o + prow * D + lane * VEC;
+
+    const int Lraw = p.context_lens[s];
+    const int eager = min(kEager, p.max_parts);  // slots inside this row's workspace
+    float2 mle[kEager];
+    float xe[kEager][VEC];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int u = 0; u < kEager; u++) {
+        if (u < eager) {
+            mle[u] = *reinterpret_cast<const float2 *>(ml + 2 * u);
+            const VecT w = *reinterpret_cast<const VecT *>(po + (size_t)u * D);
+            const float *wf = reinterpret_cast<const float *>(&w);
+#pragma unroll
+            for (int v = 0; v < VEC; v++) xe[u][v] = wf[v];
+        }
+    }
+    const int L = clamp_len(Lraw, p.len_cap, p.status, false);
+    const int nparts = (p.prefix_len ? 1 : 0) + own_parts(p, L);  // partial slots of this row
+    if (nparts <= 1) return;
+
     float acc[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; v++) acc[v] = 0.f;
     float lsum = 0.f;
-    if (M != -INFINITY) {
-        const float *po = p.part_o + prow * D + lane * VEC;
-        for (int q0 = 0; q0 < nparts; q0 += 32) {
-            const int cnt = min(32, nparts - q0);
-            float w = 0.f;
-            if (lane < cnt) {
-                w = pkv::fast_exp2(ml[2 * (q0 + lane)] - M);
-                lsum += ml[2 * (q0 + lane) + 1] * w;
-            }
-            int j = 0;
-            for (; j + 4 <= cnt; j += 4) {
-                float x[4][VEC];
+    if (nparts <= kEager) {
+        float M = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
+        for (int u = 0; u < kEager; u++)
+            if (u < nparts) M = fmaxf(M, mle[u].x);
+        if (M != -INFINITY) {
 #pragma unroll
-                    for (int v = 0; v < VEC; v++) x[u][v] = po[(size_t)(q0 + j + u) * D + v];
+            for (int u = 0; u < kEager; u++) {
+                if (u < nparts) {
+                    const float w = pkv::fast_exp2(mle[u].x - M);
+                    lsum += mle[u].y * w;
+#pragma unroll
+                    for (int v = 0; v < VEC; v++) acc[v] = fmaf(w, xe[u][v], acc[v]);
                 }
-#pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    const float wj = __shfl_sync(0xffffffffu, w, j + u);
-#pragma unroll
-                    for (int v = 0; v < VEC; v++) acc[v] = fmaf(wj, x[u][v], acc[v]);
-                }
-            }
-            for (; j < cnt; j++) {
-                const float wj = __shfl_sync(0xffffffffu, w, j);
-#pragma unroll
-                for (int v = 0; v < VEC; v++) acc[v] = fmaf(wj, po[(size_t)(q0 + j) * D + v], acc[v]);
             }
         }
-    }
+    } else {
+        float M = -INFINITY;
+        for (int q = lane; q < nparts; q += 32) M = fmaxf(M, ml[2 * q]);
 #pragma unroll
-    for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (M != -INFINITY) {
+            for (int q0 = 0; q0 < nparts; q0 += 32) {
+                const int cnt = min(32, nparts - q0);
+                float w = 0.f;
+                if (lane < cnt) {
+                    w = pkv::fast_exp2(ml[2 * (q0 + lane)] - M);
+                    lsum += ml[2 * (q0 + lane) + 1] * w;
+                }
+                int j = 0;
+                for (; j + 4 <= cnt; j += 4) {
+                    float x[4][VEC];
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+#pragma unroll
+                        for (int v = 0; v < VEC; v++) x[u][v] = po[(size_t)(q0 + j + u) * D + v];
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        const float wj = __shfl_sync(0xffffffffu, w, j + u);
+#pragma unroll
+                        for (int v = 0; v < VEC; v++) acc[v] = fmaf(wj, x[u][v], acc[v]);
+                    }
+                }
+                for (; j < cnt; j++) {
+                    const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+                    for (int v = 0; v < VEC; v++) acc[v] = fmaf(wj, po[(size_t)(q0 + j) * D + v], acc[v]);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     OutT *o = static_cast<OutT *>(p.out) + (size_t)row * D + lane * VEC;
 #pragma unroll
