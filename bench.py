@@ -324,8 +324,11 @@ def time_device(step: Step, steps: int, warmup: int, world: int):
     per_call = {}
     for j, (name, _) in enumerate(calls):
         per_call[name] = sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
-    serial_ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)) / steps
-    return span_ms, serial_ms, per_call, wall
+    step_ms = sorted(ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps))
+    serial_ms = sum(step_ms) / steps
+    # spread of the serialised step times (nearest-rank percentiles)
+    pct = {f"p{q}": round(step_ms[min(steps - 1, (q * steps) // 100)], 5) for q in (10, 50, 90)}
+    return span_ms, serial_ms, per_call, wall, pct
 
 
 def _pack(tensors, device):
@@ -507,7 +510,7 @@ def run_ours(args):
 
     clocks = ClockSampler(local)
     clocks.start()
-    span_ms, serial_ms, per_call, wall = time_device(step, args.steps, args.warmup, world)
+    span_ms, serial_ms, per_call, wall, step_pct = time_device(step, args.steps, args.warmup, world)
     clk = clocks.stop()
     span_ms = max_over_ranks(span_ms, world, dev)
     e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, world)
@@ -577,6 +580,7 @@ def run_ours(args):
         "kv_gbs": round(db["kv"] / (dec_ms / 1e3) / 1e9, 1),
         "calls_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
         "serial_ms_per_step": round(serial_ms, 5),
+        "serial_step_ms_pct": step_pct,
         "roofline": roofline,
         "e2e": {"value": round(world * seqs_per_step * args.steps / (e2e_ms / 1e3), 1),
                 "unit": "seq-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
