@@ -8,7 +8,7 @@ import torch
 import oracle
 import paged_kv_cache_297_gb300 as pkv
 
-# the benchmark spec tolerances: fp32 max abs 1e-4; bf16 (fp32 accumulation) max abs
+# Parity tolerances: fp32 max abs 1e-4; bf16 (fp32 accumulation) max abs
 # 1e-2 and mean abs 1e-3, checked on an fp32 output.  A bf16 output adds its
 # own final rounding: |err| <= 1e-2 + 2^-8 |ref|.
 TOL = {torch.float32: (1e-4, 1e-4), torch.bfloat16: (1e-2, 1e-3)}
