@@ -20,8 +20,7 @@
 //     It reads its 128 scores from TMEM 64 at a time, twice (once for the row
 //     maximum, once for the powers, so only 64 stay in registers), masks them,
 //     computes p = 2^(s * scale * log2 e - m) (one paired multiply-add per two
-//     elements; one pair in eight on the FMA pipe with a polynomial, the rest
-//     with ex2.approx on the special-function unit) and stores P as bf16 pairs
+//     elements, ex2.approx on the special-function unit) and stores P as bf16 pairs
 //     over the first 64 columns of the same S buffer, handing each half (64
 //     keys) to the MMA warp as soon as it is stored.  Each team has its own
 //     S/P buffer, O accumulator and running (m, l); the two partial results
@@ -596,16 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float pk[32];
     #pragma unroll
                     for (int i = 0; i < 32; i++) {
-                        float x0, x1, e0, e1;
+                        float x0, x1;
                         pkv::tc::unf2(pkv::tc::ffma2(pkv::tc::f2(sv[2 * i], sv[2 * i + 1]), sc2, nb2), x0, x1);
-                        // one pair in eight on the FMA pipe, the rest on the special-function
-                        // unit (about where the two take equally long)
-                        if ((i & 7) == 7) {
-                            pkv::tc::exp2_poly2(x0, x1, e0, e1);
-                        } else {
-                            e0 = pkv::tc::ex2(x0);
-                            e1 = pkv::tc::ex2(x1);
-                        }
+                        // all on the special-function unit: the fewest instructions
+                        // leave the most issue slots to the MMA-issuing thread
+                        const float e0 = pkv::tc::ex2(x0), e1 = pkv::tc::ex2(x1);
                         acc2[i & 1] = pkv::tc::fadd2(acc2[i & 1], pkv::tc::f2(e0, e1));
                         pk[i] = __uint_as_float(pkv::pack_bf16(e0, e1));
                     }

@@ -260,22 +260,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// 2^x on the FMA and integer pipes, for x <= 8 (smaller x clamped to -126).
-// x = n + f with n = rint(x) (the float magic-number method: adding
-// 1.5 * 2^23 leaves rint(x) in the low mantissa bits) and |f| <= 1/2; 2^f is
-// a cubic whose coefficients were fitted by weighted least squares for
-// minimum relative error on [-1/2, 1/2] (max relative error 7.5e-5, far below
-// bf16's 2^-9); n is then added to the exponent field.
-__device__ __forceinline__ float exp2_poly(float x) {
-    x = fmaxf(x, -126.f);
-    const float t = x + 12582912.f;
-    const float f = x - (t - 12582912.f);
-    const float p = fmaf(fmaf(fmaf(0.055171649903059006f, f, 0.2426111400127411f), f, 0.6932609677314758f), f,
-                         0.9999280571937561f);
-    const int n = __float_as_int(t) - 0x4B400000;
-    return __int_as_float(__float_as_int(p) + (n << 23));
-}
-
 // Paired fp32 arithmetic (sm_100 family): two lanes of a 64-bit register
 // pair in one instruction, each rounded as its scalar counterpart.
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
@@ -295,25 +279,6 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
     return d;
-}
-
-// exp2_poly of two values with paired arithmetic (same operations, same
-// rounding, so the results equal exp2_poly's bit for bit).
-__device__ __forceinline__ void exp2_poly2(float x0, float x1, float &e0, float &e1) {
-    const uint64_t x = f2(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-    const uint64_t t = fadd2(x, f2(12582912.f, 12582912.f));
-    const uint64_t f = ffma2(fadd2(t, f2(-12582912.f, -12582912.f)), f2(-1.f, -1.f), x);
-    uint64_t p = ffma2(f2(0.055171649903059006f, 0.055171649903059006f), f,
-                       f2(0.2426111400127411f, 0.2426111400127411f));
-    p = ffma2(p, f, f2(0.6932609677314758f, 0.6932609677314758f));
-    p = ffma2(p, f, f2(0.9999280571937561f, 0.9999280571937561f));
-    float p0, p1, t0, t1;
-    unf2(p, p0, p1);
-    unf2(t, t0, t1);
-    // (bits(t) - bits(1.5 * 2^23)) << 23 == bits(t) << 23: the magic's own
-    // bits shift out of the word
-    e0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-    e1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
 }
 
 }  // namespace tc
