@@ -40,7 +40,9 @@ def _worker(rank, world, port, values, results):
 def test_slowest_rank_time_is_taken():
     world = 2
     values = [3.25, 7.5]
-    with mp.Manager() as m:
+    # the manager process is spawned too: forking a process that already runs
+    # threads (torch, OpenMP) can deadlock the child
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_worker, args=(world, _free_port(), values, results), nprocs=world, join=True)
         assert dict(results) == {0: 7.5, 1: 7.5}
