@@ -162,6 +162,9 @@ def test_outlier_rows_long_mixed_lengths():
     ([50, 0], [200, 129], 8, 8, 128),
     ([0, 900], [40, 300], 32, 1, 128),
     ([0, 300], [77, 260], 24, 2, 128),
+    # empty chunks beside a non-empty one (their work items do nothing)
+    ([10, 0, 300], [0, 50, 0], 32, 8, 128),
+    ([10, 0, 300], [0, 50, 0], 8, 8, 64),
 ])
 def test_prefill_edges(priors, chunks, hq, hkv, d):
     b = W.custom_prefill("bf16", hq, hkv, d, priors, chunks, seed=301 + sum(chunks))
