@@ -54,6 +54,21 @@ def test_decode_workspace_sizes(lib):
     assert b"multiple of 16" in lib.pkv_last_error_string()
 
 
+def test_shared_prefix_workspace_sizes(lib):
+    # slot 0 for the shared prefix plus the suffix's 512-token partitions
+    # (the most slots any adaptive choice needs), then a 256-byte counter
+    r256 = lambda x: (x + 255) // 256 * 256
+    for S, Hq, L, P in ((256, 32, 2560, 2048), (8, 64, 100000, 512), (3, 8, 48, 32)):
+        parts = 1 + -(-(L - P) // 512)
+        rows = S * Hq * parts
+        want = (r256(rows * 128 * 4) + r256(rows * 2 * 4) if parts > 1 else 0) + 256
+        assert pkv.decode_shared_prefix_workspace_bytes(S, Hq, 128, L, P) == want
+    # head_dim 64, no prefix, a prefix not in whole blocks, a prefix past the context
+    for bad in ((4, 32, 64, 1000, 48), (4, 32, 128, 1000, 0), (4, 32, 128, 1000, 40), (4, 32, 128, 100, 112)):
+        with pytest.raises(pkv.PkvError):
+            pkv.decode_shared_prefix_workspace_bytes(*bad)
+
+
 def test_prefill_workspace_sizes(lib):
     # head_dim 128 (the tcgen05 kernel): one 8-byte work-item counter,
     # rounded to 256 bytes; head_dim 64 needs none
