@@ -50,6 +50,11 @@ struct Block {
     bool registered = false;  // in the prefix index (full, content known)
     uint64_t hash = 0;        // chain hash (registered blocks)
     uint64_t last_use = 0;    // for least-recently-used eviction
+    uint32_t gen = 0;         // times this block has been handed out
+    // registered blocks: the block before this one in the chain it was
+    // registered under (-1 for a first block) and that block's gen then
+    int32_t parent = -1;
+    uint32_t parent_gen = 0;
     std::array<int32_t, kBs> tok{};
 };
 
@@ -76,17 +81,24 @@ class BlockManager {
         const int nblk = (n + kBs - 1) / kBs;
         if (nblk > max_blocks_) return pkv::fail(PKV_ERR_INVALID, "bm_add_sequence: %d tokens exceed the table", n);
         // leading full blocks found in the prefix index
+        // A hit needs the same 16 token ids and, as its predecessor, the block
+        // already matched (the same physical block, not handed out again
+        // since): the whole prefix up to the block is then compared, and a
+        // collision of the 64-bit chain hash cannot reuse the wrong KV.
         std::vector<int32_t> hits;
-        std::vector<uint64_t> hashes;
         uint64_t h = 0;
+        int32_t prev = -1;
         for (int b = 0; prefix_ && (b + 1) * kBs <= n; b++) {
             const uint64_t hb = block_hash(h, tokens + b * kBs);
             auto it = index_.find(hb);
-            if (it == index_.end() || memcmp(blocks_[it->second].tok.data(), tokens + b * kBs, sizeof(int32_t) * kBs))
+            if (it == index_.end()) break;
+            const Block &cand = blocks_[it->second];
+            if (memcmp(cand.tok.data(), tokens + b * kBs, sizeof(int32_t) * kBs) || cand.parent != prev ||
+                (prev >= 0 && cand.parent_gen != blocks_[prev].gen))
                 break;
             hits.push_back(it->second);
-            hashes.push_back(hb);
             h = hb;
+            prev = it->second;
         }
         // hit blocks that are cached (unreferenced) leave the evictable set, so
         // they are not counted as available for the new blocks
@@ -240,6 +252,7 @@ class BlockManager {
             unregister(b);
         }
         blocks_[b].last_use = ++clock_;
+        blocks_[b].gen++;
         return b;
     }
 
@@ -262,8 +275,9 @@ class BlockManager {
         }
     }
 
-    // b has just become full as the next block of s: extend the chain hash
-    // and enter it in the index unless an identical block is already there.
+    // b has just become full as the last block of s: extend the chain hash
+    // and enter it in the index, with its predecessor, unless an identical
+    // block is already there.
     void register_full(Seq &s, int32_t b) {
         Block &blk = blocks_[b];
         const uint64_t h = block_hash(s.tail_hash, blk.tok.data());
@@ -271,6 +285,8 @@ class BlockManager {
         if (!prefix_ || blk.registered || index_.count(h)) return;
         blk.registered = true;
         blk.hash = h;
+        blk.parent = s.blocks.size() >= 2 ? s.blocks[s.blocks.size() - 2] : -1;
+        blk.parent_gen = blk.parent >= 0 ? blocks_[blk.parent].gen : 0;
         index_[h] = b;
     }
 
