@@ -34,7 +34,7 @@ __all__ = [
     "BLOCK_SIZE", "DEFAULT_PARTITION", "PkvError", "load", "library_path", "kv_append",
     "copy_blocks", "decode_workspace_bytes", "decode_partition_size", "paged_attention_decode",
     "decode_step", "decode_shared_prefix_workspace_bytes", "decode_shared_prefix",
-    "prefill_workspace_bytes", "paged_attention_prefill_chunk", "get_status", "STATUS_BITS",
+    "prefill_workspace_bytes", "paged_attention_prefill_chunk", "get_status", "set_wait_limit_ns", "STATUS_BITS",
     "EXPORTED", "kv_append_fp8", "paged_attention_decode_fp8", "check_copy_pairs", "BlockManager",
     "FP8_E4M3",
 ]
@@ -51,7 +51,7 @@ EXPORTED = (
     "pkv_paged_attention_decode", "pkv_decode_step", "pkv_paged_attention_decode_no_alloc",
     "pkv_decode_shared_prefix_workspace_bytes", "pkv_paged_attention_decode_shared_prefix",
     "pkv_prefill_workspace_bytes",
-    "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_last_error_string",
+    "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_set_wait_limit_ns", "pkv_last_error_string",
     "pkv_version",
     "pkv_kv_append_fp8", "pkv_paged_attention_decode_fp8",
     "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free_blocks", "pkv_bm_add_sequence", "pkv_bm_fork",
@@ -101,6 +101,7 @@ def load():
     lib.pkv_paged_attention_prefill_chunk.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, I,
                                                       I, F, P, I, I, P, SZ, P]
     lib.pkv_get_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
+    lib.pkv_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.pkv_last_error_string.argtypes = []
     lib.pkv_version.argtypes = []
     lib.pkv_kv_append_fp8.argtypes = [P, P, I, P, I, P, P, P, P, I, I, I, I, P]
@@ -160,6 +161,24 @@ def _stream(stream) -> int:
             return _RAW_STREAM(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _workspace(need: int, device, stream) -> Optional[torch.Tensor]:
+    """A scratch buffer of `need` bytes for one call enqueued on `stream`.
+
+    torch's caching allocator ties a block to the stream current at
+    allocation; when the call runs on another stream the block is also
+    recorded on that stream, so it is not handed out again (to work on the
+    current stream) before the call's kernels are done with it."""
+    if need <= 0:
+        return None
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    if stream is not None:
+        s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(
+            stream.cuda_stream if hasattr(stream, "cuda_stream") else stream), device=device)
+        if s.cuda_stream != torch.cuda.current_stream(device).cuda_stream:
+            ws.record_stream(s)
+    return ws
 
 
 def _cache_dims(k_cache: torch.Tensor, v_cache: torch.Tensor):
@@ -244,7 +263,7 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
         max_context_len = mb * bs
     if workspace is None:  # a caller's workspace is size-checked by the library
         need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
+        workspace = _workspace(need, q.device, stream)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().pkv_paged_attention_decode(
@@ -291,7 +310,7 @@ def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tabl
         max_context_len = mb * bs
     if workspace is None:  # a caller's workspace is size-checked by the library
         need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
+        workspace = _workspace(need, q.device, stream)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().pkv_paged_attention_decode_fp8(
@@ -322,7 +341,7 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, s
         max_context_len = mb * bs
     if workspace is None:  # a caller's workspace is size-checked by the library
         need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
+        workspace = _workspace(need, q.device, stream)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().pkv_decode_step(
@@ -368,7 +387,7 @@ def decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, scale,
         max_context_len = mb * bs
     if workspace is None:  # a caller's workspace is size-checked by the library
         need = decode_shared_prefix_workspace_bytes(S, Hq, d, max_context_len, prefix_len, partition_size)
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = _workspace(need, q.device, stream)
     _check(load().pkv_paged_attention_decode_shared_prefix(
         _dev(q, "q"), None if k_new is None else _dev(k_new, "k_new"),
         None if v_new is None else _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
@@ -409,7 +428,7 @@ def paged_attention_prefill_chunk(q, cu_q_lens, k_cache, v_cache, block_tables, 
         max_context_len = mb * bs
     if workspace is None:  # a caller's workspace is size-checked by the library
         need = prefill_workspace_bytes(S, total_q, Hq, Hkv, d, max_q_len, max_context_len)
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device) if need > 0 else None
+        workspace = _workspace(need, q.device, stream)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().pkv_paged_attention_prefill_chunk(
@@ -419,6 +438,13 @@ def paged_attention_prefill_chunk(q, cu_q_lens, k_cache, v_cache, block_tables, 
         int(max_context_len), Hq, Hkv, d, bs, NB, float(scale), _dev(out, "out"), _dt(q),
         _dt(out), ws_ptr, ws_bytes, _stream(stream)))
     return out
+
+
+def set_wait_limit_ns(ns: int = 0) -> None:
+    """Bound on each wait inside the tensor-core kernels, in nanoseconds (0:
+    the default, 200 ms); a launch whose wait runs out records the
+    ``internal`` status bit and returns with undefined outputs."""
+    _check(load().pkv_set_wait_limit_ns(int(ns)))
 
 
 def get_status(stream=None) -> int:

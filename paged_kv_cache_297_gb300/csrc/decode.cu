@@ -14,6 +14,8 @@
 //   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p 2^(m_p - M) O_p / L.
 // Logits are kept in base-2 units (scale * log2 e folded into one multiply).
 #include <math.h>
+
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -785,13 +787,15 @@ int resolve_partition(int partition_size, int *out) {
 // partitions amortise each thread block's start-up and cut the split-K
 // partials; enough units keep every SM streaming.
 // SM count of the current device (148 when there is none to ask)
+// (cached per device; host threads that race here store the same count)
 int device_sms() {
-    static int sm_count[64] = {0};
+    static std::atomic<int> sm_count[64];
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
-        if (!sm_count[dev] && cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            sm_count[dev] = 0;
-        if (sm_count[dev] > 0) sms = sm_count[dev];
+        int n = sm_count[dev].load(std::memory_order_relaxed);
+        if (n <= 0 && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            sm_count[dev].store(n, std::memory_order_relaxed);
+        if (n > 0) sms = n;
     }
     cudaGetLastError();
     return sms;
@@ -825,10 +829,11 @@ bool use_head_warps(int num_seqs, int units, int own_max, int partition) {
 template <int D, typename OutT, bool kHeadWarps, bool kFp8>
 int launch_bf16_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
     constexpr int bytes = DecodeSmem<D, kFp8>::kBytes;
-    static bool attr_set[64] = {false};
+    // set once per device (setting it twice from racing host threads is harmless)
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         // two thread blocks per SM: the largest shared-memory carve-out
         if (cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps, kFp8>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
@@ -836,7 +841,7 @@ int launch_bf16_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
                                  cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return pkv::check_launch("decode: set shared memory size");
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     const int units = p.num_kv_heads * p.head_chunks;
     // (with a shared prefix, partial slot 0 comes from another kernel)

@@ -41,9 +41,11 @@ int scratch_address(void **out) {
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess || !p)
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();  // a later call's launch check must not see this error
             return pkv::fail(PKV_ERR_CUDA, "decode_no_alloc: cudaGetSymbolAddress: %s",
                              cudaGetErrorString(e));
+        }
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
@@ -57,9 +59,14 @@ extern "C" int pkv_paged_attention_decode_no_alloc(
     int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int num_q_heads,
     int num_kv_heads, int head_dim, int block_size, int num_blocks, int max_context_len,
     int partition_size, float scale, void *out, int dtype, int out_dtype, void *stream) {
+    // The partition the call will use (partition_size 0: the adaptive choice),
+    // so that the scratch is sized for the launch that runs, not for the
+    // smallest partitions.
+    int part = 0;
+    int rc = pkv_decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size, &part);
+    if (rc) return rc;
     size_t need = 0;
-    int rc = pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
-                                        partition_size, &need);
+    rc = pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, part, &need);
     if (rc) return rc;
     if (need > kNoAllocScratchBytes)
         return pkv::fail(PKV_ERR_INVALID,
@@ -76,7 +83,7 @@ extern "C" int pkv_paged_attention_decode_no_alloc(
     // reads is written by the partition kernel of the same call.
     return pkv_paged_attention_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                       context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                      block_size, num_blocks, max_context_len, partition_size,
+                                      block_size, num_blocks, max_context_len, part,
                                       scale, out, dtype, out_dtype, scratch,
                                       need > 0 ? kNoAllocScratchBytes : 0, stream);
 }

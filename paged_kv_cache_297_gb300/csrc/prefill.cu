@@ -13,6 +13,8 @@
 // O += P V on the tensor cores.
 #include <math.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "prefill_common.cuh"
 
@@ -332,14 +334,15 @@ __global__ void __launch_bounds__(kThreads) prefill_cuda_core_kernel(const Prefi
 template <int D, typename OutT>
 int launch_bf16(const PrefillParams &p, int num_seqs, cudaStream_t st) {
     constexpr int bytes = PrefillSmem<D>::kBytes;
-    static bool attr_set[64] = {false};
+    // set once per device (setting it twice from racing host threads is harmless)
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(prefill_bf16_kernel<D, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  bytes) != cudaSuccess)
             return pkv::check_launch("prefill: set shared memory size");
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     const int tiles = (p.max_q_len * p.group + kTileQ - 1) / kTileQ;
     dim3 grid((unsigned)tiles, (unsigned)p.num_kv_heads, (unsigned)num_seqs);
@@ -366,7 +369,7 @@ extern "C" int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_
     if (!bytes || num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         max_q_len < 0 || max_context_len < 0 || (head_dim != 64 && head_dim != 128))
         return pkv::fail(PKV_ERR_INVALID, "prefill_workspace_bytes: bad argument");
-    // the tcgen05 path's work-item counter (one 8-byte word, 256-byte aligned)
+    // the tcgen05 path's work-item counter (16 bytes, in a 256-byte block)
     *bytes = head_dim == 128 ? 256 : 0;
     return PKV_OK;
 }
@@ -422,9 +425,9 @@ extern "C" int pkv_paged_attention_prefill_chunk(const void *q, const int32_t *c
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = pkv::status_ptr();
     if (pkv::prefill_tc_supported(dtype, head_dim)) {
-        if (!workspace || workspace_bytes < 8 || (reinterpret_cast<uintptr_t>(workspace) & 7u) != 0)
+        if (!workspace || workspace_bytes < 16 || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
             return pkv::fail(PKV_ERR_INVALID,
-                             "prefill: workspace of 8 bytes (8-byte aligned) needed, %zu given", workspace_bytes);
+                             "prefill: workspace of 16 bytes (16-byte aligned) needed, %zu given", workspace_bytes);
         p.item_counter = static_cast<unsigned long long *>(workspace);
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
