@@ -480,14 +480,22 @@ def fp8_batch(base: Batch, seed: int = 97) -> Batch:
     values (drawn directly as codes: random sign, exponent field uniform in
     [4, 10], mantissa uniform, so magnitudes 2^-3 .. 2^4 before scaling),
     the NaN code (0x7F) in every row the base batch poisons, and per kv head
-    scales 2^-4 (1 + g/8) for K and 2^-3 (1 + g/16) for V.  Queries and the
-    new tokens stay bf16 (the append quantises them)."""
+    scales 2^-4 (1 + g/8) for K and 2^-3 (1 + g/16) for V.  A row that the
+    base batch made an outlier (a row whose largest magnitude exceeds 8, which
+    an N(0,1) row of the workloads' sizes practically never does) keeps that
+    role: its exponent fields are raised by 4, so its values are 16 times
+    larger (magnitudes up to 240, still finite codes).  Queries and the new
+    tokens stay bf16 (the append quantises them)."""
     g = torch.Generator().manual_seed(seed)
     NB, H, bs, d = base.k_cache.shape
 
     def codes(src):
         sign = torch.randint(0, 2, src.shape, generator=g, dtype=torch.int32) << 7
-        ex = torch.randint(4, 11, src.shape, generator=g, dtype=torch.int32) << 3
+        ex = torch.randint(4, 11, src.shape, generator=g, dtype=torch.int32)
+        big = torch.empty(src.shape[:-1] + (1,), dtype=torch.bool)
+        for a in range(0, src.shape[0], 4096):  # in slices: the long-context caches hold ~1.6 GB each
+            big[a:a + 4096] = src[a:a + 4096].float().abs().amax(dim=-1, keepdim=True) > 8.0  # NaN: False
+        ex = torch.where(big, ex + 4, ex) << 3
         man = torch.randint(0, 8, src.shape, generator=g, dtype=torch.int32)
         c = (sign | ex | man).to(torch.uint8)
         c[src.isnan()] = 0x7F

@@ -90,6 +90,18 @@ def test_fp8_llama3_workload(out_dtype):
     assert_parity(out, ref, torch.bfloat16, "fp8 decode")
 
 
+@pytest.mark.parametrize("partition", [0, 512])
+def test_fp8_long_context_workload(partition):
+    # 8 sequences of 32k-131k tokens with 1% of K and V rows scaled by 20: the
+    # largest softmax weights meet the outlier V rows, and q and P enter the
+    # products as fp16; the adaptive partition and 512-token partitions (the
+    # longest reduce rows)
+    b = W.fp8_batch(W.make_batch("long_context"))
+    ref, out, (kc_o, vc_o), (kc_g, vc_g) = _fp8_step(b, partition_size=partition)
+    assert torch.equal(kc_g, kc_o) and torch.equal(vc_g, vc_o)
+    assert_parity(out, ref, torch.bfloat16, "fp8 long-context decode")
+
+
 @pytest.mark.parametrize("hq,hkv,partition", [(32, 8, 0), (64, 8, 512), (16, 1, 0), (48, 2, 256)])
 def test_fp8_edge_lengths(hq, hkv, partition):
     b = W.fp8_batch(W.custom_batch("bf16", len(EDGE_LENS), hq, hkv, 128, EDGE_LENS, seed=41 + hq))

@@ -406,6 +406,66 @@ def _cascade_step(b, prefix_len, out_dtype=torch.float32, fused=True, partition=
     return t, out
 
 
+def _prefill_call(b, t, out):
+    cu = b.prefill_cu_q_lens
+    pkv.paged_attention_prefill_chunk(
+        t["prefill_q"], t["prefill_cu_q_lens"], t["k_cache"], t["v_cache"], t["prefill_block_tables"],
+        t["prefill_context_lens"], b.scale, out, max_q_len=int((cu[1:] - cu[:-1]).max()),
+        max_context_len=int(b.prefill_context_lens.max()))
+
+
+def test_prefill_wait_limit_runs_out_and_is_reported():
+    # The tensor-core kernel's waits are bounded in time.  With a bound of 1 ns
+    # a wait runs out at once: the launch must stop, record the internal status
+    # bit and return (no hang, no fault), and the next launch with the default
+    # bound must be correct again.
+    b = W.custom_prefill("bf16", 32, 8, 128, [0, 3072], [512, 512], seed=31)
+    kc_o, vc_o, _, pout_o = oracle_step(b)
+    t = to_dev(b)
+    pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"])
+    torch.cuda.synchronize()
+    assert pkv.get_status() == 0
+    out = torch.zeros(b.prefill_q.shape, dtype=torch.float32, device="cuda")
+    pkv.set_wait_limit_ns(1)
+    try:
+        _prefill_call(b, t, out)
+        torch.cuda.synchronize()
+        status = pkv.get_status()
+    finally:
+        pkv.set_wait_limit_ns(0)
+    assert status & pkv.STATUS_BITS["internal"], status
+    out = torch.empty(b.prefill_q.shape, dtype=torch.float32, device="cuda")
+    _prefill_call(b, t, out)
+    torch.cuda.synchronize()
+    assert pkv.get_status() == 0
+    assert_parity(out, pout_o, b.dtype, "prefill after a run-out launch")
+
+
+def test_decode_on_a_side_stream_keeps_its_workspace():
+    # The binding allocates the split-K workspace on the current stream and
+    # the call runs on another one; the current stream then allocates a
+    # buffer of the same size and overwrites it while the decode may still be
+    # running.  The workspace must not be handed out again before the decode
+    # is done with it.
+    b = W.make_batch("llama3_8b_decode")
+    _, _, out_o, _ = oracle_step(b, prefill=False)
+    t = to_dev(b)
+    pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"])
+    out = torch.full(b.q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    need = pkv.decode_workspace_bytes(b.q.shape[0], b.q.shape[1], b.q.shape[2], b.max_context_len, 512)
+    for _ in range(3):
+        pkv.paged_attention_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
+                                   b.scale, out, max_context_len=b.max_context_len, partition_size=512,
+                                   stream=side)
+        junk = torch.empty(need, dtype=torch.uint8, device="cuda")
+        junk.fill_(0xFF)
+        del junk
+    torch.cuda.synchronize()
+    assert_parity(out, out_o, b.dtype, "decode on a side stream")
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_shared_prefix_cascade_workload(out_dtype):
     b = W.make_batch("shared_prefix_cow")
@@ -430,4 +490,5 @@ def test_shared_prefix_cascade_shapes(num_seqs, prefix_blocks, ctx, fused, parti
     t, out = _cascade_step(b, prefix_blocks * 16, fused=fused, partition=partition)
     assert pkv.get_status() == 0
     assert_bits_equal(t["k_cache"], kc_o, "k_cache")
+    assert_bits_equal(t["v_cache"], vc_o, "v_cache")
     assert_parity(out, out_o, b.dtype, "cascade decode")
