@@ -225,8 +225,11 @@ int pkv_decode_step(const void *q, const void *k_new, const void *v_new, void *k
  * workspace: the split-K partials go to one scratch array of
  * PKV_NO_ALLOC_SCRATCH_BYTES that is part of this library's device image.
  * Every GPU that loads the library holds that array until the process exits.
- *   - Sizes whose scratch need (pkv_decode_workspace_bytes) exceeds
- *     PKV_NO_ALLOC_SCRATCH_BYTES are rejected with PKV_ERR_INVALID.
+ *   - The scratch need is pkv_decode_workspace_bytes at the partition the
+ *     call uses (pkv_decode_partition_size: partition_size itself, or the
+ *     adaptive choice when it is 0).  Sizes whose need exceeds
+ *     PKV_NO_ALLOC_SCRATCH_BYTES are rejected with PKV_ERR_INVALID before
+ *     anything is launched.
  *   - The call allocates no memory: no cudaMalloc, cudaFree or allocating
  *     library routine.
  *   - The first call on each device looks up the array's device address
@@ -312,9 +315,9 @@ int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_heads, int 
  *   max_context_len  host-side bound on every L_s
  *   out        [total_q][num_q_heads][head_dim], out_dtype
  *   workspace  device scratch of pkv_prefill_workspace_bytes(...) bytes,
- *              8-byte aligned; it needs no initialisation (the call clears
- *              what it uses on `stream`), and calls that overlap on the GPU
- *              must not share it.
+ *              16-byte aligned; it needs no initialisation (each launch
+ *              claims its work counter with a fresh 64-bit tag), and calls
+ *              that overlap on the GPU must not share it.
  * n_s > L_s or n_s > max_q_len sets PKV_STATUS_BAD_QLEN and skips the sequence.
  */
 int pkv_paged_attention_prefill_chunk(const void *q, const int32_t *cu_q_lens,
@@ -417,6 +420,19 @@ int pkv_bm_block_tables(void *bm, const int64_t *seq_ids, int n, int32_t *tables
  * on a CUDA error.  The word is shared by every stream of the device.
  */
 int pkv_get_status(void *stream, unsigned int *flags);
+
+/*
+ * Bound on each wait inside the tensor-core kernels (the chunked-prefill tile
+ * and the shared-prefix tile of pkv_paged_attention_decode_shared_prefix): a
+ * wait on the kernel's own asynchronous copies or MMAs, or on another of its
+ * warps, that lasts longer than `ns` nanoseconds (GPU global timer) makes the
+ * kernel stop issuing work, let what it already issued finish, record
+ * PKV_STATUS_INTERNAL and return; its outputs are then undefined.  0 restores
+ * the default, 200 ms (far above any wait of a working launch, which lasts
+ * microseconds).  Process-wide; it applies to launches made after the call.
+ * Always returns PKV_OK.
+ */
+int pkv_set_wait_limit_ns(unsigned long long ns);
 
 /* Description of the last failure on the calling host thread ("" if none). */
 const char *pkv_last_error_string(void);

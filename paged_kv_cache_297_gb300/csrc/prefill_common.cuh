@@ -24,12 +24,14 @@ struct PrefillParams {
     int total_q;
     float scale_log2;
     unsigned *status;
-    // tcgen05 kernel only: persistent CTAs take (sequence, q tile, kv head)
-    // items from a counter in the workspace
+    // tcgen05 kernel only: persistent CTA pairs take (sequence, q tile, kv
+    // head) items from a counter in the workspace: 16 bytes, 16-byte
+    // aligned, {launch tag, count}, set by the kernel itself
     int num_seqs;
     int tiles_per_seq;
     int num_items;
     unsigned long long *item_counter;
+    unsigned long long launch_tag;
     // set by the launch: 1 when the q tiles are loaded by TMA (the group
     // divides the 128-row tile), 0 when the softmax threads copy them
     int q_tma;
@@ -44,10 +46,15 @@ struct PrefillParams {
     float *part_o;
     float *part_ml;
     int part_stride;
+    // tcgen05 kernel, set by the launch: the longest any of its waits may
+    // last (nanoseconds, %globaltimer) before it gives up
+    unsigned long long wait_ns;
 };
 
 // tcgen05 kernel (prefill_tc.cu): bf16 caches with head_dim 128.
 bool prefill_tc_supported(int dtype, int head_dim);
 int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaStream_t st);
+// Process-wide bound on each wait of the tcgen05 kernel (0: the default).
+void set_wait_limit_ns(unsigned long long ns);
 
 }  // namespace pkv

@@ -2,14 +2,19 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "common.cuh"
+#include "prefill_common.cuh"
 
 namespace {
 // One word per device that loads the library; kernels OR PKV_STATUS_* bits in.
 __device__ unsigned int g_status_word;
 
 constexpr int kMaxDevices = 64;
-unsigned *g_status_addr[kMaxDevices];
+// Looked up once per device; host threads that race here both store the same
+// address.
+std::atomic<unsigned *> g_status_addr[kMaxDevices];
 thread_local char g_err[512];
 }  // namespace
 
@@ -18,15 +23,17 @@ namespace pkv {
 unsigned *status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!g_status_addr[dev]) {
+    unsigned *addr = g_status_addr[dev].load(std::memory_order_acquire);
+    if (!addr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
-        g_status_addr[dev] = static_cast<unsigned *>(p);
+        addr = static_cast<unsigned *>(p);
+        g_status_addr[dev].store(addr, std::memory_order_release);
     }
-    return g_status_addr[dev];
+    return addr;
 }
 
 int fail(int code, const char *fmt, ...) {
@@ -57,6 +64,11 @@ extern "C" int pkv_get_status(void *stream, unsigned int *flags) {
     if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_get_status: %s", cudaGetErrorString(e));
     if (flags) *flags = v;
     return v ? PKV_ERR_OOB : PKV_OK;
+}
+
+extern "C" int pkv_set_wait_limit_ns(unsigned long long ns) {
+    pkv::set_wait_limit_ns(ns);
+    return PKV_OK;
 }
 
 extern "C" const char *pkv_last_error_string(void) { return g_err; }

@@ -1,5 +1,6 @@
-// Thin inline-PTX wrappers for the sm_100-family tensor-core path:
-// tcgen05 (TMEM allocation, MMA, loads/stores, commit, fences) and mbarrier.
+// Thin inline-PTX wrappers for the sm_100-family tensor-core path: tcgen05
+// (tensor memory allocation, MMA, loads and stores, commits, fences) in the
+// CTA-pair form, TMA loads, mbarrier, cluster addressing.
 #pragma once
 
 #include <stdint.h>
@@ -33,45 +34,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
                  : "memory");
 }
 
-// Arrive once on `bar` and add `bytes` to the transaction count it waits for.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile(
-        "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(
-            static_cast<uint32_t>(__cvta_generic_to_shared(bar))),
-        "r"(bytes)
-        : "memory");
-}
-
-// Add `bytes` to the transaction count the current phase waits for, without
-// arriving (the arrival comes later, from the same thread).
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(bar))),
-                 "r"(bytes)
-                 : "memory");
-}
-
-// 2-D tiled TMA load of one box into shared memory; completion is counted in
-// bytes on `bar`.  x is the inner (contiguous) coordinate, in elements.
-__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3}], [%4];\n" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y),
-        "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
-        : "memory");
-}
-
-// 3-D tiled TMA load of the box at (x, y, z) into shared memory.
-__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3, %4}], [%5];\n" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z),
-        "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
-        : "memory");
-}
-
 // One 32-byte global store (st.global.v8.b32) of two 16-byte vectors; dst
 // 32-byte aligned.
 __device__ __forceinline__ void st_global_32B(void *dst, const uint4 *v) {
@@ -80,49 +42,7 @@ __device__ __forceinline__ void st_global_32B(void *dst, const uint4 *v) {
                  : "memory");
 }
 
-// One bounded attempt sequence; returns true when phase `parity` completed,
-// false after `max_iters` unsuccessful polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned max_iters) {
-    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
-    {  // non-blocking test first: cheap when the phase has already completed
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done) return true;
-    }
-    for (unsigned it = 0; it < max_iters; it++) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done) return true;
-    }
-    return false;
-}
-
 // ---------------------------------------------------------------- TMEM
-
-// Warp-collective: allocate `ncols` TMEM columns, address written to *dst.
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, unsigned ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, unsigned ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
 
 __device__ __forceinline__ void fence_before_sync() {
     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
@@ -156,35 +76,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]: A is read from tensor memory (one row per
-// lane, two 16-bit elements per 32-bit column, lower K index in the low half).
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on `bar` when every MMA this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
-            static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
-        : "memory");
-}
-
 // ---------------------------------------------------------------- TMEM <-> registers
 
 // 32 lanes x 32 bits: this thread's TMEM lane, 32 consecutive columns from
@@ -202,46 +93,42 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
-// As tmem_ld32, 64 consecutive columns.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-    uint32_t r[64];
+// As tmem_ld32, 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
         "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 64; i++) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
-// As tmem_ld64, and also the largest of the 64 values (NaN ignored), taken
-// by the load itself (the reduction form of tcgen05.ld).
-__device__ __forceinline__ void tmem_ld64_max(uint32_t taddr, float (&v)[64], float &vmax) {
-    uint32_t r[64];
+// Store 16 consecutive columns of this thread's lane and wait for completion.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+        "tcgen05.wait::st.sync.aligned;\n"
+        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// As tmem_ld128 (128 consecutive columns), and also the largest of the 128
+// values (NaN ignored), taken by the load itself.
+__device__ __forceinline__ void tmem_ld128_max(uint32_t taddr, float (&v)[128], float &vmax) {
+    uint32_t r[128];
     float m;
     asm volatile(
-        "tcgen05.ld.red.sync.aligned.32x32b.x64.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %64, [%65];\n"
+        "tcgen05.ld.red.sync.aligned.32x32b.x128.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, %128, [%129];\n"
         "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=f"(m)
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 64; i++) v[i] = __uint_as_float(r[i]);
-    vmax = m;
-}
-
-// As tmem_ld32, 128 consecutive columns.
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
-    uint32_t r[128];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
-        "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127]), "=f"(m)
         : "r"(taddr)
         : "memory");
 #pragma unroll
     for (int i = 0; i < 128; i++) v[i] = __uint_as_float(r[i]);
+    vmax = m;
 }
 
 // Store 32 consecutive columns of this thread's lane and wait for completion.
@@ -279,6 +166,195 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+// ---------------------------------------------------------------- CTA pairs
+//
+// A cluster of two CTAs on two SMs works as one tensor-core unit
+// (cta_group::2): one thread of the even CTA issues an MMA with M = 256 whose
+// A rows 0-127 and accumulator rows 0-127 live in the even CTA (its shared
+// memory and tensor memory) and rows 128-255 in the odd CTA, at the same
+// addresses; each CTA holds one half of the B operand's N columns (the even
+// CTA the first half).  Every tcgen05 instruction of a kernel that does this
+// uses the cta_group::2 form.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the variable at shared::cta address `saddr` in
+// the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Every thread of both CTAs: arrive, then wait for all (release / acquire at
+// cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Arrive once on the mbarrier at shared::cluster address `a` (this CTA's or
+// the peer's), release at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t a) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(a) : "memory");
+}
+
+// Arrive once on the mbarrier at shared::cluster address `a` (this CTA's or
+// the peer's) with the default release at CTA scope: the cheap form, for
+// hand-offs whose data is ordered by other means (tensor-memory fences, the
+// copies' own byte counts).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t a) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t a, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;\n" ::"r"(a), "r"(bytes) : "memory");
+}
+
+// 16-byte store into shared memory at shared::cluster address `a`.
+__device__ __forceinline__ void st_cluster_v4(uint32_t a, int4 v) {
+    asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Non-blocking test of phase `parity` (acquire at cluster scope: arrivals
+// may come from the peer CTA).
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t a, unsigned parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Non-blocking and potentially suspending tests at the default (CTA) scope.
+__device__ __forceinline__ bool mbar_test_cta(uint32_t a, unsigned parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ bool mbar_try_cta(uint32_t a, unsigned parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// One potentially suspending test of phase `parity` (acquire, cluster scope).
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t a, unsigned parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// 2-D / 3-D tiled TMA load into this CTA's shared memory whose completion
+// (bytes) is counted on the mbarrier at shared::cluster address `bar`, which
+// may be the peer CTA's.
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *tmap, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];\n" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const void *tmap, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4}], [%5];\n" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// Tensor memory of both CTAs of the pair: one warp of each CTA executes these
+// together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, unsigned ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, unsigned ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// S = Q K^T over the pair for one key tile: eight M = 256 MMAs (K = 16 each)
+// over the 128 columns of d, the first overwriting D.  a0 / b0 are the
+// descriptors of the tiles' first 16 columns; the operands are 128-byte
+// swizzled with two 64-column halves, A's halves `a_half16` and B's
+// `b_half16` 16-byte units apart (the next 16 columns are 2 units on).
+template <int a_half16, int b_half16>
+__device__ __forceinline__ void mma_s_tile_pair(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+    asm volatile(
+        "{\n .reg .pred p0, p1;\n .reg .b64 a, b;\n"
+        " setp.ne.b32 p0, %3, %3;\n setp.eq.b32 p1, %3, %3;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p0;\n"
+        " add.s64 a, %1, 2;\n add.s64 b, %2, 2;\n tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, p1;\n"
+        " add.s64 a, %1, 4;\n add.s64 b, %2, 4;\n tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, p1;\n"
+        " add.s64 a, %1, 6;\n add.s64 b, %2, 6;\n tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, p1;\n"
+        " add.s64 a, %1, %4;\n add.s64 b, %2, %5;\n tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, p1;\n"
+        " add.s64 a, %1, %4 + 2;\n add.s64 b, %2, %5 + 2;\n tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, p1;\n"
+        " add.s64 a, %1, %4 + 4;\n add.s64 b, %2, %5 + 4;\n tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, p1;\n"
+        " add.s64 a, %1, %4 + 6;\n add.s64 b, %2, %5 + 6;\n tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, p1;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a0), "l"(b0), "r"(idesc), "n"(a_half16), "n"(b_half16)
+        : "memory");
+}
+
+// O (+)= P V over the pair for 64 keys: four M = 256 MMAs (K = 16 keys each),
+// A = P from tensor memory (8 columns per 16 keys), B = V MN-major (16 keys =
+// `v_step16` 16-byte units on).  The first MMA accumulates only when
+// `accumulate` is non-zero.
+template <int v_step16>
+__device__ __forceinline__ void mma_pv_half_pair(uint32_t d_tmem, uint32_t p_tmem, uint64_t v0, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p0, p1;\n .reg .b64 b;\n .reg .b32 a;\n"
+        " setp.ne.b32 p0, %4, 0;\n setp.eq.b32 p1, %3, %3;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p0;\n"
+        " add.s32 a, %1, 8;\n add.s64 b, %2, %5;\n tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, p1;\n"
+        " add.s32 a, %1, 16;\n add.s64 b, %2, %5 * 2;\n tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, p1;\n"
+        " add.s32 a, %1, 24;\n add.s64 b, %2, %5 * 3;\n tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, p1;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(p_tmem), "l"(v0), "r"(idesc), "r"(accumulate), "n"(v_step16)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at shared::cluster address `a` (either CTA's)
+// when every pair MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t a) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(a)
+                 : "memory");
 }
 
 }  // namespace tc
