@@ -10,10 +10,11 @@ context U[512, 4096], bf16).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference]
 
-N > 1 runs under torch.distributed.run, one rank per GPU: each rank serves its
-own independent batch of the same shape (sequences shard with no exchange),
-the timed region is bracketed by barriers and the slowest rank's time is used.
-Rank 0 prints one JSON line.  ``--impl reference`` times the fp64 host oracle
+N > 1 runs one rank per GPU under torch.distributed.run (started by this
+script itself when no launcher did): each rank serves its own independent
+batch of the same shape (sequences shard with no exchange), the timed region
+is bracketed by barriers and the slowest rank's time is used.  Rank 0 prints
+one JSON line.  ``--impl reference`` times the fp64 host oracle
 on the same workload instead.
 """
 
@@ -495,6 +496,107 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
+def step_rooflines(step: Step, per_call: dict, peaks: dict, workload: str):
+    """The decode call's HBM roofline (and the prefill chunk's tensor roofline,
+    the copy and append figures when the step has them) from the per-call
+    CUDA-event durations of one breakdown pass."""
+    batch = step.b
+    S, Hq, d = batch.q.shape
+    Hkv = batch.spec.num_kv_heads
+    elem = batch.q.element_size()
+    kv_elem = batch.k_cache.element_size()  # 1 for fp8 caches
+    # context lengths the decode call sees (after this step's append)
+    db = accounting.decode_bytes(batch.context_lens, Hq, Hkv, d, kv_elem, elem, elem)
+    dec_ms = per_call["decode"]
+    # the fused call also writes the appended K and V rows (it reads them from
+    # k_new/v_new instead of the cache, which the KV count already covers)
+    dec_bytes = db["total"] + (2 * S * Hkv * d * elem if step.fused else 0)
+    if step.cascade:
+        # the prefix's K/V are read once, not once per sequence: count them once
+        dec_bytes -= step.prefix_len * (S - 1) * 2 * Hkv * d * elem
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    kname = ("decode_shared_prefix" if step.cascade else "decode_step" if step.fused
+             else "paged_attention_decode_fp8" if step.fp8 else "paged_attention_decode")
+    traffic = recorded_traffic(kname, workload, CASCADE_SOURCES if step.cascade else DECODE_SOURCES)
+    roofline = {"kernel": ("decode_shared_prefix (fused append; shared-prefix tile on the tensor cores, "
+                           "partition kernel over each sequence's own tokens, log-sum-exp merge; bytes "
+                           "count the prefix once)" if step.cascade else
+                           "decode_step (fused append + partition kernel + log-sum-exp reduce)"
+                           if step.fused else
+                           "paged_attention_decode_fp8 (fp8 E4M3 cache widened to fp16 in registers, "
+                           "fp16 tile products; partition kernel + log-sum-exp reduce)" if step.fp8 else
+                           "paged_attention_decode (partition kernel + log-sum-exp reduce)"),
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "traffic_unit": "bytes per call (ncu dram read+write)",
+                "algorithmic_bytes": dec_bytes, "partition": step.part_used,
+                "kv_bytes": db["kv"], "decode_us": round(dec_ms * 1e3, 2)}
+    extra = {}
+    if step.pout is not None:
+        fl = accounting.prefill_flops(batch.prefill_cu_q_lens, batch.prefill_context_lens, Hq, d)
+        tf = fl / (per_call["prefill_chunk"] / 1e3) / 1e12
+        extra["prefill_roofline"] = {
+            "kernel": "prefill_tc_kernel (tcgen05, chunked-prefill tile)", "bound": "tensor",
+            "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+            "peak_source": f"{peaks['source']} bf16_tflops (cuBLAS burst)", "unit": "TFLOP/s",
+            "frac": round(tf / peaks["bf16_tflops"], 4),
+            "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+            "flops": fl, "us": round(per_call["prefill_chunk"] * 1e3, 2)}
+    if step.has_copy:
+        cb = accounting.copy_blocks_bytes(int(batch.copy_pairs.shape[0]), Hkv, d, elem)
+        extra["copy_blocks"] = {"pairs": int(batch.copy_pairs.shape[0]), "bytes": cb,
+                                "us": round(per_call["copy_blocks"] * 1e3, 2)}
+    if "kv_append" in per_call:
+        ab = accounting.append_bytes(int(batch.slot_mapping.numel()), Hkv, d, elem)
+        extra["append_gbs"] = round(ab / (per_call["kv_append"] / 1e3) / 1e9, 1)
+    return roofline, extra, db
+
+
+def seqs_per_step(batch: W.Batch) -> int:
+    return batch.num_seqs + (0 if batch.prefill_context_lens is None else int(batch.prefill_context_lens.numel()))
+
+
+# Workloads whose own targets ride on the headline run as sub-records: the
+# long-context decode (HBM roofline) and the mixed step (its prefill chunk
+# against the bf16 tensor roofline), plus the headline batch itself over a
+# long timed region.
+TARGET_WORKLOADS = ("llama3_8b_decode", "long_context", "mixed_step")
+
+
+def target_record(name: str, dev: str, peaks: dict, args, world: int, min_ms: float = 250.0) -> dict:
+    """One workload's step timed over at least `min_ms` of GPU time (so the
+    clock sampler sees it under load), with its rooflines."""
+    batch = W.make_batch(name, poison=False)
+    step = Step(batch, dev, args.partition, args.unfused, args.no_cascade)
+    calls = step.calls()
+    for _ in range(3):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        for _, fn in calls:
+            fn()
+    e1.record()
+    torch.cuda.synchronize()
+    n = max(10, int(math.ceil(min_ms / max(1e-3, e0.elapsed_time(e1) / 5))))
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    span_ms, serial_ms, per_call, _, pct = time_device(step, n, 3, world)
+    clk = clocks.stop()
+    roofline, extra, _ = step_rooflines(step, per_call, peaks, name)
+    rec = {"steps": n, "timed_ms": round(span_ms, 1), "ms_per_step": round(span_ms / n, 5),
+           "value": round(world * seqs_per_step(batch) * n / (span_ms / 1e3), 1), "unit": "seq-steps/s",
+           "calls_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
+           "serial_ms_per_step": round(serial_ms, 5), "roofline": roofline, "clocks": clk}
+    rec.update(extra)
+    del step
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     init_dist(world, "nccl")
@@ -516,53 +618,12 @@ def run_ours(args):
     e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, world)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
-    seqs_per_step = batch.num_seqs + (0 if batch.prefill_context_lens is None
-                                      else int(batch.prefill_context_lens.numel()))
+    sps = seqs_per_step(batch)
     ms_per_step = span_ms / args.steps
-    value = world * seqs_per_step * args.steps / (span_ms / 1e3)
+    value = world * sps * args.steps / (span_ms / 1e3)
     S, Hq, d = batch.q.shape
-    elem = batch.q.element_size()
-    kv_elem = batch.k_cache.element_size()  # 1 for fp8 caches
-    # context lengths the decode call sees (after this step's append)
-    db = accounting.decode_bytes(batch.context_lens, Hq, batch.spec.num_kv_heads, d, kv_elem, elem, elem)
-    ab = accounting.append_bytes(int(batch.slot_mapping.numel()), batch.spec.num_kv_heads, d, elem)
+    roofline, extra, db = step_rooflines(step, per_call, peaks, args.workload)
     dec_ms = per_call["decode"]
-    # the fused call also writes the appended K and V rows (it reads them from
-    # k_new/v_new instead of the cache, which the KV count already covers)
-    dec_bytes = db["total"] + (2 * S * batch.spec.num_kv_heads * d * elem if step.fused else 0)
-    if step.cascade:
-        # the prefix's K/V are read once, not once per sequence: count them once
-        dec_bytes -= step.prefix_len * (S - 1) * 2 * batch.spec.num_kv_heads * d * elem
-    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
-    kname = ("decode_shared_prefix" if step.cascade else "decode_step" if step.fused
-             else "paged_attention_decode_fp8" if step.fp8 else "paged_attention_decode")
-    traffic = recorded_traffic(kname, args.workload, CASCADE_SOURCES if step.cascade else DECODE_SOURCES)
-    roofline = {"kernel": ("decode_shared_prefix (fused append; shared-prefix tile on the tensor cores, "
-                           "partition kernel over each sequence's own tokens, log-sum-exp merge; bytes "
-                           "count the prefix once)" if step.cascade else
-                           "decode_step (fused append + partition kernel + log-sum-exp reduce)"
-                           if step.fused else
-                           "paged_attention_decode_fp8 (fp8 E4M3 cache widened to fp16 in registers, "
-                           "fp16 tile products; partition kernel + log-sum-exp reduce)" if step.fp8 else
-                           "paged_attention_decode (partition kernel + log-sum-exp reduce)"),
-                "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic, "traffic_unit": "bytes per call (ncu dram read+write)",
-                "algorithmic_bytes": dec_bytes, "partition": step.part_used,
-                "kv_bytes": db["kv"], "decode_us": round(dec_ms * 1e3, 2)}
-    extra = {}
-    if step.pout is not None:
-        fl = accounting.prefill_flops(batch.prefill_cu_q_lens, batch.prefill_context_lens, Hq, d)
-        tf = fl / (per_call["prefill_chunk"] / 1e3) / 1e12
-        extra["prefill_roofline"] = {"bound": "tensor", "achieved": round(tf, 1),
-                                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                                     "frac": round(tf / peaks["bf16_tflops"], 4), "flops": fl}
-    if step.has_copy:
-        cb = accounting.copy_blocks_bytes(int(batch.copy_pairs.shape[0]), batch.spec.num_kv_heads,
-                                          d, elem)
-        extra["copy_blocks"] = {"pairs": int(batch.copy_pairs.shape[0]), "bytes": cb,
-                                "us": round(per_call["copy_blocks"] * 1e3, 2)}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "seq-steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -582,17 +643,20 @@ def run_ours(args):
         "serial_ms_per_step": round(serial_ms, 5),
         "serial_step_ms_pct": step_pct,
         "roofline": roofline,
-        "e2e": {"value": round(world * seqs_per_step * args.steps / (e2e_ms / 1e3), 1),
+        "e2e": {"value": round(world * sps * args.steps / (e2e_ms / 1e3), 1),
                 "unit": "seq-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk,
         "wall_s": round(wall, 4),
     }
-    if "kv_append" in per_call:
-        extra["append_gbs"] = round(ab / (per_call["kv_append"] / 1e3) / 1e9, 1)
     line.update(extra)
+    del step
+    torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(batch)
+    if (world == 1 and not args.no_targets and args.workload == W.HEADLINE and args.kv_dtype == "bf16"
+            and args.partition == 0 and not args.unfused and not args.no_cascade):
+        line["targets"] = {name: target_record(name, dev, peaks, args, world) for name in TARGET_WORKLOADS}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -644,7 +708,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_ranks(n: int, argv) -> int:
+    """Run this script as `n` ranks, one process per GPU, under
+    torch.distributed.run on this node; returns its exit status.  Rank 0
+    prints the JSON line."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
@@ -660,9 +742,19 @@ def main(argv=None):
                     help="plain decode even where the batch shares a prefix")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="fp8: the same step over fp8 E4M3 caches (decode-only workloads)")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the long-timed records of the target workloads (headline run only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    world = os.environ.get("WORLD_SIZE")
+    if world is None and args.gpus > 1:
+        # not started by a launcher: start the ranks here
+        sys.exit(launch_ranks(args.gpus, argv))
+    if world is not None and int(world) != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: the launcher and the flag disagree")
     if args.impl == "reference":
         run_reference(args)
     else:
