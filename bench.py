@@ -194,6 +194,8 @@ class Step:
         self.partition = partition
         # the partition the library uses (decides whether the reduce launches)
         self.part_used = pkv.decode_partition_size(S, batch.spec.num_kv_heads, self.max_ctx, partition)
+        if batch.k_scale is not None:  # the fp8 kernel's own adaptive choice
+            self.part_used = pkv.decode_partition_size_fp8(S, Hq, batch.spec.num_kv_heads, self.max_ctx, partition)
         ws = pkv.decode_workspace_bytes(S, Hq, d, self.max_ctx, partition)
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
         self.pout = None

@@ -137,6 +137,17 @@ int pkv_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_le
                               int partition_size, int *out);
 
 /*
+ * As pkv_decode_partition_size for pkv_paged_attention_decode_fp8, whose
+ * adaptive choice differs: when num_seqs x units (units = num_kv_heads x
+ * ceil(num_q_heads / num_kv_heads / 8)) is between 2 and 4 times the SM
+ * count, one resident wave of its thread blocks covers the batch and no
+ * sequence is split (the partition is max_context_len rounded up to a
+ * multiple of 16); otherwise the choice of pkv_decode_partition_size.
+ */
+int pkv_decode_partition_size_fp8(int num_seqs, int num_q_heads, int num_kv_heads, int max_context_len,
+                                  int partition_size, int *out);
+
+/*
  * Paged-attention decode.  One query token per sequence and head attends to
  * every cached token of its sequence:
  *   out[s,h,:] = softmax_t(scale * q[s,h,:] . K_t) V_t,  t = 0 .. L_s - 1,
@@ -180,6 +191,7 @@ int pkv_paged_attention_decode(const void *q, const void *k_cache, const void *v
  *   k_cache, v_cache  [num_blocks][num_kv_heads][16][128] bytes
  *   k_scale, v_scale  [num_kv_heads] float32 device arrays
  *   out           [num_seqs][num_q_heads][128], out_dtype
+ * partition_size 0 takes the choice of pkv_decode_partition_size_fp8.
  * Precision: codes widen to fp16 exactly; q is rounded to fp16 once (a
  * query beyond the fp16 range, 65504, overflows); the softmax weights enter
  * the value product as fp16; accumulation is fp32.

@@ -53,7 +53,7 @@ EXPORTED = (
     "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_set_wait_limit_ns", "pkv_last_error_string",
     "pkv_version",
-    "pkv_kv_append_fp8", "pkv_paged_attention_decode_fp8",
+    "pkv_kv_append_fp8", "pkv_paged_attention_decode_fp8", "pkv_decode_partition_size_fp8",
     "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free_blocks", "pkv_bm_add_sequence", "pkv_bm_fork",
     "pkv_bm_append_tokens", "pkv_bm_slots", "pkv_bm_free_sequence", "pkv_bm_block_tables",
 )
@@ -89,6 +89,7 @@ def load():
     lib.pkv_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I, P]
     lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I, I, ctypes.POINTER(SZ)]
     lib.pkv_decode_partition_size.argtypes = [I, I, I, I, ctypes.POINTER(I)]
+    lib.pkv_decode_partition_size_fp8.argtypes = [I, I, I, I, I, ctypes.POINTER(I)]
     lib.pkv_paged_attention_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I,
                                                I, P, SZ, P]
     lib.pkv_decode_step.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I, I, P, SZ, P]
@@ -243,6 +244,15 @@ def decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_siz
     out = ctypes.c_int(0)
     _check(load().pkv_decode_partition_size(int(num_seqs), int(num_kv_heads), int(max_context_len),
                                             int(partition_size), ctypes.byref(out)))
+    return int(out.value)
+
+
+def decode_partition_size_fp8(num_seqs, num_q_heads, num_kv_heads, max_context_len,
+                              partition_size: int = 0) -> int:
+    """As :func:`decode_partition_size` for :func:`paged_attention_decode_fp8`."""
+    out = ctypes.c_int(0)
+    _check(load().pkv_decode_partition_size_fp8(int(num_seqs), int(num_q_heads), int(num_kv_heads),
+                                                int(max_context_len), int(partition_size), ctypes.byref(out)))
     return int(out.value)
 
 

@@ -17,6 +17,9 @@ constexpr int kBlock = 16;  // tokens per cache block
 
 // Device address of this device's status word (nullptr if it cannot be had).
 unsigned *status_ptr();
+// A 64-bit value drawn afresh for each launch that tags the work counters it
+// keeps in a caller's workspace (no clearing pass is needed before it).
+unsigned long long next_launch_tag();
 // Record a message for pkv_last_error_string() and return `code`.
 int fail(int code, const char *fmt, ...);
 // Turn a pending launch error into PKV_ERR_CUDA.

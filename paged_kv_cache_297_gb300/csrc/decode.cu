@@ -74,6 +74,7 @@ struct DecodeParams {
     const float *v_scale;
 };
 
+
 // Partitions of the tokens this launch covers for a sequence of L tokens.
 __device__ __forceinline__ int own_parts(const DecodeParams &p, int L) {
     if (p.prefix_len == 0) return L > 0 ? (L + p.partition - 1) / p.partition : 1;
@@ -114,14 +115,10 @@ __device__ __forceinline__ int clamp_len(int L, int cap, unsigned *status, bool 
 // bf16 tensor-core decode
 // ----------------------------------------------------------------------------
 
-template <int D, bool kFp8 = false>
+template <int D>
 struct DecodeSmem {
-    // ring depth in blocks: an fp8 block is half the bytes, and the fp8
-    // kernel runs three thread blocks per SM, so 4 stages of 4 KB per warp
-    // keep the bf16 kernel's bytes in flight per SM (2 blocks x 4 warps x
-    // 3 stages x 8 KB = 192 KB), which is what an HBM-bound SM needs
-    static constexpr int kRing = kFp8 ? 4 : kStages;
-    static constexpr int kRowBytes = D * (kFp8 ? 1 : 2);   // one cached row
+    static constexpr int kRing = kStages;                  // ring depth in blocks
+    static constexpr int kRowBytes = D * 2;                // one cached row
     static constexpr int kTile = kBlock * kRowBytes;      // one block of one kv head
     static constexpr int kStage = 2 * kTile;               // K + V
     static constexpr int kWarp = kRing * kStage;
@@ -132,23 +129,9 @@ struct DecodeSmem {
     static constexpr int kBytes = kStaging > kMerge ? kStaging : kMerge;
 };
 
-// kFp8: the cache holds fp8 E4M3 codes of value / scale (per kv head).  The
-// codes go from the shared-memory ring straight into mma.sync fragments,
-// widened to fp16 (exact) in registers: fp16 tile products with fp32
-// accumulation (the query rounded to fp16 once, P as one fp16 operand), the
-// K scale folded into the softmax scale, the V scale applied to the output.
-// Two permutations let whole 4-byte words feed the fragments:
-//  - S = q.K^T sums over d, so any order of d serves if q and K agree:
-//    in k-step kk, thread (gid, tig) supplies d = 32 tig + 4 kk + {0,1} as
-//    fragment positions {2 tig, 2 tig + 1} and + {2, 3} as {2 tig + 8,
-//    2 tig + 9}; its 32 K codes of a token are one 32-byte run.
-//  - O = P.V is computed in a permuted d order, undone at the store:
-//    column n of n-tile 4 m + j is d = 32 m + 4 n + j, so one 4-byte word
-//    of a token row serves four n-tiles, and two rows' words, byte-permuted,
-//    give the (token, token + 1) pairs of the B fragments.
-template <int D, typename OutT, bool kHeadWarps, bool kFp8 = false>
-__global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(const DecodeParams p) {
-    using Sm = DecodeSmem<D, kFp8>;
+template <int D, typename OutT, bool kHeadWarps>
+__global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodeParams p) {
+    using Sm = DecodeSmem<D>;
     constexpr int CH = Sm::kRowBytes / 16;    // 16-byte chunks per cached row
     constexpr int PER_LANE = kBlock * CH / 32;
     constexpr int KSTEPS = D / 16;
@@ -214,26 +197,11 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(con
             qa[kk][1] = vb ? *reinterpret_cast<const uint32_t *>(qb_row + col) : 0u;
             qa[kk][2] = va ? *reinterpret_cast<const uint32_t *>(qa_row + col + 8) : 0u;
             qa[kk][3] = vb ? *reinterpret_cast<const uint32_t *>(qb_row + col + 8) : 0u;
-            if constexpr (kFp8) {
-                // the permuted d order (see above), as fp16 pairs
-                const int pcol = 32 * tig + 4 * kk;
-                const uint2 ra = va ? *reinterpret_cast<const uint2 *>(qa_row + pcol) : make_uint2(0u, 0u);
-                const uint2 rb = vb ? *reinterpret_cast<const uint2 *>(qb_row + pcol) : make_uint2(0u, 0u);
-                const uint32_t w[4] = {ra.x, rb.x, ra.y, rb.y};
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
-                    qa[kk][e] = pkv::pack_f16(__low2float(h2), __high2float(h2));
-                }
-            }
         }
     }
-    // softmax scale in base-2 units (fp8: times the kv head's K scale) and
-    // the output factor (fp8: the V scale)
-    const float sl2 = kFp8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
-    const float vsc = kFp8 ? p.v_scale[kvh] : 1.f;
+    const float sl2 = p.scale_log2;  // softmax scale in base-2 units
 
-    if (!kFp8 && p.k_new && part == nparts - 1 && L > 0) {
+    if (p.k_new && part == nparts - 1 && L > 0) {
         // the new row is read below through L2 by other threads
         if (kHeadWarps) {
             // (warps of other chunks of the same kv head write the same bytes)
@@ -311,22 +279,7 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(con
 
         // S = q . K^T for the block's 16 tokens (two n-tiles of 8 tokens)
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (kFp8) {
-            // tokens gid and gid + 8: their codes d = 32 tig .. 32 tig + 31
-            const uint4 a0 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid, 2 * tig, Sm::kRowBytes));
-            const uint4 a1 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid, 2 * tig + 1, Sm::kRowBytes));
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid + 8, 2 * tig, Sm::kRowBytes));
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid + 8, 2 * tig + 1, Sm::kRowBytes));
-            const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const uint32_t wc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS; kk++) {
-                pkv::mma_f16(s0, qa[kk], pkv::e4m3x2_to_f16x2((uint16_t)(wa[kk] & 0xffffu)),
-                             pkv::e4m3x2_to_f16x2((uint16_t)(wa[kk] >> 16)));
-                pkv::mma_f16(s1, qa[kk], pkv::e4m3x2_to_f16x2((uint16_t)(wc[kk] & 0xffffu)),
-                             pkv::e4m3x2_to_f16x2((uint16_t)(wc[kk] >> 16)));
-            }
-        } else {
+        {
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; kk++) {
                 uint32_t b0, b1, b2, b3;
@@ -351,54 +304,37 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(con
         mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
         mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
         mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
-        const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
-        const float baseA = nA == -INFINITY ? 0.f : nA;
-        const float baseB = nB == -INFINITY ? 0.f : nB;
-        const float alA = pkv::fast_exp2(mA - baseA), alB = pkv::fast_exp2(mB - baseB);
-        mA = nA;
-        mB = nB;
+        // The running maximum moves only when a row's scores exceed it by
+        // more than 2^8 (base-2 units), so the state (m, l, O) is rescaled
+        // rarely; P = 2^(x - m) then stays at most 256, which fp16 and the
+        // bf16 hi/lo split of P hold without loss of relative precision,
+        // and the result O / l does not depend on which m is used.
+        if (__any_sync(0xffffffffu, mxA > mA + 8.f || mxB > mB + 8.f)) {
+            const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
+            const float alA = pkv::fast_exp2(mA - (nA == -INFINITY ? 0.f : nA));
+            const float alB = pkv::fast_exp2(mB - (nB == -INFINITY ? 0.f : nB));
+            mA = nA;
+            mB = nB;
+            lA *= alA;
+            lB *= alB;
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                o[nt][0] *= alA;
+                o[nt][1] *= alA;
+                o[nt][2] *= alB;
+                o[nt][3] *= alB;
+            }
+        }
+        const float baseA = mA == -INFINITY ? 0.f : mA;
+        const float baseB = mB == -INFINITY ? 0.f : mB;
         float pr[8];
 #pragma unroll
         for (int e = 0; e < 4; e++) pr[e] = pkv::fast_exp2(x[e] - baseA);
 #pragma unroll
         for (int e = 4; e < 8; e++) pr[e] = pkv::fast_exp2(x[e] - baseB);
-        lA = lA * alA + (pr[0] + pr[1] + pr[2] + pr[3]);
-        lB = lB * alB + (pr[4] + pr[5] + pr[6] + pr[7]);
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++) {
-            o[nt][0] *= alA;
-            o[nt][1] *= alA;
-            o[nt][2] *= alB;
-            o[nt][3] *= alB;
-        }
-        if constexpr (kFp8) {
-            // P as one fp16 A fragment (11 significant bits; P <= 1)
-            const uint32_t ph[4] = {pkv::pack_f16(pr[0], pr[1]), pkv::pack_f16(pr[4], pr[5]),
-                                    pkv::pack_f16(pr[2], pr[3]), pkv::pack_f16(pr[6], pr[7])};
-            // O += P . V in the permuted column order: rows 2 tig, 2 tig + 1,
-            // 2 tig + 8, 2 tig + 9 (the fragment's token pairs), bytes
-            // 32 m + 4 gid .. + 3 of each
-            auto word = [&](int row, int m) {
-                const int cb = 32 * m + 4 * gid;
-                return *reinterpret_cast<const uint32_t *>(vs + pkv::swz(row, cb >> 4, Sm::kRowBytes) + (cb & 15));
-            };
-#pragma unroll
-            for (int m = 0; m < D / 32; m++) {
-                const uint32_t wa = word(2 * tig, m), wb = word(2 * tig + 1, m);
-                const uint32_t wc = word(2 * tig + 8, m), wd = word(2 * tig + 9, m);
-                // (token, token + 1) code pairs for columns j = 0 .. 3
-                const uint32_t p01 = __byte_perm(wa, wb, 0x5140), p23 = __byte_perm(wa, wb, 0x7362);
-                const uint32_t q01 = __byte_perm(wc, wd, 0x5140), q23 = __byte_perm(wc, wd, 0x7362);
-                pkv::mma_f16(o[4 * m], ph, pkv::e4m3x2_to_f16x2((uint16_t)(p01 & 0xffffu)),
-                             pkv::e4m3x2_to_f16x2((uint16_t)(q01 & 0xffffu)));
-                pkv::mma_f16(o[4 * m + 1], ph, pkv::e4m3x2_to_f16x2((uint16_t)(p01 >> 16)),
-                             pkv::e4m3x2_to_f16x2((uint16_t)(q01 >> 16)));
-                pkv::mma_f16(o[4 * m + 2], ph, pkv::e4m3x2_to_f16x2((uint16_t)(p23 & 0xffffu)),
-                             pkv::e4m3x2_to_f16x2((uint16_t)(q23 & 0xffffu)));
-                pkv::mma_f16(o[4 * m + 3], ph, pkv::e4m3x2_to_f16x2((uint16_t)(p23 >> 16)),
-                             pkv::e4m3x2_to_f16x2((uint16_t)(q23 >> 16)));
-            }
-        } else {
+        lA += (pr[0] + pr[1] + pr[2] + pr[3]);
+        lB += (pr[4] + pr[5] + pr[6] + pr[7]);
+        {
             // P as two bf16 A fragments, hi + lo, so P keeps ~16 significant bits
             float hi[8], lo[8];
 #pragma unroll
@@ -432,18 +368,11 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(con
     pkv::cp_async_wait<0>();
     // The accumulator as pairs of adjacent output columns: slot k holds, for
     // row gid (hi = 0) or gid + 8 (hi = 1), the values of columns col and
-    // col + 1 (fp8: in the permuted order of the value product, undone here).
+    // col + 1.
     auto out_pair = [&](int k, int hi, float &x0, float &x1) -> int {
-        if constexpr (kFp8) {
-            const int m = k >> 2, e = (k >> 1) & 1, j = (k & 1) * 2;
-            x0 = o[4 * m + j][2 * hi + e];
-            x1 = o[4 * m + j + 1][2 * hi + e];
-            return 32 * m + 8 * tig + 4 * e + j;
-        } else {
-            x0 = o[k][2 * hi];
-            x1 = o[k][2 * hi + 1];
-            return k * 8 + tig * 2;
-        }
+        x0 = o[k][2 * hi];
+        x1 = o[k][2 * hi + 1];
+        return k * 8 + tig * 2;
     };
     if (kHeadWarps) {
         // the warp holds its rows' whole state for this partition
@@ -452,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(con
         if (nslots == 1) {
             OutT *oa = static_cast<OutT *>(p.out) + orow * D;
             OutT *ob = oa + 8 * D;
-            const float ia = lA > 0.f ? vsc / lA : 0.f, ib = lB > 0.f ? vsc / lB : 0.f;
+            const float ia = lA > 0.f ? 1.f / lA : 0.f, ib = lB > 0.f ? 1.f / lB : 0.f;
 #pragma unroll
             for (int k = 0; k < NT; k++) {
                 float x0, x1, y0, y1;
@@ -468,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(con
                 float x0, x1, y0, y1;
                 const int col = out_pair(k, 0, x0, x1);
                 out_pair(k, 1, y0, y1);
-                if (okA) *reinterpret_cast<float2 *>(p.part_o + pa * D + col) = make_float2(x0 * vsc, x1 * vsc);
-                if (okB) *reinterpret_cast<float2 *>(p.part_o + pb * D + col) = make_float2(y0 * vsc, y1 * vsc);
+                if (okA) *reinterpret_cast<float2 *>(p.part_o + pa * D + col) = make_float2(x0, x1);
+                if (okB) *reinterpret_cast<float2 *>(p.part_o + pb * D + col) = make_float2(y0, y1);
             }
             if (tig == 0 && okA) *reinterpret_cast<float2 *>(p.part_ml + pa * 2) = make_float2(mA, lA);
             if (tig == 0 && okB) *reinterpret_cast<float2 *>(p.part_ml + pb * 2) = make_float2(mB, lB);
@@ -516,10 +445,10 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(con
         }
         const size_t orow = (size_t)s * p.num_q_heads + h0 + r;
         if (nslots == 1) {
-            pkv::store1(static_cast<OutT *>(p.out) + orow * D + c, lsum > 0.f ? acc * vsc / lsum : 0.f);
+            pkv::store1(static_cast<OutT *>(p.out) + orow * D + c, lsum > 0.f ? acc / lsum : 0.f);
         } else {
             const size_t prow = orow * p.max_parts + slot0 + part;
-            p.part_o[prow * D + c] = acc * vsc;
+            p.part_o[prow * D + c] = acc;
             if (c == 0) {
                 p.part_ml[prow * 2] = M;
                 p.part_ml[prow * 2 + 1] = lsum;
@@ -527,6 +456,328 @@ __global__ void __launch_bounds__(kThreads, kFp8 ? 3 : 2) decode_bf16_kernel(con
         }
     }
     if (tail_wait) pkv::grid_dependency_wait();
+}
+
+// ----------------------------------------------------------------------------
+// fp8 decode with the operands swapped
+// ----------------------------------------------------------------------------
+// The scores are computed transposed, S^T = K q^T, and the output as
+// O^T = V^T P^T: the 16 tokens of a block are the M side of each
+// m16n8k16 product and the unit's (at most) 8 query rows its N side.  With
+// 4 or 8 query heads per kv head this wastes at most half of each product
+// (the layout with queries on the M side wastes 12 of 16 rows for 4), so a
+// block takes half the tensor-core products, half the exponentials and half
+// the accumulator registers, and four thread blocks (16 warps) fit per SM.
+// The codes still reach the fragments as whole 4-byte words, widened to
+// fp16 in registers:
+//  - S^T: in k-step kk, fragment columns {2 tig, 2 tig + 1} take
+//    d = 32 tig + 4 kk + {0, 1} and {2 tig + 8, 2 tig + 9} take + {2, 3}
+//    (the query is read in the same order), so thread (gid, tig) reads the
+//    32-byte run [32 tig, 32 tig + 32) of tokens gid and gid + 8;
+//  - O^T: accumulator row (mt, gid + 8 h) of m-tile mt is d = 16 gid +
+//    2 mt + h, so the thread reads the 16 bytes [16 gid, 16 gid + 16) of
+//    tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 and ends holding 16
+//    consecutive output columns of query rows 2 tig and 2 tig + 1;
+//  - P^T reaches the B fragments through one 8x8 transpose (movmatrix) per
+//    8 tokens of the score accumulator.
+constexpr int kRows8 = 8;  // query rows of one fp8 unit
+
+struct Fp8Smem {
+    static constexpr int kRing = 3;                        // blocks per warp ring
+    static constexpr int kRowBytes = 128;                  // one cached row (d = 128 codes)
+    static constexpr int kTile = kBlock * kRowBytes;       // one block of one kv head
+    static constexpr int kStage = 2 * kTile;               // K + V
+    static constexpr int kWarp = kRing * kStage;
+    static constexpr int kStaging = kWarps * kWarp;
+    static constexpr int kMergeStride = 128 + 4;           // floats per merged row
+    static constexpr int kMergeWarp = kRows8 * kMergeStride + 2 * kRows8;
+    static constexpr int kMerge = kWarps * kMergeWarp * 4;
+    static constexpr int kBytes = kStaging > kMerge ? kStaging : kMerge;
+};
+
+__device__ __forceinline__ uint32_t transpose8x8_b16(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+    return d;
+}
+
+template <typename OutT, bool kHeadWarps>
+__global__ void __launch_bounds__(kThreads, 4) decode_fp8_kernel(const DecodeParams p) {
+    using Sm = Fp8Smem;
+    constexpr int D = 128, KSTEPS = 8, MT = 8;
+    constexpr int PER_LANE = kBlock * (Sm::kRowBytes / 16) / 32;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    pkv::allow_dependents();
+    pkv::grid_dependency_wait();  // the rows the previous launch appended
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int unit = kHeadWarps ? blockIdx.x * kWarps + warp : blockIdx.x;
+    const bool idle = kHeadWarps && unit >= p.num_kv_heads * p.head_chunks;
+    const int kvh = unit / p.head_chunks, chunk = unit - kvh * p.head_chunks;
+    const int s = blockIdx.y, part = blockIdx.z;
+    const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
+    const int blk_begin = part * p.partition / kBlock;
+    // the warp's blocks (a head warp: all of the partition; a split warp:
+    // every fourth); the first 32 block ids come with one coalesced load
+    const int bstride = kHeadWarps ? 1 : kWarps;
+    const int bfirst = blk_begin + (kHeadWarps ? 0 : warp);
+    int my_id = 0;
+    if (!idle && bfirst + bstride * lane < p.max_blocks) my_id = table[bfirst + bstride * lane];
+
+    const int L = clamp_len(p.context_lens[s], p.len_cap, p.status,
+                            part == 0 && blockIdx.x == 0 && threadIdx.x == 0);
+    const int nparts = own_parts(p, L);
+    if (part >= nparts || idle) return;
+
+    const int h0 = kvh * p.group + chunk * kRows8;
+    const int rows = min(kRows8, p.group - chunk * kRows8);
+    const int t_end = min(L, (part + 1) * p.partition);
+    const int nblk = (t_end + kBlock - 1) / kBlock - blk_begin;
+    const int n = kHeadWarps ? nblk : max(0, (nblk - warp + kWarps - 1) / kWarps);
+    const unsigned char *kc = static_cast<const unsigned char *>(p.k_cache);
+    const unsigned char *vc = static_cast<const unsigned char *>(p.v_cache);
+
+    // q^T as B fragments (query row gid of the unit, zero past `rows`), d
+    // in the order the K codes are read
+    uint32_t qb[KSTEPS][2];
+    {
+        const bool ok = gid < rows;
+        const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(p.q) +
+                                    ((size_t)s * p.num_q_heads + h0 + (ok ? gid : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; kk++) {
+            const uint2 r = ok ? *reinterpret_cast<const uint2 *>(qrow + 32 * tig + 4 * kk) : make_uint2(0u, 0u);
+            const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&r.x);
+            const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&r.y);
+            qb[kk][0] = pkv::pack_f16(__low2float(lo), __high2float(lo));
+            qb[kk][1] = pkv::pack_f16(__low2float(hi), __high2float(hi));
+        }
+    }
+    // base-2 softmax scale times the kv head's K scale; the V scale
+    const float sl2 = p.scale_log2 * p.k_scale[kvh];
+    const float vsc = p.v_scale[kvh];
+
+    unsigned char *ring = smem + warp * Sm::kWarp;
+    auto block_id = [&](int li) -> int {
+        return li < 32 ? __shfl_sync(0xffffffffu, my_id, li) : table[bfirst + bstride * li];
+    };
+    // rows of the warp's li-th block that hold tokens of this partition (-1 for a bad id)
+    auto block_rows = [&](int li, int &phys) -> int {
+        phys = block_id(li);
+        if (phys < 0 || phys >= p.num_blocks) return -1;
+        return min(kBlock, t_end - (bfirst + bstride * li) * kBlock);
+    };
+    // copies of the li-th block into stage st, rows past the keys zeroed
+    auto issue = [&](int li, int st) {
+        int phys;
+        int valid = block_rows(li, phys);
+        if (valid < 0) {
+            if (lane == 0) pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+            valid = 0;
+            phys = 0;
+        }
+        const size_t base = ((size_t)phys * p.num_kv_heads + kvh) * Sm::kTile;
+        unsigned char *ks = ring + st * Sm::kStage;
+#pragma unroll
+        for (int j = 0; j < PER_LANE; j++) {
+            const int i = lane + 32 * j;
+            const int r = i >> 3, c = i & 7;
+            const int nb = r < valid ? 16 : 0;
+            const int go = nb ? r * Sm::kRowBytes + c * 16 : 0;
+            pkv::cp_async16(ks + pkv::swz(r, c, Sm::kRowBytes), kc + base + go, nb);
+            pkv::cp_async16(ks + Sm::kTile + pkv::swz(r, c, Sm::kRowBytes), vc + base + go, nb);
+        }
+    };
+
+    float o[MT][4];
+#pragma unroll
+    for (int i = 0; i < MT; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    // running max and (this thread's part of the) sum of query rows 2 tig, 2 tig + 1
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+#pragma unroll
+    for (int st = 0; st < Sm::kRing - 1; st++) {
+        if (st < n) issue(st, st);
+        pkv::cp_async_commit();
+    }
+    for (int i = 0; i < n; i++) {
+        {
+            const int nx = i + Sm::kRing - 1;
+            if (nx < n) issue(nx, nx % Sm::kRing);
+            pkv::cp_async_commit();
+        }
+        pkv::cp_async_wait<Sm::kRing - 1>();
+        __syncwarp();
+        const unsigned char *ks = ring + (i % Sm::kRing) * Sm::kStage;
+        const unsigned char *vs = ks + Sm::kTile;
+        int phys;
+        int valid = block_rows(i, phys);
+        if (valid < 0) valid = 0;
+
+        // S^T for the block: tokens gid and gid + 8 (codes d = 32 tig ..)
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid, 2 * tig, Sm::kRowBytes));
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid, 2 * tig + 1, Sm::kRowBytes));
+            const uint4 b0 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid + 8, 2 * tig, Sm::kRowBytes));
+            const uint4 b1 = *reinterpret_cast<const uint4 *>(ks + pkv::swz(gid + 8, 2 * tig + 1, Sm::kRowBytes));
+            const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; kk++) {
+                const uint32_t af[4] = {pkv::e4m3x2_to_f16x2((uint16_t)(wa[kk] & 0xffffu)),
+                                        pkv::e4m3x2_to_f16x2((uint16_t)(wb[kk] & 0xffffu)),
+                                        pkv::e4m3x2_to_f16x2((uint16_t)(wa[kk] >> 16)),
+                                        pkv::e4m3x2_to_f16x2((uint16_t)(wb[kk] >> 16))};
+                pkv::mma_f16(c, af, qb[kk][0], qb[kk][1]);
+            }
+        }
+        // base-2 units, tokens past the keys masked; c[0], c[1]: token gid,
+        // rows 2 tig, 2 tig + 1; c[2], c[3]: token gid + 8
+        const float x0 = gid < valid ? c[0] * sl2 : -INFINITY;
+        const float x1 = gid < valid ? c[1] * sl2 : -INFINITY;
+        const float x2 = gid + 8 < valid ? c[2] * sl2 : -INFINITY;
+        const float x3 = gid + 8 < valid ? c[3] * sl2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        // the running maximum moves only when a row's scores pass it by more
+        // than 2^8, so P <= 256 (exact enough in fp16) and O, l are rescaled rarely
+        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float al0 = pkv::fast_exp2(m0 - (n0 == -INFINITY ? 0.f : n0));
+            const float al1 = pkv::fast_exp2(m1 - (n1 == -INFINITY ? 0.f : n1));
+            m0 = n0;
+            m1 = n1;
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int mt = 0; mt < MT; mt++) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+        }
+        const float base0 = m0 == -INFINITY ? 0.f : m0, base1 = m1 == -INFINITY ? 0.f : m1;
+        const float p0 = pkv::fast_exp2(x0 - base0), p1 = pkv::fast_exp2(x1 - base1);
+        const float p2 = pkv::fast_exp2(x2 - base0), p3 = pkv::fast_exp2(x3 - base1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        // P^T as B fragments: {P[row gid][token 2 tig], [2 tig + 1]} and + 8
+        const uint32_t pb0 = transpose8x8_b16(pkv::pack_f16(p0, p1));
+        const uint32_t pb1 = transpose8x8_b16(pkv::pack_f16(p2, p3));
+
+        // O^T += V^T P^T: tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9, codes
+        // d = 16 gid .. 16 gid + 15
+        const int t0 = 2 * tig;
+        const uint4 v0 = *reinterpret_cast<const uint4 *>(vs + pkv::swz(t0, gid, Sm::kRowBytes));
+        const uint4 v1 = *reinterpret_cast<const uint4 *>(vs + pkv::swz(t0 + 1, gid, Sm::kRowBytes));
+        const uint4 v2 = *reinterpret_cast<const uint4 *>(vs + pkv::swz(t0 + 8, gid, Sm::kRowBytes));
+        const uint4 v3 = *reinterpret_cast<const uint4 *>(vs + pkv::swz(t0 + 9, gid, Sm::kRowBytes));
+        const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+        const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+        for (int mt = 0; mt < MT; mt++) {
+            // bytes 2 mt, 2 mt + 1 of each row: (token, token + 1) code pairs
+            const unsigned sel = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t lo = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
+            const uint32_t hi = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
+            const uint32_t af[4] = {pkv::e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu)),
+                                    pkv::e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
+                                    pkv::e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu)),
+                                    pkv::e4m3x2_to_f16x2((uint16_t)(hi >> 16))};
+            pkv::mma_f16(o[mt], af, pb0, pb1);
+        }
+        __syncwarp();
+    }
+    pkv::cp_async_wait<0>();
+
+    // the row sums over all 32 lanes' tokens
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    const int nslots = nparts;
+    // this thread's values of query row 2 tig + e, columns 16 gid + j
+    auto val = [&](int j, int e) -> float { return o[j >> 1][2 * (j & 1) + e]; };
+
+    if (kHeadWarps) {
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+            const int r = 2 * tig + e;
+            if (r >= rows) continue;
+            const float m = e ? m1 : m0, l = e ? l1 : l0;
+            const size_t orow = (size_t)s * p.num_q_heads + h0 + r;
+            if (nslots == 1) {
+                OutT *op = static_cast<OutT *>(p.out) + orow * D + 16 * gid;
+                const float inv = l > 0.f ? vsc / l : 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) pkv::store2(op + j, val(j, e) * inv, val(j + 1, e) * inv);
+            } else {
+                const size_t prow = orow * p.max_parts + part;
+                float *po = p.part_o + prow * D + 16 * gid;
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4 *>(po + j) =
+                        make_float4(val(j, e) * vsc, val(j + 1, e) * vsc, val(j + 2, e) * vsc, val(j + 3, e) * vsc);
+                if (gid == 0) *reinterpret_cast<float2 *>(p.part_ml + prow * 2) = make_float2(m, l);
+            }
+        }
+        return;
+    }
+
+    __syncthreads();  // every warp is done with its ring; reuse it for the merge
+    float *mw = reinterpret_cast<float *>(smem) + warp * Sm::kMergeWarp;
+    float *mm = mw + kRows8 * Sm::kMergeStride;
+    float *ll = mm + kRows8;
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int r = 2 * tig + e;
+        if (gid == 0) {
+            mm[r] = e ? m1 : m0;
+            ll[r] = e ? l1 : l0;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(mw + r * Sm::kMergeStride + 16 * gid + j) =
+                make_float4(val(j, e), val(j + 1, e), val(j + 2, e), val(j + 3, e));
+    }
+    __syncthreads();
+
+    const float *base = reinterpret_cast<const float *>(smem);
+    for (int idx = threadIdx.x; idx < rows * D; idx += kThreads) {
+        const int r = idx / D, col = idx - (idx / D) * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; w++) M = fmaxf(M, base[w * Sm::kMergeWarp + kRows8 * Sm::kMergeStride + r]);
+        float acc = 0.f, lsum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; w++) {
+                const float *bw = base + w * Sm::kMergeWarp;
+                const float f = pkv::fast_exp2(bw[kRows8 * Sm::kMergeStride + r] - M);
+                lsum += bw[kRows8 * Sm::kMergeStride + kRows8 + r] * f;
+                acc += bw[r * Sm::kMergeStride + col] * f;
+            }
+        }
+        const size_t orow = (size_t)s * p.num_q_heads + h0 + r;
+        if (nslots == 1) {
+            pkv::store1(static_cast<OutT *>(p.out) + orow * D + col, lsum > 0.f ? acc * vsc / lsum : 0.f);
+        } else {
+            const size_t prow = orow * p.max_parts + part;
+            p.part_o[prow * D + col] = acc * vsc;
+            if (col == 0) {
+                p.part_ml[prow * 2] = M;
+                p.part_ml[prow * 2 + 1] = lsum;
+            }
+        }
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -811,6 +1062,17 @@ int adaptive_partition(int num_seqs, int num_kv_heads, int max_context_len) {
     return PKV_DEFAULT_PARTITION;
 }
 
+// The fp8 kernel's choice: when the (sequence, unit) pairs fill between two
+// and four of its thread blocks per SM, a sequence is not split at all: one
+// resident wave covers the batch, and the partials and the merge launch cost
+// more than the uneven lengths do.  Otherwise as adaptive_partition.
+int fp8_partition(int num_seqs, int units_per_seq, int num_kv_heads, int max_context_len) {
+    const long long units = (long long)num_seqs * units_per_seq, sms = device_sms();
+    if (units >= 2 * sms && units <= 4 * sms && max_context_len > 0)
+        return (max_context_len + kBlock - 1) / kBlock * kBlock;
+    return adaptive_partition(num_seqs, num_kv_heads, max_context_len);
+}
+
 // Head warps when a partition spans at most this many tokens (split four
 // ways it would give each warp at most 8 blocks, too few to amortise the
 // block's start: length, block ids, first copies, merge), provided the
@@ -826,18 +1088,18 @@ bool use_head_warps(int num_seqs, int units, int own_max, int partition) {
     return (long long)num_seqs * ((units + kWarps - 1) / kWarps) * parts >= 2LL * device_sms();
 }
 
-template <int D, typename OutT, bool kHeadWarps, bool kFp8>
+template <int D, typename OutT, bool kHeadWarps>
 int launch_bf16_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
-    constexpr int bytes = DecodeSmem<D, kFp8>::kBytes;
+    constexpr int bytes = DecodeSmem<D>::kBytes;
     // set once per device (setting it twice from racing host threads is harmless)
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         // two thread blocks per SM: the largest shared-memory carve-out
-        if (cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps, kFp8>,
+        if (cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
-            cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps, kFp8>,
+            cudaFuncSetAttribute(decode_bf16_kernel<D, OutT, kHeadWarps>,
                                  cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return pkv::check_launch("decode: set shared memory size");
@@ -848,15 +1110,39 @@ int launch_bf16_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
     dim3 grid((unsigned)(kHeadWarps ? (units + kWarps - 1) / kWarps : units), (unsigned)num_seqs,
               (unsigned)(p.max_parts - (p.prefix_len ? 1 : 0)));
     cudaError_t e =
-        pkv::launch_dependent(decode_bf16_kernel<D, OutT, kHeadWarps, kFp8>, grid, dim3(kThreads), bytes, st, p);
+        pkv::launch_dependent(decode_bf16_kernel<D, OutT, kHeadWarps>, grid, dim3(kThreads), bytes, st, p);
     if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "decode_bf16: %s", cudaGetErrorString(e));
     return pkv::check_launch("decode_bf16");
 }
 
-template <int D, typename OutT, bool kFp8 = false>
+template <int D, typename OutT>
 int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
-    return p.head_warps ? launch_bf16_variant<D, OutT, true, kFp8>(p, num_seqs, st)
-                        : launch_bf16_variant<D, OutT, false, kFp8>(p, num_seqs, st);
+    return p.head_warps ? launch_bf16_variant<D, OutT, true>(p, num_seqs, st)
+                        : launch_bf16_variant<D, OutT, false>(p, num_seqs, st);
+}
+
+template <typename OutT, bool kHeadWarps>
+int launch_fp8_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
+    constexpr int bytes = Fp8Smem::kBytes;
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
+        // four thread blocks per SM: the largest shared-memory carve-out
+        if (cudaFuncSetAttribute(decode_fp8_kernel<OutT, kHeadWarps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 bytes) != cudaSuccess ||
+            cudaFuncSetAttribute(decode_fp8_kernel<OutT, kHeadWarps>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return pkv::check_launch("decode_fp8: set shared memory size");
+        attr_set[dev].store(true, std::memory_order_release);
+    }
+    const int units = p.num_kv_heads * p.head_chunks;
+    dim3 grid((unsigned)(kHeadWarps ? (units + kWarps - 1) / kWarps : units), (unsigned)num_seqs,
+              (unsigned)p.max_parts);
+    cudaError_t e = pkv::launch_dependent(decode_fp8_kernel<OutT, kHeadWarps>, grid, dim3(kThreads), bytes, st, p);
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "decode_fp8: %s", cudaGetErrorString(e));
+    return pkv::check_launch("decode_fp8");
 }
 
 template <typename T, typename OutT>
@@ -872,7 +1158,8 @@ int launch_decode(const DecodeParams &p, int num_seqs, int D, int dtype, cudaStr
     if (dtype == PKV_BF16) {
         rc = D == 128 ? launch_bf16<128, OutT>(p, num_seqs, st) : launch_bf16<64, OutT>(p, num_seqs, st);
     } else if (dtype == PKV_FP8_E4M3) {
-        rc = launch_bf16<128, OutT, true>(p, num_seqs, st);
+        rc = p.head_warps ? launch_fp8_variant<OutT, true>(p, num_seqs, st)
+                          : launch_fp8_variant<OutT, false>(p, num_seqs, st);
     } else {
         rc = launch_core<float, OutT>(p, num_seqs, D, st);
     }
@@ -913,6 +1200,19 @@ extern "C" int pkv_decode_partition_size(int num_seqs, int num_kv_heads, int max
     return PKV_OK;
 }
 
+extern "C" int pkv_decode_partition_size_fp8(int num_seqs, int num_q_heads, int num_kv_heads, int max_context_len,
+                                             int partition_size, int *out) {
+    int part;
+    int rc = resolve_partition(partition_size, &part);
+    if (rc) return rc;
+    if (!out || num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        max_context_len < 0)
+        return pkv::fail(PKV_ERR_INVALID, "decode_partition_size_fp8: bad argument");
+    const int units = num_kv_heads * ((num_q_heads / num_kv_heads + kRows8 - 1) / kRows8);
+    *out = partition_size == 0 ? fp8_partition(num_seqs, units, num_kv_heads, max_context_len) : part;
+    return PKV_OK;
+}
+
 namespace {
 
 int decode_impl(const void *q, const void *k_new, const void *v_new, const void *k_cache, const void *v_cache,
@@ -944,7 +1244,11 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
     if (!(scale == scale)) return pkv::fail(PKV_ERR_INVALID, "decode: scale is NaN");
     if (num_seqs == 0) return PKV_OK;
     if (num_seqs > 65535) return pkv::fail(PKV_ERR_INVALID, "decode: at most 65535 sequences per call");
-    if (partition_size == 0) part = adaptive_partition(num_seqs, num_kv_heads, max_context_len);
+    if (partition_size == 0)
+        part = dtype == PKV_FP8_E4M3
+                   ? fp8_partition(num_seqs, num_kv_heads * ((num_q_heads / num_kv_heads + kRows8 - 1) / kRows8),
+                                   num_kv_heads, max_context_len)
+                   : adaptive_partition(num_seqs, num_kv_heads, max_context_len);
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return pkv::fail(PKV_ERR_INVALID, "decode: null pointer");
     if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) || !pkv::aligned16(out))
@@ -961,7 +1265,9 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
     p.group = num_q_heads / num_kv_heads;
-    p.head_chunks = (p.group + kRows - 1) / kRows;
+    // query rows per unit: 16 for the bf16 kernel, 8 for the fp8 one
+    const int unit_rows = dtype == PKV_FP8_E4M3 ? kRows8 : kRows;
+    p.head_chunks = (p.group + unit_rows - 1) / unit_rows;
     p.num_blocks = num_blocks;
     const long long cap = (long long)max_blocks_per_seq * kBlock;
     p.len_cap = (int)(cap < max_context_len ? cap : max_context_len);

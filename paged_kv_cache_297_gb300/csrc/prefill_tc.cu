@@ -926,19 +926,6 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 
-// A fresh 64-bit tag per launch: the splitmix64 finaliser of a per-process
-// starting point (the clock and an address) plus a launch count.
-unsigned long long next_launch_tag() {
-    static const unsigned long long salt =
-        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() ^
-        (unsigned long long)reinterpret_cast<uintptr_t>(&g_wait_ns);
-    static std::atomic<unsigned long long> count{0};
-    unsigned long long x = salt + 0x9e3779b97f4a7c15ull * (count.fetch_add(1) + 1);
-    x = (x ^ (x >> 30)) * 0xbf58476d1ce4e5b9ull;
-    x = (x ^ (x >> 27)) * 0x94d049bb133111ebull;
-    return x ^ (x >> 31);
-}
-
 void encode_once();
 
 // 2-D view of one cache: [num_blocks * num_kv_heads * 16 rows][128 columns]
@@ -1070,7 +1057,7 @@ int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaS
     if (pp.num_items == 0) return PKV_OK;
     if (reinterpret_cast<uintptr_t>(pp.item_counter) & 15u)
         return fail(PKV_ERR_INVALID, "prefill: the workspace must be 16-byte aligned");
-    pp.launch_tag = next_launch_tag();
+    pp.launch_tag = pkv::next_launch_tag();
     return out_dtype == PKV_F32 ? launch_typed<float>(pp, tq, tk, tv, st)
                                 : launch_typed<__nv_bfloat16>(pp, tq, tk, tv, st);
 }

@@ -3,6 +3,7 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <chrono>
 
 #include "common.cuh"
 #include "prefill_common.cuh"
@@ -19,6 +20,19 @@ thread_local char g_err[512];
 }  // namespace
 
 namespace pkv {
+
+// A fresh 64-bit tag per launch: the splitmix64 finaliser of a per-process
+// starting point (the clock and an address) plus a launch count.
+unsigned long long next_launch_tag() {
+    static const unsigned long long salt =
+        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() ^
+        (unsigned long long)reinterpret_cast<uintptr_t>(&g_status_addr);
+    static std::atomic<unsigned long long> count{0};
+    unsigned long long x = salt + 0x9e3779b97f4a7c15ull * (count.fetch_add(1) + 1);
+    x = (x ^ (x >> 30)) * 0xbf58476d1ce4e5b9ull;
+    x = (x ^ (x >> 27)) * 0x94d049bb133111ebull;
+    return x ^ (x >> 31);
+}
 
 unsigned *status_ptr() {
     int dev = 0;

@@ -96,6 +96,22 @@ def test_decode_partition_choice(lib):
         pkv.decode_partition_size(1, 8, 100, 24)
 
 
+def test_decode_partition_choice_fp8(lib):
+    # the fp8 kernel (four blocks of 4 warps per SM) leaves a batch unsplit
+    # when its (sequence, unit) pairs fill 2..4 blocks per SM; with 148 SMs
+    # (no device) that is 296..592 units
+    assert pkv.decode_partition_size_fp8(64, 32, 8, 4096) == 4096       # 512 units
+    assert pkv.decode_partition_size_fp8(64, 32, 8, 4090) == 4096       # rounded up to 16
+    assert pkv.decode_partition_size_fp8(8, 64, 8, 131072) == 3072      # 64 units: split
+    assert pkv.decode_partition_size_fp8(256, 32, 8, 2560) == 3072      # 2048 units: split
+    assert pkv.decode_partition_size_fp8(32, 128, 8, 4096) == 4096      # group 16: 2 units per kv head
+    assert pkv.decode_partition_size_fp8(64, 32, 8, 4096, 256) == 256   # explicit
+    # unsplit needs no workspace; the partition-0 workspace still covers it
+    assert pkv.decode_workspace_bytes(64, 32, 128, 4096, 4096) == 0
+    with pytest.raises(pkv.PkvError):
+        pkv.decode_partition_size_fp8(1, 12, 8, 100)
+
+
 @pytest.mark.parametrize("bad", ["block_size", "head_dim", "dtype", "heads"])
 def test_host_rejects_bad_arguments(lib, bad):
     P = ctypes.c_void_p
