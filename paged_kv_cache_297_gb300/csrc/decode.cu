@@ -459,6 +459,316 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
 }
 
 // ----------------------------------------------------------------------------
+// bf16 decode with the products transposed (query groups of at most 8)
+// ----------------------------------------------------------------------------
+// S^T = K q^T and O^T = V^T P^T, as in the fp8 kernel below: the block's 16
+// tokens are the M side of each m16n8k16 product and the unit's (at most 8)
+// query rows its N side, which halves the products and the exponentials per
+// block against the layout with the queries on the M side when a kv head
+// has 4 or 8 query heads.  K reaches the A fragments by ldmatrix, V^T by
+// ldmatrix.trans; q^T is read from global memory as B fragments once; P^T
+// goes from the score accumulator to B fragments by one 8x8 transpose in
+// registers per 8 tokens, as two bf16 halves (hi + lo, about 16 significant
+// bits, as in the bf16 kernel above).  The state of the rows leaves through
+// shared memory, so every row is written out (or merged) contiguously.
+constexpr int kRows8 = 8;  // query rows of one unit of the transposed kernels
+
+template <int D>
+struct DecodeTSmem {
+    static constexpr int kRing = kStages;
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kTile = kBlock * kRowBytes;
+    static constexpr int kStage = 2 * kTile;
+    static constexpr int kWarp = kRing * kStage;
+    static constexpr int kStaging = kWarps * kWarp;
+    static constexpr int kStride = D + 4;                  // floats per staged row
+    static constexpr int kStateWarp = 8 * kStride + 16;    // O rows, then m[8], l[8]
+    static constexpr int kState = kWarps * kStateWarp * 4;
+    static constexpr int kBytes = kStaging > kState ? kStaging : kState;
+};
+
+__device__ __forceinline__ uint32_t transpose8x8_b16(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+    return d;
+}
+
+template <int D, typename OutT, bool kHeadWarps>
+__global__ void __launch_bounds__(kThreads, 2) decode_bf16t_kernel(const DecodeParams p) {
+    using Sm = DecodeTSmem<D>;
+    constexpr int CH = Sm::kRowBytes / 16;    // 16-byte chunks per cached row
+    constexpr int PER_LANE = kBlock * CH / 32;
+    constexpr int KSTEPS = D / 16, MT = D / 16;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    pkv::allow_dependents();
+    if (!p.overlap_prev) pkv::grid_dependency_wait();  // the appended tokens of the previous launch
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int unit = kHeadWarps ? blockIdx.x * kWarps + warp : blockIdx.x;
+    const bool idle = kHeadWarps && unit >= p.num_kv_heads * p.head_chunks;
+    const int kvh = unit / p.head_chunks, chunk = unit - kvh * p.head_chunks;
+    const int s = blockIdx.y, part = blockIdx.z;
+    const int32_t *table = p.block_tables + (size_t)s * p.max_blocks;
+    const int blk_begin = (p.prefix_len + part * p.partition) / kBlock;
+    const int bstride = kHeadWarps ? 1 : kWarps;
+    const int bfirst = blk_begin + (kHeadWarps ? 0 : warp);
+    int my_id = 0;
+    if (!idle && bfirst + bstride * lane < p.max_blocks) my_id = table[bfirst + bstride * lane];
+
+    const int L = clamp_len(p.context_lens[s], p.len_cap, p.status,
+                            part == 0 && blockIdx.x == 0 && threadIdx.x == 0);
+    if (p.prefix_len && L <= p.prefix_len && part == 0 && blockIdx.x == 0 && threadIdx.x == 0)
+        pkv::flag(p.status, PKV_STATUS_BAD_LENGTH);  // no private token after the shared prefix
+    const int nparts = own_parts(p, L);
+    const bool tail_wait = p.overlap_prev && blockIdx.x == gridDim.x - 1 &&
+                           blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1;
+    if (part >= nparts || idle) {
+        if (tail_wait) pkv::grid_dependency_wait();
+        return;
+    }
+    const int slot0 = p.prefix_len ? 1 : 0;  // partial slot 0 holds the shared prefix
+    const int nslots = slot0 + nparts;
+
+    const int h0 = kvh * p.group + chunk * kRows8;
+    const int rows = min(kRows8, p.group - chunk * kRows8);
+    const int t_begin = p.prefix_len + part * p.partition;
+    const int t_end = min(L, t_begin + p.partition);
+    const int nblk = (t_end + kBlock - 1) / kBlock - blk_begin;
+    const int n = kHeadWarps ? nblk : max(0, (nblk - warp + kWarps - 1) / kWarps);
+    const unsigned char *kc = static_cast<const unsigned char *>(p.k_cache);
+    const unsigned char *vc = static_cast<const unsigned char *>(p.v_cache);
+
+    // q^T as B fragments: query row gid of the unit (zero past `rows`),
+    // d = 16 kk + 2 tig + {0, 1} and + 8
+    uint32_t qb[KSTEPS][2];
+    {
+        const bool ok = gid < rows;
+        const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(p.q) +
+                                    ((size_t)s * p.num_q_heads + h0 + (ok ? gid : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; kk++) {
+            qb[kk][0] = ok ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tig) : 0u;
+            qb[kk][1] = ok ? *reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tig + 8) : 0u;
+        }
+    }
+    const float sl2 = p.scale_log2;
+
+    if (p.k_new && part == nparts - 1 && L > 0) {
+        // the new row is read below through L2 by other threads
+        if (kHeadWarps) {
+            append_new_token<__nv_bfloat16>(p, table, s, kvh, L, D, lane, 32);
+            __syncwarp();
+        } else {
+            append_new_token<__nv_bfloat16>(p, table, s, kvh, L, D, threadIdx.x, kThreads);
+            __syncthreads();
+        }
+    }
+
+    unsigned char *ring = smem + warp * Sm::kWarp;
+    auto block_id = [&](int li) -> int {
+        return li < 32 ? __shfl_sync(0xffffffffu, my_id, li) : table[bfirst + bstride * li];
+    };
+    auto block_rows = [&](int li, int &phys) -> int {
+        phys = block_id(li);
+        if (phys < 0 || phys >= p.num_blocks) return -1;
+        return min(kBlock, t_end - (bfirst + bstride * li) * kBlock);
+    };
+    auto issue = [&](int li, int st) {
+        int phys;
+        int valid = block_rows(li, phys);
+        if (valid < 0) {
+            if (lane == 0) pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+            valid = 0;
+            phys = 0;
+        }
+        const size_t base = ((size_t)phys * p.num_kv_heads + kvh) * Sm::kTile;
+        unsigned char *ks = ring + st * Sm::kStage;
+#pragma unroll
+        for (int j = 0; j < PER_LANE; j++) {
+            const int i = lane + 32 * j;
+            const int r = i / CH, c = i - (i / CH) * CH;
+            const int nb = r < valid ? 16 : 0;
+            const int go = nb ? r * Sm::kRowBytes + c * 16 : 0;
+            pkv::cp_async16(ks + pkv::swz(r, c, Sm::kRowBytes), kc + base + go, nb);
+            pkv::cp_async16(ks + Sm::kTile + pkv::swz(r, c, Sm::kRowBytes), vc + base + go, nb);
+        }
+    };
+
+    float o[MT][4];
+#pragma unroll
+    for (int i = 0; i < MT; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    // running max and this thread's part of the sum, query rows 2 tig, 2 tig + 1
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+#pragma unroll
+    for (int st = 0; st < Sm::kRing - 1; st++) {
+        if (st < n) issue(st, st);
+        pkv::cp_async_commit();
+    }
+    // ldmatrix row addresses: K as A (matrix j = lane / 8: tokens 8 (j & 1) ..,
+    // column chunk 2 kk + j / 2), V as A of V^T (tokens 8 (j / 2) .., column
+    // chunk 2 mt + (j & 1))
+    const int ktok = ((lane >> 3) & 1) * 8 + (lane & 7), kch = lane >> 4;
+    const int vtok = (lane >> 4) * 8 + (lane & 7), vch = (lane >> 3) & 1;
+    for (int i = 0; i < n; i++) {
+        {
+            const int nx = i + Sm::kRing - 1;
+            if (nx < n) issue(nx, nx % Sm::kRing);
+            pkv::cp_async_commit();
+        }
+        pkv::cp_async_wait<Sm::kRing - 1>();
+        __syncwarp();
+        const unsigned char *ks = ring + (i % Sm::kRing) * Sm::kStage;
+        const unsigned char *vs = ks + Sm::kTile;
+        int phys;
+        int valid = block_rows(i, phys);
+        if (valid < 0) valid = 0;
+
+        // S^T: c[0], c[1] token gid, rows 2 tig, 2 tig + 1; c[2], c[3] token gid + 8
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; kk++) {
+            uint32_t a[4];
+            pkv::ldsm_x4(a[0], a[1], a[2], a[3], ks + pkv::swz(ktok, 2 * kk + kch, Sm::kRowBytes));
+            pkv::mma_bf16(c, a, qb[kk][0], qb[kk][1]);
+        }
+        const float x0 = gid < valid ? c[0] * sl2 : -INFINITY;
+        const float x1 = gid < valid ? c[1] * sl2 : -INFINITY;
+        const float x2 = gid + 8 < valid ? c[2] * sl2 : -INFINITY;
+        const float x3 = gid + 8 < valid ? c[3] * sl2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        // the running maximum moves only when a row's scores pass it by more
+        // than 2^8; P <= 256 then, and O, l are rescaled rarely
+        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float al0 = pkv::fast_exp2(m0 - (n0 == -INFINITY ? 0.f : n0));
+            const float al1 = pkv::fast_exp2(m1 - (n1 == -INFINITY ? 0.f : n1));
+            m0 = n0;
+            m1 = n1;
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int mt = 0; mt < MT; mt++) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+        }
+        const float base0 = m0 == -INFINITY ? 0.f : m0, base1 = m1 == -INFINITY ? 0.f : m1;
+        const float p0 = pkv::fast_exp2(x0 - base0), p1 = pkv::fast_exp2(x1 - base1);
+        const float p2 = pkv::fast_exp2(x2 - base0), p3 = pkv::fast_exp2(x3 - base1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        // P^T as B fragments (hi and lo halves): {P[row gid][token 2 tig],
+        // [2 tig + 1]} and the same 8 tokens later
+        float h0f, h1f, h2f, h3f, q0, q1, q2, q3;
+        pkv::split_bf16(p0, h0f, q0);
+        pkv::split_bf16(p1, h1f, q1);
+        pkv::split_bf16(p2, h2f, q2);
+        pkv::split_bf16(p3, h3f, q3);
+        const uint32_t ph0 = transpose8x8_b16(pkv::pack_bf16(h0f, h1f));
+        const uint32_t ph1 = transpose8x8_b16(pkv::pack_bf16(h2f, h3f));
+        const uint32_t pl0 = transpose8x8_b16(pkv::pack_bf16(q0, q1));
+        const uint32_t pl1 = transpose8x8_b16(pkv::pack_bf16(q2, q3));
+
+        // O^T += V^T P^T: m-tile mt is d = 16 mt .. 16 mt + 15
+#pragma unroll
+        for (int mt = 0; mt < MT; mt++) {
+            uint32_t a[4];
+            pkv::ldsm_x4_t(a[0], a[1], a[2], a[3], vs + pkv::swz(vtok, 2 * mt + vch, Sm::kRowBytes));
+            pkv::mma_bf16(o[mt], a, ph0, ph1);
+            pkv::mma_bf16(o[mt], a, pl0, pl1);
+        }
+        __syncwarp();
+    }
+    pkv::cp_async_wait<0>();
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+
+    // stage the warp's state in shared memory: O rows [8][D] (o[mt][2h + e]
+    // is row 2 tig + e, column 16 mt + gid + 8 h), then m[8], l[8]
+    if (!kHeadWarps) __syncthreads();  // every warp is done with its ring
+    float *sw = reinterpret_cast<float *>(kHeadWarps ? ring : smem) + (kHeadWarps ? 0 : warp * Sm::kStateWarp);
+    __syncwarp();
+#pragma unroll
+    for (int mt = 0; mt < MT; mt++)
+#pragma unroll
+        for (int h = 0; h < 2; h++)
+#pragma unroll
+            for (int e = 0; e < 2; e++) sw[(2 * tig + e) * Sm::kStride + 16 * mt + gid + 8 * h] = o[mt][2 * h + e];
+    if (gid == 0) {
+        sw[8 * Sm::kStride + 2 * tig] = m0;
+        sw[8 * Sm::kStride + 2 * tig + 1] = m1;
+        sw[8 * Sm::kStride + 8 + 2 * tig] = l0;
+        sw[8 * Sm::kStride + 8 + 2 * tig + 1] = l1;
+    }
+
+    if (kHeadWarps) {
+        __syncwarp();
+        // lane: 4 consecutive columns of a row per pass
+        for (int idx = lane; idx < rows * (D / 4); idx += 32) {
+            const int r = idx / (D / 4), c = (idx - r * (D / 4)) * 4;
+            const float4 v = *reinterpret_cast<const float4 *>(sw + r * Sm::kStride + c);
+            const float m = sw[8 * Sm::kStride + r], l = sw[8 * Sm::kStride + 8 + r];
+            const size_t orow = (size_t)s * p.num_q_heads + h0 + r;
+            if (nslots == 1) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                OutT *op = static_cast<OutT *>(p.out) + orow * D + c;
+                pkv::store2(op, v.x * inv, v.y * inv);
+                pkv::store2(op + 2, v.z * inv, v.w * inv);
+            } else {
+                const size_t prow = orow * p.max_parts + slot0 + part;
+                *reinterpret_cast<float4 *>(p.part_o + prow * D + c) = v;
+                if (c == 0) *reinterpret_cast<float2 *>(p.part_ml + prow * 2) = make_float2(m, l);
+            }
+        }
+        if (tail_wait) pkv::grid_dependency_wait();
+        return;
+    }
+
+    __syncthreads();
+    const float *base = reinterpret_cast<const float *>(smem);
+    for (int idx = threadIdx.x; idx < rows * D; idx += kThreads) {
+        const int r = idx / D, col = idx - (idx / D) * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; w++) M = fmaxf(M, base[w * Sm::kStateWarp + 8 * Sm::kStride + r]);
+        float acc = 0.f, lsum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; w++) {
+                const float *bw = base + w * Sm::kStateWarp;
+                const float f = pkv::fast_exp2(bw[8 * Sm::kStride + r] - M);
+                lsum += bw[8 * Sm::kStride + 8 + r] * f;
+                acc += bw[r * Sm::kStride + col] * f;
+            }
+        }
+        const size_t orow = (size_t)s * p.num_q_heads + h0 + r;
+        if (nslots == 1) {
+            pkv::store1(static_cast<OutT *>(p.out) + orow * D + col, lsum > 0.f ? acc / lsum : 0.f);
+        } else {
+            const size_t prow = orow * p.max_parts + slot0 + part;
+            p.part_o[prow * D + col] = acc;
+            if (col == 0) {
+                p.part_ml[prow * 2] = M;
+                p.part_ml[prow * 2 + 1] = lsum;
+            }
+        }
+    }
+    if (tail_wait) pkv::grid_dependency_wait();
+}
+
+// ----------------------------------------------------------------------------
 // fp8 decode with the operands swapped
 // ----------------------------------------------------------------------------
 // The scores are computed transposed, S^T = K q^T, and the output as
@@ -480,7 +790,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(const DecodePa
 //    consecutive output columns of query rows 2 tig and 2 tig + 1;
 //  - P^T reaches the B fragments through one 8x8 transpose (movmatrix) per
 //    8 tokens of the score accumulator.
-constexpr int kRows8 = 8;  // query rows of one fp8 unit
 
 struct Fp8Smem {
     static constexpr int kRing = 3;                        // blocks per warp ring
@@ -494,12 +803,6 @@ struct Fp8Smem {
     static constexpr int kMerge = kWarps * kMergeWarp * 4;
     static constexpr int kBytes = kStaging > kMerge ? kStaging : kMerge;
 };
-
-__device__ __forceinline__ uint32_t transpose8x8_b16(uint32_t a) {
-    uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
-    return d;
-}
 
 template <typename OutT, bool kHeadWarps>
 __global__ void __launch_bounds__(kThreads, 4) decode_fp8_kernel(const DecodeParams p) {
@@ -1115,8 +1418,38 @@ int launch_bf16_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
     return pkv::check_launch("decode_bf16");
 }
 
+template <int D, typename OutT, bool kHeadWarps>
+int launch_bf16t_variant(const DecodeParams &p, int num_seqs, cudaStream_t st) {
+    constexpr int bytes = DecodeTSmem<D>::kBytes;
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(decode_bf16t_kernel<D, OutT, kHeadWarps>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+            cudaFuncSetAttribute(decode_bf16t_kernel<D, OutT, kHeadWarps>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return pkv::check_launch("decode: set shared memory size");
+        attr_set[dev].store(true, std::memory_order_release);
+    }
+    const int units = p.num_kv_heads * p.head_chunks;
+    // (with a shared prefix, partial slot 0 comes from another kernel)
+    dim3 grid((unsigned)(kHeadWarps ? (units + kWarps - 1) / kWarps : units), (unsigned)num_seqs,
+              (unsigned)(p.max_parts - (p.prefix_len ? 1 : 0)));
+    cudaError_t e =
+        pkv::launch_dependent(decode_bf16t_kernel<D, OutT, kHeadWarps>, grid, dim3(kThreads), bytes, st, p);
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "decode_bf16t: %s", cudaGetErrorString(e));
+    return pkv::check_launch("decode_bf16t");
+}
+
+// Query groups of at most 8 heads per kv head (one unit of 8 rows) take the
+// transposed kernel, larger groups the one with the queries on the M side.
 template <int D, typename OutT>
 int launch_bf16(const DecodeParams &p, int num_seqs, cudaStream_t st) {
+    if (p.group <= kRows8)
+        return p.head_warps ? launch_bf16t_variant<D, OutT, true>(p, num_seqs, st)
+                            : launch_bf16t_variant<D, OutT, false>(p, num_seqs, st);
     return p.head_warps ? launch_bf16_variant<D, OutT, true>(p, num_seqs, st)
                         : launch_bf16_variant<D, OutT, false>(p, num_seqs, st);
 }
