@@ -289,6 +289,17 @@ DECODE_SOURCES = ("common.cuh", "decode.cu")
 CASCADE_SOURCES = DECODE_SOURCES + ("prefill_common.cuh", "prefill_tc.cu", "tcgen05.cuh")
 
 
+def sleep_ahead(ms: float) -> None:
+    """Keep the current stream busy for about `ms` milliseconds (a spin
+    kernel of torch's; nothing of this library runs)."""
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is None or ms <= 0:
+        return
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    mhz = getattr(props, "clock_rate", 0) / 1e3  # kHz -> MHz
+    sleep(int(ms * 1e3 * (mhz if mhz > 0 else 2070.0)))
+
+
 def time_device(step: Step, steps: int, warmup: int, world: int):
     """Two timed passes of `steps` steps each.  The throughput pass records an
     event only before the first and after the last step, so consecutive
@@ -318,6 +329,12 @@ def time_device(step: Step, steps: int, warmup: int, world: int):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
           for _ in range(steps)]
     torch.cuda.synchronize()
+    # The host needs about as long to enqueue a short step with its events as
+    # the GPU needs to run it; an idle gap between an event and the launch
+    # after it would count as call time.  A device-side sleep ahead of the
+    # loop (as long as the throughput pass, at most 200 ms) lets the host
+    # queue steps while the GPU is busy, so the events time only the calls.
+    sleep_ahead(min(200.0, span_ms))
     for i in range(steps):
         ev[i][0].record(stream)
         for j, (_, fn) in enumerate(calls):
@@ -526,7 +543,8 @@ def step_rooflines(step: Step, per_call: dict, peaks: dict, workload: str):
                            "decode_step (fused append + partition kernel + log-sum-exp reduce)"
                            if step.fused else
                            "paged_attention_decode_fp8 (fp8 E4M3 cache widened to fp16 in registers, "
-                           "fp16 tile products; partition kernel + log-sum-exp reduce)" if step.fp8 else
+                           "transposed fp16 tile products; one wave without a split when it covers the "
+                           "batch, else partitions + log-sum-exp reduce)" if step.fp8 else
                            "paged_attention_decode (partition kernel + log-sum-exp reduce)"),
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
