@@ -369,7 +369,7 @@ extern "C" int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_
     if (!bytes || num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         max_q_len < 0 || max_context_len < 0 || (head_dim != 64 && head_dim != 128))
         return pkv::fail(PKV_ERR_INVALID, "prefill_workspace_bytes: bad argument");
-    // the tcgen05 path's work-item counter (16 bytes, in a 256-byte block)
+    // the tcgen05 path's work-item counters (32 bytes, in a 256-byte block)
     *bytes = head_dim == 128 ? 256 : 0;
     return PKV_OK;
 }

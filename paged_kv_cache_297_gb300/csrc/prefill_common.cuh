@@ -25,8 +25,9 @@ struct PrefillParams {
     float scale_log2;
     unsigned *status;
     // tcgen05 kernel only: persistent CTA pairs take (sequence, q tile, kv
-    // head) items from a counter in the workspace: 16 bytes, 16-byte
-    // aligned, {launch tag, count}, set by the kernel itself
+    // head) items from a counter in the workspace: 32 bytes, 16-byte
+    // aligned, {launch tag, items taken} and {launch tag, CTAs done}, kept
+    // by the kernel itself (the last CTA clears both tags)
     int num_seqs;
     int tiles_per_seq;
     int num_items;

@@ -220,6 +220,33 @@ __device__ __forceinline__ int next_item(const PrefillParams &p) {
     return item < (unsigned long long)p.num_items ? (int)item : 0x7fffffff;
 }
 
+// Count this CTA's exit in the second pair of the workspace counter,
+// {launch tag, CTAs done}, installed like the first.  The launch's last CTA
+// clears both tags, so the next launch installs its own pairs even when it
+// carries this launch's tag: a launch replayed from a CUDA graph keeps the
+// parameters, tag included, that it was captured with.  (By then every CTA
+// has made its last fetch from the first pair.)
+__device__ __forceinline__ void count_exit(const PrefillParams &p) {
+    unsigned long long *c = p.item_counter + 2;
+    const unsigned long long tag = p.launch_tag;
+    unsigned long long t = *reinterpret_cast<volatile unsigned long long *>(c);
+    if (t != tag) {
+        unsigned long long cnt = *reinterpret_cast<volatile unsigned long long *>(c + 1);
+        for (int tries = 0; tries < 64 && t != tag; tries++) {
+            unsigned long long ot, oc;
+            cas128(c, t, cnt, tag, 0ull, ot, oc);
+            if (ot == t && oc == cnt) break;  // installed
+            t = ot;
+            cnt = oc;
+        }
+    }
+    const unsigned long long k = atomicAdd(c + 1, 1ull);
+    if (k == (unsigned long long)gridDim.x - 1) {
+        atomicExch(p.item_counter, 0ull);
+        atomicExch(c, 0ull);
+    }
+}
+
 // Item (sequence, pair tile, kv head) as published in the shared-memory
 // queue: (item, q0, n, L); every role of both CTAs derives the rest.
 struct ItemInfo {
@@ -910,6 +937,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc::cluster_sync();
     tc::fence_after_sync();
     if (warp == 0 && !misaligned) tc::tmem_dealloc_pair(tmem, kTmemCols);
+    // every role of the pair has passed its last item fetch
+    if (tid == 0) count_exit(p);
 }
 
 }  // namespace
@@ -1058,6 +1087,7 @@ int launch_prefill_tc(const PrefillParams &p, int num_seqs, int out_dtype, cudaS
     if (reinterpret_cast<uintptr_t>(pp.item_counter) & 15u)
         return fail(PKV_ERR_INVALID, "prefill: the workspace must be 16-byte aligned");
     pp.launch_tag = pkv::next_launch_tag();
+    if (pp.launch_tag == 0) pp.launch_tag = 1;  // 0 marks a cleared counter
     return out_dtype == PKV_F32 ? launch_typed<float>(pp, tq, tk, tv, st)
                                 : launch_typed<__nv_bfloat16>(pp, tq, tk, tv, st);
 }

@@ -405,11 +405,12 @@ def make_batch(name: str, poison: bool = True, seed: Optional[int] = None, **kw)
     """Draw the named workload.  ``poison`` fills every cache row that holds no
     token with NaN so that any over-read shows up as a non-finite output."""
     spec = SPECS[name]
-    if "num_seqs" in kw or "ctx" in kw:
+    if "num_seqs" in kw or "ctx" in kw or "heads" in kw:
         from dataclasses import replace
         ctx = kw.pop("ctx", (spec.ctx_lo, spec.ctx_hi))
+        hq, hkv = kw.pop("heads", (spec.num_q_heads, spec.num_kv_heads))
         spec = replace(spec, num_seqs=kw.pop("num_seqs", spec.num_seqs),
-                       ctx_lo=ctx[0], ctx_hi=ctx[1])
+                       ctx_lo=ctx[0], ctx_hi=ctx[1], num_q_heads=hq, num_kv_heads=hkv)
     seed = SEED_BASE + spec.index if seed is None else seed
     if name == "shared_prefix_cow":
         b = _shared_prefix_batch(spec, seed, poison, **kw)

@@ -414,6 +414,68 @@ def _prefill_call(b, t, out):
         max_context_len=int(b.prefill_context_lens.max()))
 
 
+def _replay_checks(call, out, expected, dtype, what, replays=3):
+    # capture one call in a CUDA graph (after one plain call: attributes and
+    # occupancy queries happen outside the capture), then replay it with the
+    # output cleared each time
+    call()
+    torch.cuda.synchronize()
+    assert pkv.get_status() == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for rep in range(replays):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert pkv.get_status() == 0, (what, rep)
+        assert_parity(out, expected, dtype, f"{what}, graph replay {rep}")
+
+
+def test_prefill_replays_from_a_cuda_graph():
+    # A graph replays a launch with the parameters it was captured with, the
+    # work counter's launch tag included: every replay must still hand out
+    # all of its items (the kernel clears the counter's tags when it ends).
+    b = W.custom_prefill("bf16", 32, 8, 128, [0, 3072], [512, 512], seed=37)
+    _, _, _, pout_o = oracle_step(b)
+    t = to_dev(b)
+    pkv.kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"])
+    cu = b.prefill_cu_q_lens
+    mq, mc = int((cu[1:] - cu[:-1]).max()), int(b.prefill_context_lens.max())
+    ws = torch.empty(max(1, pkv.prefill_workspace_bytes(int(cu.numel()) - 1, b.prefill_q.shape[0], 32, 8, 128,
+                                                         mq, mc)), dtype=torch.uint8, device="cuda")
+    out = torch.empty(b.prefill_q.shape, dtype=torch.float32, device="cuda")
+
+    def call():
+        pkv.paged_attention_prefill_chunk(
+            t["prefill_q"], t["prefill_cu_q_lens"], t["k_cache"], t["v_cache"], t["prefill_block_tables"],
+            t["prefill_context_lens"], b.scale, out, max_q_len=mq, max_context_len=mc, workspace=ws)
+
+    _replay_checks(call, out, pout_o, b.dtype, "prefill")
+
+
+def test_shared_prefix_decode_replays_from_a_cuda_graph():
+    # 1024 sequences: 4096 query rows per kv head, 128 prefix items, more
+    # than one per resident CTA pair, so items also come from the counter
+    b = W.make_batch("shared_prefix_cow", num_seqs=1024, ctx=(16, 200), prefix_blocks=8)
+    _, _, out_o, _ = oracle_step(b)
+    t = to_dev(b)
+    pkv.copy_blocks(t["copy_pairs"], t["k_cache"], t["v_cache"])
+    S, Hq, d = b.q.shape
+    P = 8 * 16
+    ws = torch.empty(pkv.decode_shared_prefix_workspace_bytes(S, Hq, d, b.max_context_len, P),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty(b.q.shape, dtype=torch.float32, device="cuda")
+
+    def call():
+        # (the fused append writes the same rows on every replay)
+        pkv.decode_shared_prefix(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
+                                 b.scale, out, P, k_new=t["k_new"], v_new=t["v_new"],
+                                 max_context_len=b.max_context_len, workspace=ws)
+
+    _replay_checks(call, out, out_o, b.dtype, "cascade decode")
+
+
 def test_prefill_wait_limit_runs_out_and_is_reported():
     # The tensor-core kernel's waits are bounded in time.  With a bound of 1 ns
     # a wait runs out at once: the launch must stop, record the internal status
@@ -478,14 +540,18 @@ def test_shared_prefix_cascade_workload(out_dtype):
     assert_parity(out, out_o, b.dtype, "cascade decode")
 
 
-@pytest.mark.parametrize("num_seqs,prefix_blocks,ctx,fused,partition", [
-    (40, 3, (16, 300), True, 0),      # 48-token prefix (one partial key tile), 160 query rows
-    (5, 9, (1, 40), False, 0),        # tiny suffixes, one row tile, append outside
-    (64, 20, (100, 2000), True, 256), # long suffixes split in 256-token partitions
-    (160, 4, (16, 600), True, 256),   # head-warp suffix partitions with partials
+@pytest.mark.parametrize("num_seqs,prefix_blocks,ctx,fused,partition,heads", [
+    (40, 3, (16, 300), True, 0, (32, 8)),       # 48-token prefix (one partial key tile), 160 query rows
+    (5, 9, (1, 40), False, 0, (32, 8)),         # tiny suffixes, one row tile, append outside
+    (64, 20, (100, 2000), True, 256, (32, 8)),  # long suffixes split in 256-token partitions
+    (160, 4, (16, 600), True, 256, (32, 8)),    # head-warp suffix partitions with partials
+    (24, 5, (16, 200), True, 0, (64, 8)),       # group of 8: every row of the transposed tile
+    (48, 6, (1, 700), True, 0, (8, 4)),         # group of 2
+    (20, 7, (10, 500), True, 0, (48, 4)),       # group of 12: the kernel with queries on M
 ])
-def test_shared_prefix_cascade_shapes(num_seqs, prefix_blocks, ctx, fused, partition):
-    b = W.make_batch("shared_prefix_cow", num_seqs=num_seqs, ctx=ctx, prefix_blocks=prefix_blocks)
+def test_shared_prefix_cascade_shapes(num_seqs, prefix_blocks, ctx, fused, partition, heads):
+    b = W.make_batch("shared_prefix_cow", num_seqs=num_seqs, ctx=ctx, prefix_blocks=prefix_blocks,
+                     heads=heads)
     kc_o, vc_o, out_o, _ = oracle_step(b)
     t, out = _cascade_step(b, prefix_blocks * 16, fused=fused, partition=partition)
     assert pkv.get_status() == 0
