@@ -294,7 +294,8 @@ int pkv_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int 
  * sequence's output is undefined).  Other arguments as
  * pkv_paged_attention_decode / pkv_decode_step; workspace of
  * pkv_decode_shared_prefix_workspace_bytes(...) bytes, 256-byte aligned,
- * needing no initialisation.
+ * needing no initialisation (replays of a captured call are fine, as for
+ * pkv_paged_attention_prefill_chunk).
  */
 int pkv_paged_attention_decode_shared_prefix(const void *q, const void *k_new, const void *v_new,
                                              void *k_cache, void *v_cache, const int32_t *block_tables,
@@ -328,7 +329,9 @@ int pkv_prefill_workspace_bytes(int num_seqs, int total_q, int num_q_heads, int 
  *   out        [total_q][num_q_heads][head_dim], out_dtype
  *   workspace  device scratch of pkv_prefill_workspace_bytes(...) bytes,
  *              16-byte aligned; it needs no initialisation (each launch
- *              claims its work counter with a fresh 64-bit tag), and calls
+ *              claims its work counter with a fresh 64-bit tag, and the
+ *              launch's last thread block clears it, so a call captured in
+ *              a CUDA graph may be replayed any number of times), and calls
  *              that overlap on the GPU must not share it.
  * n_s > L_s or n_s > max_q_len sets PKV_STATUS_BAD_QLEN and skips the sequence.
  */
