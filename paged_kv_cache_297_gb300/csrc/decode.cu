@@ -1,9 +1,12 @@
 // Paged-attention decode with split-K partitions and a log-sum-exp reduce.
 //
-// Work unit: one CTA per (kv head [x q-head chunk of 16], sequence, partition of
-// `partition` tokens).  The G = Hq / Hkv query heads that share a kv head form
-// the M = 16 rows of a tensor-core tile, so every K/V byte fetched is used by
-// all G heads (GQA, chengxuchu #47 section 2.3).  The partition's 16-token
+// Work unit: one CTA per (kv head [x q-head chunk], sequence, partition of
+// `partition` tokens).  The G = Hq / Hkv query heads that share a kv head
+// share every K/V byte fetched (GQA, chengxuchu #47 section 2.3): for G <= 8
+// (and for fp8 caches) the block's 16 tokens are the M side of each
+// tensor-core product and the G query rows its N side (decode_bf16t_kernel,
+// decode_fp8_kernel); for larger groups the query rows are the M = 16 side
+// (decode_bf16_kernel).  The partition's 16-token
 // blocks are split between the CTA's 4 warps; each warp streams its blocks
 // through a private ring of shared-memory stages filled by 16-byte cp.async
 // copies, looked up through the block table (section 5.2), and keeps its own
@@ -112,7 +115,7 @@ __device__ __forceinline__ int clamp_len(int L, int cap, unsigned *status, bool 
 }
 
 // ----------------------------------------------------------------------------
-// bf16 tensor-core decode
+// bf16 tensor-core decode, query rows on the M side (groups of 9 to 16 heads)
 // ----------------------------------------------------------------------------
 
 template <int D>
@@ -1093,10 +1096,6 @@ template <typename T>
 __device__ __forceinline__ float ld_elem(const T *p);
 template <>
 __device__ __forceinline__ float ld_elem<float>(const float *p) { return *p; }
-template <>
-__device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16 *p) {
-    return __bfloat162float(*p);
-}
 
 __device__ __forceinline__ float block_reduce(float v, float *red, bool is_max) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
