@@ -115,7 +115,8 @@ __device__ __forceinline__ int clamp_len(int L, int cap, unsigned *status, bool 
 }
 
 // ----------------------------------------------------------------------------
-// bf16 tensor-core decode, query rows on the M side (groups of 9 to 16 heads)
+// bf16 tensor-core decode, query rows on the M side (groups above 8 heads, in
+// chunks of 16)
 // ----------------------------------------------------------------------------
 
 template <int D>
