@@ -300,31 +300,73 @@ def sleep_ahead(ms: float) -> None:
     sleep(int(ms * 1e3 * (mhz if mhz > 0 else 2070.0)))
 
 
+def capture_step(calls):
+    """One step's calls captured in a CUDA graph (the library's launches,
+    programmatic dependencies included), or None if capture is refused."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _, fn in calls:
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+    except Exception as e:  # noqa: BLE001 - fall back to eager dispatch
+        print(f"bench: CUDA graph capture refused ({type(e).__name__}: {e}); timing eager dispatch",
+              file=sys.stderr)
+        torch.cuda.synchronize()
+        return None
+
+
 def time_device(step: Step, steps: int, warmup: int, world: int):
-    """Two timed passes of `steps` steps each.  The throughput pass records an
-    event only before the first and after the last step, so consecutive
-    launches keep their programmatic-dependent overlap; the breakdown pass
-    brackets every call with events (for per-call durations and the
-    roofline), which serialises the calls."""
+    """Timed passes of `steps` steps each.  Throughput: the calls dispatched
+    eagerly through the API, then the same step captured once in a CUDA graph
+    and replayed (as a serving loop dispatches a decode step); each pass
+    records an event only before the first and after the last step, and the
+    faster of the two is the step's time (both are kept in
+    `step.dispatch_ms`).  Eager steps keep the programmatic-dependent overlap
+    of consecutive launches, but a short step's calls can outrun the host's
+    dispatch; a graph replay takes no host time per call but starts each
+    step as a new graph launch.  The breakdown pass calls the API eagerly and
+    brackets every call with events (per-call durations and the roofline),
+    which serialises the calls."""
     calls = step.calls()
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         for _, fn in calls:
             fn()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    e0.record(stream)
-    for _ in range(steps):
+
+    def timed(run_step):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(steps):
+            run_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall_s = time.perf_counter() - t0
+        barrier(world)
+        return e0.elapsed_time(e1), wall_s
+
+    def eager():
         for _, fn in calls:
             fn()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    barrier(world)
-    span_ms = e0.elapsed_time(e1)
+
+    span_ms, wall = timed(eager)
+    step.dispatch, step.dispatch_ms = "eager", {"eager": round(span_ms / steps, 5)}
+    graph = capture_step(calls)
+    dev = f"cuda:{torch.cuda.current_device()}"
+    # every rank takes the same path: graphs only if every rank captured one,
+    # and used only if they are faster on every rank
+    if max_over_ranks(0.0 if graph is not None else 1.0, world, dev) == 0.0:
+        g_ms, g_wall = timed(graph.replay)
+        step.dispatch_ms["cuda_graph"] = round(g_ms / steps, 5)
+        if max_over_ranks(g_ms - span_ms, world, dev) < 0:
+            span_ms, wall, step.dispatch = g_ms, g_wall, "cuda_graph"
+    del graph
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
           for _ in range(steps)]
@@ -582,12 +624,20 @@ def seqs_per_step(batch: W.Batch) -> int:
 # against the bf16 tensor roofline), plus the headline batch itself over a
 # long timed region.
 TARGET_WORKLOADS = ("llama3_8b_decode", "long_context", "mixed_step")
+# Further records on the same line: the same decode batches over fp8 E4M3
+# caches and the shared-prefix (cascade) step, each with its own roofline.
+EXTRA_RECORDS = (("llama3_8b_decode_fp8", "llama3_8b_decode", "fp8"),
+                 ("long_context_fp8", "long_context", "fp8"),
+                 ("shared_prefix_cow", "shared_prefix_cow", "bf16"))
 
 
-def target_record(name: str, dev: str, peaks: dict, args, world: int, min_ms: float = 250.0) -> dict:
+def target_record(name: str, dev: str, peaks: dict, args, world: int, min_ms: float = 250.0,
+                  kv_dtype: str = "bf16") -> dict:
     """One workload's step timed over at least `min_ms` of GPU time (so the
     clock sampler sees it under load), with its rooflines."""
     batch = W.make_batch(name, poison=False)
+    if kv_dtype == "fp8":
+        batch = W.fp8_batch(batch)
     step = Step(batch, dev, args.partition, args.unfused, args.no_cascade)
     calls = step.calls()
     for _ in range(3):
@@ -607,7 +657,8 @@ def target_record(name: str, dev: str, peaks: dict, args, world: int, min_ms: fl
     span_ms, serial_ms, per_call, _, pct = time_device(step, n, 3, world)
     clk = clocks.stop()
     roofline, extra, _ = step_rooflines(step, per_call, peaks, name)
-    rec = {"steps": n, "timed_ms": round(span_ms, 1), "ms_per_step": round(span_ms / n, 5),
+    rec = {"kv_dtype": kv_dtype, "step_dispatch": getattr(step, "dispatch", "eager"),
+           "dispatch_ms_per_step": getattr(step, "dispatch_ms", None), "steps": n, "timed_ms": round(span_ms, 1), "ms_per_step": round(span_ms / n, 5),
            "value": round(world * seqs_per_step(batch) * n / (span_ms / 1e3), 1), "unit": "seq-steps/s",
            "calls_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
            "serial_ms_per_step": round(serial_ms, 5), "roofline": roofline, "clocks": clk}
@@ -657,7 +708,9 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (KV per step %.0f MB > 129 MB L2); no flush"
                          % (db["kv"] / 1e6) if db["kv"] > 129e6 else
                          "working set fits L2; numbers are L2-assisted",
-                   "parallelism": f"replicas x{world} (sequences shard, no collective)"},
+                   "parallelism": f"replicas x{world} (sequences shard, no collective)",
+                   "step_dispatch": getattr(step, "dispatch", "eager"),
+                   "dispatch_ms_per_step": getattr(step, "dispatch_ms", None)},
         "kv_gbs": round(db["kv"] / (dec_ms / 1e3) / 1e9, 1),
         "calls_us": {k: round(v * 1e3, 2) for k, v in per_call.items()},
         "serial_ms_per_step": round(serial_ms, 5),
@@ -677,6 +730,8 @@ def run_ours(args):
     if (world == 1 and not args.no_targets and args.workload == W.HEADLINE and args.kv_dtype == "bf16"
             and args.partition == 0 and not args.unfused and not args.no_cascade):
         line["targets"] = {name: target_record(name, dev, peaks, args, world) for name in TARGET_WORKLOADS}
+        for key, name, kvd in EXTRA_RECORDS:
+            line["targets"][key] = target_record(name, dev, peaks, args, world, kv_dtype=kvd)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
