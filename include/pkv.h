@@ -140,9 +140,10 @@ int pkv_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_le
  * As pkv_decode_partition_size for pkv_paged_attention_decode_fp8, whose
  * adaptive choice differs: when num_seqs x units (units = num_kv_heads x
  * ceil(num_q_heads / num_kv_heads / 8)) is between 2 and 4 times the SM
- * count, one resident wave of its thread blocks covers the batch and no
- * sequence is split (the partition is max_context_len rounded up to a
- * multiple of 16); otherwise the choice of pkv_decode_partition_size.
+ * count and max_context_len is at most 8192, one resident wave of its thread
+ * blocks covers the batch and no sequence is split (the partition is
+ * max_context_len rounded up to a multiple of 16); otherwise the choice of
+ * pkv_decode_partition_size.
  */
 int pkv_decode_partition_size_fp8(int num_seqs, int num_q_heads, int num_kv_heads, int max_context_len,
                                   int partition_size, int *out);

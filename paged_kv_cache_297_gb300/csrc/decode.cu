@@ -1366,12 +1366,17 @@ int adaptive_partition(int num_seqs, int num_kv_heads, int max_context_len) {
 }
 
 // The fp8 kernel's choice: when the (sequence, unit) pairs fill between two
-// and four of its thread blocks per SM, a sequence is not split at all: one
-// resident wave covers the batch, and the partials and the merge launch cost
-// more than the uneven lengths do.  Otherwise as adaptive_partition.
+// and four of its thread blocks per SM and no context exceeds
+// kFp8UnsplitTokens, a sequence is not split at all: one resident wave
+// covers the batch, and the partials and the merge launch cost more than the
+// uneven lengths do.  (Longer contexts make a thread block's work, and the
+// spread between the longest and the rest, large against the merge.)
+// Otherwise as adaptive_partition.
+constexpr int kFp8UnsplitTokens = 8192;
+
 int fp8_partition(int num_seqs, int units_per_seq, int num_kv_heads, int max_context_len) {
     const long long units = (long long)num_seqs * units_per_seq, sms = device_sms();
-    if (units >= 2 * sms && units <= 4 * sms && max_context_len > 0)
+    if (units >= 2 * sms && units <= 4 * sms && max_context_len > 0 && max_context_len <= kFp8UnsplitTokens)
         return (max_context_len + kBlock - 1) / kBlock * kBlock;
     return adaptive_partition(num_seqs, num_kv_heads, max_context_len);
 }

@@ -105,6 +105,8 @@ def test_decode_partition_choice_fp8(lib):
     assert pkv.decode_partition_size_fp8(8, 64, 8, 131072) == 3072      # 64 units: split
     assert pkv.decode_partition_size_fp8(256, 32, 8, 2560) == 3072      # 2048 units: split
     assert pkv.decode_partition_size_fp8(32, 128, 8, 4096) == 4096      # group 16: 2 units per kv head
+    assert pkv.decode_partition_size_fp8(64, 32, 8, 8192) == 8192       # the longest context left unsplit
+    assert pkv.decode_partition_size_fp8(64, 32, 8, 8193) == 3072       # longer: split (64x8x2 units)
     assert pkv.decode_partition_size_fp8(64, 32, 8, 4096, 256) == 256   # explicit
     # unsplit needs no workspace; the partition-0 workspace still covers it
     assert pkv.decode_workspace_bytes(64, 32, 128, 4096, 4096) == 0
