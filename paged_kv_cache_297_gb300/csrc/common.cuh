@@ -69,6 +69,40 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Compare-and-swap of the 16 bytes at `addr` (16-byte aligned); returns the
+// previous contents through old_lo / old_hi.
+__device__ __forceinline__ void cas128(unsigned long long *addr, unsigned long long cmp_lo, unsigned long long cmp_hi,
+                                       unsigned long long new_lo, unsigned long long new_hi,
+                                       unsigned long long &old_lo, unsigned long long &old_hi) {
+    asm volatile(
+        "{\n .reg .b128 d, c, n;\n mov.b128 c, {%3, %4};\n mov.b128 n, {%5, %6};\n"
+        " atom.relaxed.gpu.global.cas.b128 d, [%2], c, n;\n mov.b128 {%0, %1}, d;\n}\n"
+        : "=l"(old_lo), "=l"(old_hi)
+        : "l"(addr), "l"(cmp_lo), "l"(cmp_hi), "l"(new_lo), "l"(new_hi)
+        : "memory");
+}
+
+// A work counter in a caller's workspace that needs no clearing pass: the
+// 16 bytes at `c` (16-byte aligned) hold {launch tag, count}.  The first
+// caller of a launch finds another tag (an earlier launch's, a cleared 0, or
+// whatever the workspace held) and installs {tag, 0} with one 16-byte
+// compare-and-swap; every call then adds one to the count and returns the
+// count before it.  Tags are non-zero 64-bit values drawn per launch.
+__device__ __forceinline__ unsigned long long tagged_add(unsigned long long *c, unsigned long long tag) {
+    unsigned long long t = *reinterpret_cast<volatile unsigned long long *>(c);
+    if (t != tag) {
+        unsigned long long cnt = *reinterpret_cast<volatile unsigned long long *>(c + 1);
+        for (int tries = 0; tries < 64 && t != tag; tries++) {
+            unsigned long long ot, oc;
+            cas128(c, t, cnt, tag, 0ull, ot, oc);
+            if (ot == t && oc == cnt) break;  // installed
+            t = ot;
+            cnt = oc;
+        }
+    }
+    return atomicAdd(c + 1, 1ull);
+}
+
 // 16-byte global->shared copy; src_bytes = 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)),

@@ -181,19 +181,6 @@ __device__ __forceinline__ int sw128(int r, int c16) {
     return (r >> 3) * 1024 + (r & 7) * 128 + ((c16 ^ (r & 7)) << 4);
 }
 
-// Compare-and-swap of the 16 bytes at `addr` (16-byte aligned); returns the
-// previous contents through old_lo / old_hi.
-__device__ __forceinline__ void cas128(unsigned long long *addr, unsigned long long cmp_lo, unsigned long long cmp_hi,
-                                       unsigned long long new_lo, unsigned long long new_hi,
-                                       unsigned long long &old_lo, unsigned long long &old_hi) {
-    asm volatile(
-        "{\n .reg .b128 d, c, n;\n mov.b128 c, {%3, %4};\n mov.b128 n, {%5, %6};\n"
-        " atom.relaxed.gpu.global.cas.b128 d, [%2], c, n;\n mov.b128 {%0, %1}, d;\n}\n"
-        : "=l"(old_lo), "=l"(old_hi)
-        : "l"(addr), "l"(cmp_lo), "l"(cmp_hi), "l"(new_lo), "l"(new_hi)
-        : "memory");
-}
-
 // The next work item for this cluster: items below the number of clusters
 // are each cluster's first; later ones are handed out in order by a counter
 // in the workspace.  The counter is the pair {launch tag, count} (16 bytes):
@@ -202,20 +189,7 @@ __device__ __forceinline__ void cas128(unsigned long long *addr, unsigned long l
 // compare-and-swap, so the call needs no clearing pass before the kernel.
 // Tags are 64-bit values drawn per launch; only a launch's own tag can match.
 __device__ __forceinline__ int next_item(const PrefillParams &p) {
-    unsigned long long *c = p.item_counter;
-    const unsigned long long tag = p.launch_tag;
-    unsigned long long t = *reinterpret_cast<volatile unsigned long long *>(c);
-    if (t != tag) {
-        unsigned long long cnt = *reinterpret_cast<volatile unsigned long long *>(c + 1);
-        for (int tries = 0; tries < 64 && t != tag; tries++) {
-            unsigned long long ot, oc;
-            cas128(c, t, cnt, tag, 0ull, ot, oc);
-            if (ot == t && oc == cnt) break;  // installed
-            t = ot;
-            cnt = oc;
-        }
-    }
-    const unsigned long long k = atomicAdd(c + 1, 1ull);
+    const unsigned long long k = pkv::tagged_add(p.item_counter, p.launch_tag);
     const unsigned long long item = (unsigned long long)(gridDim.x / 2) + k;
     return item < (unsigned long long)p.num_items ? (int)item : 0x7fffffff;
 }
@@ -227,23 +201,10 @@ __device__ __forceinline__ int next_item(const PrefillParams &p) {
 // parameters, tag included, that it was captured with.  (By then every CTA
 // has made its last fetch from the first pair.)
 __device__ __forceinline__ void count_exit(const PrefillParams &p) {
-    unsigned long long *c = p.item_counter + 2;
-    const unsigned long long tag = p.launch_tag;
-    unsigned long long t = *reinterpret_cast<volatile unsigned long long *>(c);
-    if (t != tag) {
-        unsigned long long cnt = *reinterpret_cast<volatile unsigned long long *>(c + 1);
-        for (int tries = 0; tries < 64 && t != tag; tries++) {
-            unsigned long long ot, oc;
-            cas128(c, t, cnt, tag, 0ull, ot, oc);
-            if (ot == t && oc == cnt) break;  // installed
-            t = ot;
-            cnt = oc;
-        }
-    }
-    const unsigned long long k = atomicAdd(c + 1, 1ull);
+    const unsigned long long k = pkv::tagged_add(p.item_counter + 2, p.launch_tag);
     if (k == (unsigned long long)gridDim.x - 1) {
         atomicExch(p.item_counter, 0ull);
-        atomicExch(c, 0ull);
+        atomicExch(p.item_counter + 2, 0ull);
     }
 }
 
