@@ -215,8 +215,7 @@ class Step:
         self.fp8 = batch.k_scale is not None
         if self.fp8:
             t["k_scale"], t["v_scale"] = batch.k_scale.to(dev), batch.v_scale.to(dev)
-            self.fused = False
-        self.cascade = (self.fused and not no_cascade and self.prefix_len > 0
+        self.cascade = (self.fused and not self.fp8 and not no_cascade and self.prefix_len > 0
                         and batch.dtype == torch.bfloat16 and d == 128)
         if self.cascade:
             ws = pkv.decode_shared_prefix_workspace_bytes(S, Hq, d, self.max_ctx, self.prefix_len, partition)
@@ -250,6 +249,12 @@ class Step:
         if self.has_copy:
             out.append(("copy_blocks", lambda: pkv.copy_blocks(t["copy_pairs"], t["k_cache"],
                                                                t["v_cache"])))
+        if self.fp8 and self.fused:
+            out.append(("decode", lambda: pkv.decode_step_fp8(
+                t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"],
+                t["block_tables"], t["context_lens"], b.scale, self.out, max_context_len=self.max_ctx,
+                partition_size=self.partition, workspace=self.ws)))
+            return out
         if self.fp8:
             out.append(("kv_append", lambda: pkv.kv_append_fp8(t["k_new"], t["v_new"], t["slot_mapping"],
                                                                t["k_cache"], t["v_cache"], t["k_scale"],
@@ -571,17 +576,21 @@ def step_rooflines(step: Step, per_call: dict, peaks: dict, workload: str):
     dec_ms = per_call["decode"]
     # the fused call also writes the appended K and V rows (it reads them from
     # k_new/v_new instead of the cache, which the KV count already covers)
-    dec_bytes = db["total"] + (2 * S * Hkv * d * elem if step.fused else 0)
+    dec_bytes = db["total"] + (2 * S * Hkv * d * kv_elem if step.fused else 0)
     if step.cascade:
         # the prefix's K/V are read once, not once per sequence: count them once
         dec_bytes -= step.prefix_len * (S - 1) * 2 * Hkv * d * elem
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
-    kname = ("decode_shared_prefix" if step.cascade else "decode_step" if step.fused
-             else "paged_attention_decode_fp8" if step.fp8 else "paged_attention_decode")
+    kname = ("decode_shared_prefix" if step.cascade else "decode_step_fp8" if step.fp8 and step.fused
+             else "decode_step" if step.fused else "paged_attention_decode_fp8" if step.fp8
+             else "paged_attention_decode")
     traffic = recorded_traffic(kname, workload, CASCADE_SOURCES if step.cascade else DECODE_SOURCES)
     roofline = {"kernel": ("decode_shared_prefix (fused append; shared-prefix tile on the tensor cores, "
                            "partition kernel over each sequence's own tokens, log-sum-exp merge; bytes "
                            "count the prefix once)" if step.cascade else
+                           "decode_step_fp8 (fused quantising append; fp8 E4M3 cache widened to fp16 in "
+                           "registers, transposed fp16 tile products; one wave without a split when it "
+                           "covers the batch, else partitions + log-sum-exp reduce)" if step.fp8 and step.fused else
                            "decode_step (fused append + partition kernel + log-sum-exp reduce)"
                            if step.fused else
                            "paged_attention_decode_fp8 (fp8 E4M3 cache widened to fp16 in registers, "

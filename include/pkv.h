@@ -228,6 +228,25 @@ int pkv_decode_step(const void *q, const void *k_new, const void *v_new, void *k
                     int dtype, int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pkv_decode_step over fp8 E4M3 caches: pkv_kv_append_fp8 of each sequence's
+ * new token at logical position L_s - 1 (code = E4M3(value / scale) of its kv
+ * head, the same bytes) followed by pkv_paged_attention_decode_fp8, in one
+ * launch.
+ *   k_new, v_new  [num_seqs][num_kv_heads][128] bf16, 16-byte aligned
+ *   k_cache, v_cache  [num_blocks][num_kv_heads][16][128] E4M3 codes, updated
+ *                 in place and then read
+ * All other arguments, results and errors are those of
+ * pkv_paged_attention_decode_fp8 (partition_size 0: the choice of
+ * pkv_decode_partition_size_fp8).
+ */
+int pkv_decode_step_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                        const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, int num_blocks, int max_context_len,
+                        int partition_size, float scale, void *out, int out_dtype, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
  * Paged-attention decode that allocates nothing, for callers that cannot
  * allocate device memory where they run decode (code inside an allocator or
  * memory-pool hook that must not re-enter the allocator, or embedders whose

@@ -53,7 +53,7 @@ EXPORTED = (
     "pkv_prefill_workspace_bytes",
     "pkv_paged_attention_prefill_chunk", "pkv_get_status", "pkv_set_wait_limit_ns", "pkv_last_error_string",
     "pkv_version",
-    "pkv_kv_append_fp8", "pkv_paged_attention_decode_fp8", "pkv_decode_partition_size_fp8",
+    "pkv_kv_append_fp8", "pkv_paged_attention_decode_fp8", "pkv_decode_partition_size_fp8", "pkv_decode_step_fp8",
     "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free_blocks", "pkv_bm_add_sequence", "pkv_bm_fork",
     "pkv_bm_append_tokens", "pkv_bm_slots", "pkv_bm_free_sequence", "pkv_bm_block_tables",
 )
@@ -108,6 +108,7 @@ def load():
     lib.pkv_kv_append_fp8.argtypes = [P, P, I, P, I, P, P, P, P, I, I, I, I, P]
     lib.pkv_paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I, P,
                                                    SZ, P]
+    lib.pkv_decode_step_fp8.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, F, P, I, P, SZ, P]
     L = ctypes.c_int64
     lib.pkv_bm_create.argtypes = [I, I, I, ctypes.POINTER(P)]
     lib.pkv_bm_destroy.argtypes = [P]
@@ -329,6 +330,40 @@ def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tabl
         _dev(block_tables, "block_tables", torch.int32), mb,
         _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, d, bs, NB,
         int(max_context_len), int(partition_size), float(scale), _dev(out, "out"),
+        _dt(out), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                    out, max_context_len: Optional[int] = None, partition_size: int = 0,
+                    workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """:func:`kv_append_fp8` of each sequence's new K/V row (``k_new``/``v_new``
+    ``[S, Hkv, 128]`` bf16, at position L-1) fused into
+    :func:`paged_attention_decode_fp8`: one launch."""
+    NB, Hkv, bs, d = _cache_dims(k_cache, v_cache)
+    S, Hq, dq = q.shape
+    if k_cache.dtype != torch.uint8 or q.dtype != torch.bfloat16 or dq != d:
+        raise ValueError("q must be bf16 [S, Hq, head_dim] over uint8 (E4M3) caches")
+    if k_new.shape != (S, Hkv, d) or v_new.shape != k_new.shape or k_new.dtype != torch.bfloat16 \
+            or v_new.dtype != torch.bfloat16:
+        raise ValueError("k_new/v_new must be bf16 [S, num_kv_heads, head_dim]")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks] and context_lens [S]")
+    mb = int(block_tables.shape[1])
+    if max_context_len is None:
+        max_context_len = mb * bs
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        need = decode_workspace_bytes(S, Hq, d, max_context_len, partition_size)
+        workspace = _workspace(need, q.device, stream)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().pkv_decode_step_fp8(
+        _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+        _dev(block_tables, "block_tables", torch.int32), mb, _dev(context_lens, "context_lens", torch.int32),
+        S, Hq, Hkv, d, bs, NB, int(max_context_len), int(partition_size), float(scale), _dev(out, "out"),
         _dt(out), ws_ptr, ws_bytes, _stream(stream)))
     return out
 

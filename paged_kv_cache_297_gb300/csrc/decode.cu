@@ -106,6 +106,36 @@ __device__ __forceinline__ void append_new_token(const DecodeParams &p, const in
     }
 }
 
+// fp8 caches: quantise and write the new token's K and V rows (bf16, d =
+// 128) of sequence s, kv head kvh at logical position L-1, exactly as
+// pkv_kv_append_fp8 does (code = E4M3(x / scale): IEEE division, nearest
+// even, saturated at 448).  16 chunks of 16 values (8 for K, 8 for V), taken
+// by the threads [first, first + count); a barrier over them follows before
+// the row is read.
+__device__ __forceinline__ void append_new_token_fp8(const DecodeParams &p, const int32_t *table, int s, int kvh,
+                                                     int L, int first, int count) {
+    const int t = L - 1;
+    const int phys = table[t / kBlock];
+    if (phys < 0 || phys >= p.num_blocks) return;  // reported by the gather
+    const size_t row = ((size_t)phys * p.num_kv_heads + kvh) * kBlock + (t % kBlock);  // 128-byte rows
+    const size_t src = ((size_t)s * p.num_kv_heads + kvh) * 128;
+    for (int i = first; i < 16; i += count) {
+        const bool is_v = i >= 8;
+        const int c = i & 7;
+        const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(is_v ? p.v_new : p.k_new) + src + 16 * c;
+        const float sc = is_v ? p.v_scale[kvh] : p.k_scale[kvh];
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float a0 = __fdiv_rn(__bfloat162float(x[4 * q]), sc), a1 = __fdiv_rn(__bfloat162float(x[4 * q + 1]), sc);
+            const float a2 = __fdiv_rn(__bfloat162float(x[4 * q + 2]), sc), a3 = __fdiv_rn(__bfloat162float(x[4 * q + 3]), sc);
+            w[q] = (uint32_t)pkv::f32x2_to_e4m3x2(a0, a1) | ((uint32_t)pkv::f32x2_to_e4m3x2(a2, a3) << 16);
+        }
+        uint4 *dst = static_cast<uint4 *>(const_cast<void *>(is_v ? p.v_cache : p.k_cache)) + row * 8 + c;
+        *dst = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 __device__ __forceinline__ int clamp_len(int L, int cap, unsigned *status, bool report) {
     if (L < 0 || L > cap) {
         if (report) pkv::flag(status, PKV_STATUS_BAD_LENGTH);
@@ -865,6 +895,18 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp8_kernel(const DecodePar
     const float sl2 = p.scale_log2 * p.k_scale[kvh];
     const float vsc = p.v_scale[kvh];
 
+    if (p.k_new && part == nparts - 1 && L > 0) {
+        // the new row is read below through L2 by other threads
+        if (kHeadWarps) {
+            // (warps of other chunks of the same kv head write the same bytes)
+            append_new_token_fp8(p, table, s, kvh, L, lane, 32);
+            __syncwarp();
+        } else {
+            append_new_token_fp8(p, table, s, kvh, L, threadIdx.x, kThreads);
+            __syncthreads();
+        }
+    }
+
     unsigned char *ring = smem + warp * Sm::kWarp;
     auto block_id = [&](int li) -> int {
         return li < 32 ? __shfl_sync(0xffffffffu, my_id, li) : table[bfirst + bstride * li];
@@ -1570,7 +1612,7 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
     if (dtype == PKV_FP8_E4M3) {  // bf16 queries over an fp8 cache
         if (head_dim != 128) return pkv::fail(PKV_ERR_INVALID, "fp8 decode: head_dim must be 128");
         if (!k_scale || !v_scale) return pkv::fail(PKV_ERR_INVALID, "fp8 decode: null scales");
-        if (k_new || v_new) return pkv::fail(PKV_ERR_INVALID, "fp8 decode: no fused append");
+        // (the fused append of pkv_decode_step_fp8 takes bf16 rows)
     }
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return pkv::fail(PKV_ERR_INVALID, "bad out_dtype %d", out_dtype);
@@ -1666,6 +1708,19 @@ extern "C" int pkv_paged_attention_decode_fp8(const void *q, const void *k_cache
                        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len,
                        partition_size, scale, out, PKV_FP8_E4M3, out_dtype, workspace, workspace_bytes, stream,
                        k_scale, v_scale);
+}
+
+extern "C" int pkv_decode_step_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                   void *v_cache, const float *k_scale, const float *v_scale,
+                                   const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                   int num_blocks, int max_context_len, int partition_size, float scale, void *out,
+                                   int out_dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    if (num_seqs > 0 && (!k_new || !v_new))
+        return pkv::fail(PKV_ERR_INVALID, "decode_step_fp8: null k_new or v_new");
+    return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, partition_size,
+                       scale, out, PKV_FP8_E4M3, out_dtype, workspace, workspace_bytes, stream, k_scale, v_scale);
 }
 
 extern "C" int pkv_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,

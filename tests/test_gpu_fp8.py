@@ -117,6 +117,41 @@ def test_fp8_head_warp_schedule():
     assert_parity(out, ref, torch.bfloat16, "fp8 decode")
 
 
+@pytest.mark.parametrize("case", ["llama3", "edges", "head_warps"])
+def test_fp8_decode_step_equals_append_then_decode(case):
+    # the fused call writes the same codes as kv_append_fp8 and then reads the
+    # same cache: caches and outputs bitwise equal to the two calls
+    if case == "llama3":
+        b = W.fp8_batch(W.make_batch("llama3_8b_decode"))
+    elif case == "edges":
+        b = W.fp8_batch(W.custom_batch("bf16", len(EDGE_LENS), 32, 8, 128, EDGE_LENS, seed=43))
+    else:
+        lens = np.random.Generator(np.random.PCG64(5)).integers(1, 400, 320).tolist()
+        b = W.fp8_batch(W.custom_batch("bf16", len(lens), 32, 8, 128, lens, seed=79))
+    live = b.context_lens > 0
+    mc = max(1, b.max_context_len)
+    ta, tb = to_dev(b), to_dev(b)
+    ks, vs = b.k_scale.cuda(), b.v_scale.cuda()
+    out_a = torch.empty(b.q.shape, dtype=torch.float32, device="cuda")
+    out_b = torch.empty(b.q.shape, dtype=torch.float32, device="cuda")
+    pkv.kv_append_fp8(ta["k_new"], ta["v_new"], ta["slot_mapping"], ta["k_cache"], ta["v_cache"], ks, vs)
+    pkv.paged_attention_decode_fp8(ta["q"], ta["k_cache"], ta["v_cache"], ks, vs, ta["block_tables"],
+                                   ta["context_lens"], b.scale, out_a, max_context_len=mc)
+    # the fused call takes one row per sequence (sequences with L = 0 append nothing)
+    S, Hkv, d = b.q.shape[0], b.k_cache.shape[1], b.k_cache.shape[3]
+    k_new = torch.zeros((S, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    v_new = torch.zeros((S, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    idx = torch.nonzero(live).flatten().cuda()
+    k_new[idx] = tb["k_new"][: idx.numel()]
+    v_new[idx] = tb["v_new"][: idx.numel()]
+    pkv.decode_step_fp8(tb["q"], k_new, v_new, tb["k_cache"], tb["v_cache"], ks, vs, tb["block_tables"],
+                        tb["context_lens"], b.scale, out_b, max_context_len=mc)
+    torch.cuda.synchronize()
+    assert pkv.get_status() == 0
+    assert torch.equal(ta["k_cache"], tb["k_cache"]) and torch.equal(ta["v_cache"], tb["v_cache"])
+    assert torch.equal(out_a, out_b)
+
+
 def test_fp8_rejects_what_it_does_not_support():
     b = W.fp8_batch(W.custom_batch("bf16", 2, 8, 8, 64, [5, 9], seed=2))
     t = to_dev(b)
