@@ -12,78 +12,80 @@
 // CTA holds rows 0-127, the odd CTA rows 128-255, and threads of the even CTA
 // issue every MMA in the pair form (tcgen05 cta_group::2, M = 256), which
 // runs on both SMs' tensor cores at once:
-//   S(t)  = Q K(t)^T : M=256, N=128 keys, K=d; A = Q (each CTA its 128 rows),
+//   S(g)  = Q K(g)^T : M=256, N=128 keys, K=d; A = Q (each CTA its 128 rows),
 //                      B = K (each CTA 64 of the 128 keys), S in each CTA's
 //                      tensor memory (its 128 rows x 128 keys);
-//   O    += P(t) V(t): M=256, N=d, K=128 keys; A = P from each CTA's tensor
+//   O    += P(g) V(g): M=256, N=d, K=128 keys; A = P from each CTA's tensor
 //                      memory, B = V (each CTA 64 of the 128 columns of d).
 // One MMA instruction does both SMs' work, and each SM loads only half of
 // every K and V tile.  (Measured on GB300: one thread issues a tcgen05.mma
 // about every 64 cycles whatever its N, and one thread issues a 2 KB TMA box
-// about every 130-180 cycles; the one-SM form of this kernel was bound by the
-// latter.)
-// Warp roles (one CTA per SM, 12 warps, in both CTAs of the pair):
-//   * two softmax teams of 4 warps: team 0 takes key tiles 0, 2, 4, ..., team 1
-//     tiles 1, 3, 5, ...  Thread r of a team owns query row r of its CTA
-//     (TMEM lane r).  It reads its 128 scores from TMEM in one load, whose
-//     own reduction gives the row maximum, masks them, computes
-//     p = 2^(s * scale * log2 e - m) (one paired multiply-add per two
-//     elements, ex2.approx on the special-function unit) and stores P as bf16
-//     pairs over the first 64 columns of the same S buffer, handing each half
-//     (64 keys) to its team's MMA lane once both CTAs have stored it.  Each
-//     team has its own S/P buffer, O accumulator and running (m, l); the two
-//     partial results are merged by log-sum-exp at the end.  One team's
-//     softmax overlaps the other team's MMAs.
-//   * two MMA-issuing lanes, lane 0 of warps 8 (team 0's tiles) and 9 (team
-//     1's) of the even CTA, each in its team's tile order: PV(t) (half by
-//     half as P(t) is stored), then S(t+2) into the same buffer.  tcgen05.mma
-//     operations issued by one thread execute in order, so S(t+2) cannot
-//     overwrite P(t) before PV(t) has read it; the two lanes touch disjoint
-//     tensor memory and ring stages, and while one is blocked issuing (the
-//     pipe takes an MMA about as fast as it runs one) or waiting for its
-//     team's P, the other proceeds.
-//   * two loader warps per CTA, one for K and one for V, that gather this
+// about every 130-180 cycles.)
+//
+// The key tiles of an item run through double buffers: S of tile g in one of
+// two tensor-memory buffers, its P in one of two others, so that S(g+2) is
+// computed while the softmax still works on S(g), and PV(g) while it works on
+// S(g+1).  The tensor pipe then runs without waiting for the softmax, which
+// is the bound when each S buffer has to hold its P until PV has read it.
+// Warp roles (one CTA per SM, 14 warps, in both CTAs of the pair):
+//   * 8 softmax warps.  Warp w owns rows 32 (w % 4) .. +31 of its CTA (its
+//     tensor-memory lanes) and keys 64 (w / 4) .. +63 of every tile, so two
+//     threads share each row.  A thread reads its 64 scores in one load,
+//     whose own reduction gives their maximum, releases the S buffer, trades
+//     maxima with the other thread of its row through shared memory, masks,
+//     computes p = 2^(s * scale * log2 e - m) (one paired multiply-add per
+//     two elements, ex2.approx on the special-function unit) and stores its
+//     64 keys of P as bf16 pairs; P(g) goes to the PV lane once all 8 warps
+//     of both CTAs have stored it (either half's PV writes the whole O row,
+//     which both threads of the row may have to rescale first).  Both
+//     threads of a row keep the same reference max m, one O row and a
+//     partial row sum, added at the end.
+//   * two MMA-issuing lanes in the even CTA: lane 0 of warp 8 issues every
+//     S(g) (once K(g) has landed and S(g-2) has been read out of the
+//     buffer), lane 0 of warp 9 every PV(g) (once V(g) has landed and P(g)
+//     is stored).  They write disjoint tensor
+//     memory and need no order between them.
+//   * four loader warps per CTA, two for K and two for V, that gather this
 //     CTA's half of each tile through the block table with 2-D TMA boxes (the
 //     cache viewed as [num_blocks * num_kv_heads * 16 rows][128] with 128-byte
 //     swizzle, which writes exactly the layout the MMAs read), reading the
-//     table one tile ahead.  K: this CTA's 4 blocks of the tile's 8, both
-//     64-column halves; blocks past the keys are not loaded (their scores are
-//     masked).  V: all 8 blocks, this CTA's 64 columns; rows past the keys are
-//     zeroed in place (P = 0 times a NaN in an unused row would still poison
-//     O) and a block that the keys end inside is copied with zero-filling
-//     cp.async.  Every load of either CTA counts its bytes on the even CTA's
-//     barrier of that stage, where the MMA lane waits.  Each team has stages
-//     of its own in both rings (three for K, two for V), so that every phase
-//     of a stage is waited for by one lane, in order; a stage is refilled when
-//     the S (for K) or PV (for V) that read it has finished.  The K loader
-//     also loads this CTA's Q rows of each item (TMA, 3-D box) and, in the
-//     even CTA, hands out the items.
+//     table one tile ahead.  K: this CTA's 4 blocks of the tile's 8 (2 per
+//     warp), both 64-column halves; blocks past the keys are not loaded
+//     (their scores are masked).  V: all 8 blocks (4 per warp), this CTA's
+//     64 columns; rows past the keys are zeroed in place (P = 0 times a NaN
+//     in an unused row would still poison O) and a block that the keys end
+//     inside is copied with zero-filling cp.async.  Every load of either CTA
+//     counts its bytes on the even CTA's barrier of that stage, where the
+//     MMA lane waits; a stage is refilled when the S (for K) or PV (for V)
+//     that read it has finished.  The first K loader also loads this CTA's
+//     Q rows of each item (TMA, 3-D box) and, in the even CTA, hands out the
+//     items.
 // The running max of a row is only moved when a tile maximum exceeds it by
 // more than 8 (log2 units), so P <= 256 and O is rarely rescaled; numerator
 // and denominator share the same reference, so the result is exact.
 //
-// TMEM columns (all 512, in each CTA): S/P of team t at 128t, O of team t at
-// 256 + 128t.  Shared memory per CTA, in the 128-byte-swizzled canonical
-// layout (8-row atoms of 8 x 128 bytes, 16-byte chunk c of row r at chunk
-// c ^ (r % 8)):
+// TMEM columns (all 512, in each CTA): S of tile g at 128 (g % 2), O at 256,
+// P of tile g at 384 + 64 (g % 2).  Shared memory per CTA, in the
+// 128-byte-swizzled canonical layout (8-row atoms of 8 x 128 bytes, 16-byte
+// chunk c of row r at chunk c ^ (r % 8)):
 //   Q : two 64-column halves of this CTA's 128 rows              (32 KB)
 //   K : six stages x two 64-column halves of this CTA's 64 keys  (96 KB)
 //   V : four stages x 128 keys of this CTA's 64 columns          (64 KB)
-// Waits.  Every wait on an mbarrier is bounded in time (PrefillParams::
-// wait_ns, from %globaltimer).  A wait that runs out makes the whole warp
-// leave its role loop (the decision is taken warp-wide, so no lane is left
-// at a warp barrier) and raises an abort flag in both CTAs, at which the
-// other roles' waits give up too.  A role that has left issues no further
-// copies or MMAs.  At the end one thread of each CTA waits for the MMA
-// thread's final commit, which arrives after every earlier one (a separate,
-// fixed bound of one second), the pair meets at a cluster barrier, and if
-// anything failed both CTAs wait 100 us more so that copies already issued
-// land before either CTA's shared memory is released; the CTA records
-// PKV_STATUS_INTERNAL, frees its tensor memory and returns.  (A failure
-// stops all further issue, so the only copies that can still be in flight
-// were issued before it; a TMA load or cp.async of a few KB lands within
-// microseconds.  Waiting on their barriers instead is not possible: after a
-// failure a phase may never collect all its arrivals.)
+// Waits.  Every wait on an mbarrier or on the other thread of a row is
+// bounded in time (PrefillParams::wait_ns, from %globaltimer).  A wait that
+// runs out makes the whole warp leave its role loop (the decision is taken
+// warp-wide, so no lane is left at a warp barrier) and raises an abort flag
+// in both CTAs, at which the other roles' waits give up too.  A role that
+// has left issues no further copies or MMAs.  At the end one thread of each
+// CTA waits for both MMA lanes' final commits, which arrive after every
+// earlier one (a separate, fixed bound of one second), the pair meets at a
+// cluster barrier, and if anything failed both CTAs wait 100 us more so that
+// copies already issued land before either CTA's shared memory is released;
+// the CTA records PKV_STATUS_INTERNAL, frees its tensor memory and returns.
+// (A failure stops all further issue, so the only copies that can still be
+// in flight were issued before it; a TMA load or cp.async of a few KB lands
+// within microseconds.  Waiting on their barriers instead is not possible:
+// after a failure a phase may never collect all its arrivals.)
 #include <math.h>
 
 #include <cuda.h>
@@ -105,22 +107,17 @@ using pkv::PrefillParams;
 namespace tc = pkv::tc;
 
 constexpr int D = 128;
-constexpr int BM = 128;        // query rows per CTA
+constexpr int BM = 128;         // query rows per CTA
 constexpr int kPairRows = 256;  // query rows per work item (both CTAs)
-constexpr int BN = 128;        // keys per tile
-constexpr int kTeamThreads = 128;
-constexpr int kMmaWarp = 8;  // warps 8 (team 0) and 9 (team 1) of the even CTA: MMA issue
-constexpr int kKLoadWarp = 10, kVLoadWarp = 11;
-constexpr int kThreads = 12 * 32;
+constexpr int BN = 128;         // keys per tile
+constexpr int kSoftmaxThreads = 256;  // warps 0-7
+constexpr int kSWarp = 8, kPVWarp = 9;  // the even CTA's MMA lanes: S = Q K^T, and O += P V
+constexpr int kLoadWarp0 = 10;          // 10, 11: K loaders; 12, 13: V loaders
+constexpr int kThreads = 14 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;  // S/P of team t at 128t, O of team t at kOCol + 128t
-// Each ring has stages of its own per softmax team: the team's j-th key
-// tile goes to stage team * n + j % n of a ring with n stages per team, so
-// every phase of a stage is waited for by one issuing thread, in order.  K
-// gets three per team: the next S of a team is issued a team period after
-// its previous one, about the latency of a K load.
-constexpr int kKPerTeam = 3, kVPerTeam = 2;
-constexpr int kKStages = 2 * kKPerTeam, kVStages = 2 * kVPerTeam;
+// S of tile g in columns 128 (g % 2); O at 256; P of tile g at 384 + 64 (g % 2)
+constexpr uint32_t kOCol = 256, kPCol = 384;
+constexpr int kKStages = 6, kVStages = 4;
 
 constexpr int kQHalf = BM * 128;        // 16 KB: 128 rows x 64 bf16
 constexpr int kQBytes = 2 * kQHalf;     // 32 KB
@@ -129,42 +126,44 @@ constexpr int kKStage = 2 * kKHalf;     // 16 KB
 constexpr int kVStage = BN * 128;       // 16 KB: 128 keys x this CTA's 64 bf16
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;                  // 32768
-constexpr int kOffV = kOffK + kKStages * kKStage;       // 98304
-constexpr int kOffBar = kOffV + kVStages * kVStage;     // 163840
+constexpr int kOffV = kOffK + kKStages * kKStage;       // 131072
+constexpr int kOffBar = kOffV + kVStages * kVStage;     // 196608
 
 // mbarrier indices.  "both": each CTA has its own, signalled for both by the
 // even CTA's MMA commits.  "even": used in the even CTA only, which both
 // CTAs' threads (or copies) arrive at.
 enum Bar : int {
-    B_PFULL = 0,        // [team][half] P(t) of keys 64h .. 64h+63 stored; even, 8 warps
-    B_KFULL = 4,        // [stage] K tile landed (both halves); even, 2 loaders + bytes
+    B_PFULL = 0,   // [g % 2][half] P(g) of keys 64h .. 64h+63 stored; even, its 4 warps per CTA
+    B_SFREE = 4,   // [g % 2] S(g) read into registers by every softmax warp; even, 8 warps per CTA
+    B_KFULL = 6,   // [stage] K tile landed; even, 2 loaders per CTA + bytes
     // [stage] the S reading the stage is done; both.  Also the softmax
-    // team's "S(t) computed" (and, as the MMAs before it are done too, "its
-    // PV(t-2) done"): the stage cannot be reused before the team has
-    // finished with tile t, so the phase the team waits for is never
-    // overtaken
+    // warps' "S(g) computed": its next phase needs S(g + 6), which the
+    // warps' own reads of S(g + 4) hold back
     B_KEMPTY = B_KFULL + kKStages,
-    B_VFULL = B_KEMPTY + kKStages,   // [stage] V tile landed; even, 2 loaders + bytes
-    // [stage] the PV reading the stage is done; both.  Also the team's "PV(t)
-    // done" at the end of an item (same argument)
+    B_VFULL = B_KEMPTY + kKStages,   // [stage] V tile landed; even, 2 loaders per CTA + bytes
+    // [stage] the PV reading the stage is done; both.  Also the softmax
+    // warps' "PV(g) done": P(g) buffer free, O holds every tile up to g
     B_VEMPTY = B_VFULL + kVStages,
     B_GO = B_VEMPTY + kVStages,      // [k & 1] Q of the k-th item with work landed; even
     B_ITEM_FULL = B_GO + 2,          // [slot] item published; both
     B_ITEM_EMPTY = B_ITEM_FULL + 2,  // [slot] every reader of both CTAs has read it; even
-    B_DONE = B_ITEM_EMPTY + 2,       // all MMAs finished (the last commit); both
-    B_QFREE = B_DONE + 1,            // every S of the k-th item with work finished; both, 2 commits
+    B_DONE = B_ITEM_EMPTY + 2,       // all MMAs finished (each lane's last commit); both
+    B_QFREE = B_DONE + 1,            // every S of the k-th item with work finished; both
     B_EPI = B_QFREE + 1,             // the k-th item's O read by both CTAs' softmax warps; even, 16 warps
-    B_ML = B_EPI + 1,                // [team] the team's (m, l) of the k-th item written; per CTA, 4 warps
-    kNumBars = B_ML + 2,
+    kNumBars = B_EPI + 1,
 };
-// item queue readers: even CTA V loader, two MMA lanes and 8 softmax warps;
-// odd CTA K loader, V loader and 8 softmax warps
-constexpr int kItemReaders = 21;
+// item queue readers: even CTA: K loader 1, V loaders, two MMA lanes and 8
+// softmax warps; odd CTA: four loaders and 8 softmax warps
+constexpr int kItemReaders = 25;
 constexpr int kOffSlots = (kOffBar + kNumBars * 8 + 15) & ~15;  // TMEM address (16 B), two item slots, abort flag
 static_assert(kOffSlots % 16 == 0, "item slots are 16-byte vectors");
 constexpr int kOffAbort = kOffSlots + 16 + 2 * 16;
-constexpr int kOffRed = kOffAbort + 16;
-constexpr int kSmemBytes = kOffRed + 2 * 2 * 2 * BM * 4;  // [item & 1][team][m, l][row]
+// Row exchange between the two threads that share a row: [slot][half][row]
+// 64-bit {value, tag}; slots 0 and 1 carry tile maxima, slot 2 row sums.
+constexpr int kOffX = kOffAbort + 16;
+constexpr int kXBytes = 3 * 2 * BM * 8;
+constexpr int kSmemBytes = kOffX + kXBytes;
+static_assert(kOffX % 8 == 0, "exchange words are 8-byte aligned");
 static_assert(kSmemBytes <= 232448, "more shared memory than a CTA may have");
 static_assert(kSmemBytes > 232448 / 2, "one CTA per SM: the tensor memory is all allocated by one CTA");
 
@@ -270,7 +269,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffSlots);
     int4 *item_slots = reinterpret_cast<int4 *>(smem + kOffSlots + 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
-    float *red = reinterpret_cast<float *>(smem + kOffRed);  // [item & 1][team][m, l][row]
+    unsigned long long *xch = reinterpret_cast<unsigned long long *>(smem + kOffX);
     // shared::cta address of barrier i, and the shared::cluster windows of
     // the even CTA, this CTA and the other CTA
     auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
@@ -280,27 +279,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto bar_own = [&](int i) { return base_own + kOffBar + 8u * (uint32_t)i; };
     auto bar_other = [&](int i) { return base_other + kOffBar + 8u * (uint32_t)i; };
 
+    if (!misaligned) {
+        // exchange tags start at 0; every tag used is at least 1
+        for (int e = tid; e < kXBytes / 8; e += kThreads) xch[e] = 0ull;
+    }
     if (tid == 0 && !misaligned) {
+        uint64_t *b = reinterpret_cast<uint64_t *>(smem + kOffBar);
         for (int t = 0; t < 2; t++) {
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_PFULL + 2 * t, 8);
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_PFULL + 2 * t + 1, 8);
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_ITEM_FULL + t, 1);
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_ITEM_EMPTY + t, kItemReaders);
-            // Q lands by TMA (each CTA's K loader arrives with its bytes) or
-            // by the softmax threads' copies (8 warps in each CTA)
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_GO + t, p.q_tma ? 2 : 16);
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_ML + t, 4);
+            tc::mbar_init(b + B_PFULL + 2 * t, 8);
+            tc::mbar_init(b + B_PFULL + 2 * t + 1, 8);
+            tc::mbar_init(b + B_SFREE + t, 16);
+            tc::mbar_init(b + B_ITEM_FULL + t, 1);
+            tc::mbar_init(b + B_ITEM_EMPTY + t, kItemReaders);
+            // Q lands by TMA (each CTA's first K loader arrives with its
+            // bytes) or by the softmax threads' copies (8 warps in each CTA)
+            tc::mbar_init(b + B_GO + t, p.q_tma ? 2 : 16);
         }
-        tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_DONE, 2);  // one final commit per issuing lane
-        tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_QFREE, 2);
-        tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_EPI, 16);
+        tc::mbar_init(b + B_DONE, 2);  // one final commit per issuing lane
+        tc::mbar_init(b + B_QFREE, 1);
+        tc::mbar_init(b + B_EPI, 16);
         for (int st = 0; st < kKStages; st++) {
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_KFULL + st, 2);
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_KEMPTY + st, 1);
+            tc::mbar_init(b + B_KFULL + st, 4);
+            tc::mbar_init(b + B_KEMPTY + st, 1);
         }
         for (int st = 0; st < kVStages; st++) {
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_VFULL + st, 2);
-            tc::mbar_init(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_VEMPTY + st, 1);
+            tc::mbar_init(b + B_VFULL + st, 4);
+            tc::mbar_init(b + B_VEMPTY + st, 1);
         }
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -370,37 +374,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
 
     // Running counts that carry the barrier phases from one item to the next:
-    // tiles of each team (its ring stages and P barriers) and items with work
-    // (the Q, epilogue and (m, l) barriers).  Every role of both CTAs walks
-    // the same items, so every role's counts agree.
-    int team_base0 = 0, team_base1 = 0, go_count = 0;
+    // key tiles of the items with work so far (the global tile index g of
+    // an item's tile t is g0 + t: S, P and ring buffers and their phases) and
+    // items with work (the Q, epilogue and exchange phases).  Every role of
+    // both CTAs walks the same items, so every role's counts agree.
+    int g0 = 0, go_count = 0;
     auto advance = [&](const ItemInfo &it) {
-        team_base0 += (it.nkt + 1) / 2;
-        team_base1 += it.nkt / 2;
+        g0 += it.nkt;
         go_count += it.skip ? 0 : 1;
     };
 
-    // Ring slot of tile t of the current item: the team's j-th tile goes to
-    // stage team * n + j % n, phase j / n of that stage's barriers (n stages
-    // per team: kKPerTeam for K, kVPerTeam for V).
-    auto team_tile = [&](int t) { return ((t & 1) ? team_base1 : team_base0) + (t >> 1); };
-    auto kstage = [&](int t) { return (t & 1) * kKPerTeam + team_tile(t) % kKPerTeam; };
-    auto kphase = [&](int t) { return (unsigned)((team_tile(t) / kKPerTeam) & 1); };
-    auto vstage = [&](int t) { return (t & 1) * kVPerTeam + team_tile(t) % kVPerTeam; };
-    auto vphase = [&](int t) { return (unsigned)((team_tile(t) / kVPerTeam) & 1); };
-
     if (failed) {
         // nothing: misaligned shared memory (reported below)
-    } else if (warp == kKLoadWarp || warp == kVLoadWarp) {
-        // ---------------- loaders; the even CTA's K loader also runs the item queue
-        const bool is_k = warp == kKLoadWarp;
-        const CUtensorMap *tmap_kv[2] = {&tmap_k, &tmap_v};
+    } else if (warp >= kLoadWarp0) {
+        // ---------------- loaders: two for K (each 2 of this CTA's 4 blocks
+        // of a tile, both 64-column halves) and two for V (each 4 of the 8
+        // blocks, this CTA's 64 columns); a thread issues a TMA box only
+        // every 130-180 cycles, so each tile's 16 boxes are split over four
+        // warps.  The even CTA's first K loader also runs the item queue,
+        // and each CTA's first K loader loads its Q rows.
+        const int lw = warp - kLoadWarp0;
+        const bool is_k = lw < 2;
+        const int sub = lw & 1;
+        const bool runs_queue = is_k && sub == 0 && even;
         const int full0 = is_k ? B_KFULL : B_VFULL, empty0 = is_k ? B_KEMPTY : B_VEMPTY;
+        const int nstage = is_k ? kKStages : kVStages;
         const unsigned char *cache = static_cast<const unsigned char *>(is_k ? p.k_cache : p.v_cache);
         int item = (int)(blockIdx.x >> 1);  // the cluster's first item; later ones come from the counter
         for (int i = 0;; i++) {
             ItemInfo it;
-            if (is_k && even) {
+            if (runs_queue) {
                 int4 v = make_int4(item, 0, 0, 0);
                 if (i >= 2 && !wait_lane0(B_ITEM_EMPTY + (i & 1), (unsigned)(((i >> 1) - 1) & 1))) break;
                 if (lane == 0) {
@@ -433,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             if (it.stop) break;
-            if (is_k && p.q_tma && !it.skip) {
+            if (is_k && sub == 0 && p.q_tma && !it.skip) {
                 // This CTA's q rows, as soon as the previous item's S MMAs are
                 // done with the buffer: they land while that item finishes.
                 // Row r = j * G + h is query q0 + row0/G + j, head kvh*G + h:
@@ -451,11 +454,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
             const int32_t *table = p.block_tables + (size_t)(it.skip ? 0 : it.s) * p.max_blocks;
-            const int nb = is_k ? 4 : 8;              // blocks of a tile this CTA loads
-            const int b0 = is_k ? 4 * (int)rank : 0;  // the first of them
-            // Block ids of this CTA's blocks of tile t (lane q < nb: block q),
-            // -1 past the keys.  They are read one tile ahead, so the copies
-            // of a tile never wait for its table entries.
+            const int nb = is_k ? 2 : 4;                                   // blocks of a tile this warp loads
+            const int b0 = is_k ? 4 * (int)rank + 2 * sub : 4 * sub;       // the first of them
+            // Block ids of this warp's blocks of tile t (lane q < nb: block
+            // b0 + q), -1 past the keys.  They are read one tile ahead, so the
+            // copies of a tile never wait for its table entries.
             auto table_id = [&](int t) {
                 int id = -1;
                 if (t < it.nkt && lane < nb && t * BN + (b0 + lane) * kBlock < it.kv_end) id = table[t * 8 + b0 + lane];
@@ -464,10 +467,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int next_id = table_id(0);
             bool ok = true;
             for (int t = 0; t < it.nkt; t++) {
-                const int per = is_k ? kKPerTeam : kVPerTeam;
-                const int st = is_k ? kstage(t) : vstage(t), jt = team_tile(t);
-                // the stage's previous tile (the team's tile jt - per) has been read
-                if (jt >= per && !(ok = wait_warp(empty0 + st, (unsigned)((jt / per - 1) & 1)))) break;
+                const int g = g0 + t, st = g % nstage;
+                // the stage's previous tile (g - nstage) has been read
+                if (g >= nstage && !(ok = wait_warp(empty0 + st, (unsigned)((g / nstage - 1) & 1)))) break;
                 const int my_id = next_id;
                 next_id = table_id(t + 1);
                 const uint32_t full = bar_even(full0 + st);
@@ -475,12 +477,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int nbk = (tile_keys + kBlock - 1) / kBlock;  // blocks of the tile holding keys
                 const int box_rows = p.num_blocks * p.num_kv_heads * kBlock;  // rows of the 2-D view
                 if (is_k) {
-                    // this CTA's keys: blocks 4*rank .. 4*rank+3 of the tile,
-                    // those holding keys (the rest are masked out of S)
+                    // this warp's blocks holding keys (the rest are masked out of S)
                     unsigned char *dst = smem + kOffK + st * kKStage;
-                    const int nk = max(0, min(4, nbk - 4 * (int)rank));
+                    const int nk = max(0, min(2, nbk - b0));
                     int y = box_rows;
                     if (lane < nk) {
+                        if (my_id >= 0 && my_id < p.num_blocks)
+                            y = (my_id * p.num_kv_heads + it.kvh) * kBlock;
+                        else
+                            pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                    }
+                    const int y0 = __shfl_sync(0xffffffffu, y, 0), y1 = __shfl_sync(0xffffffffu, y, 1);
+                    if (lane == 0) {
+                        tc::mbar_arrive_expect_tx_remote(full, (uint32_t)(nk * 2 * 2048));
+                        // block b0 + q is this CTA's block 2 sub + q of the tile
+#pragma unroll
+                        for (int q = 0; q < 2; q++) {
+                            if (q >= nk) break;
+#pragma unroll
+                            for (int h = 0; h < 2; h++)
+                                tc::tma_load_2d_pair(dst + h * kKHalf + (2 * sub + q) * 2048, &tmap_k,
+                                                     h * 64, q ? y1 : y0, full);
+                        }
+                    }
+                } else {
+                    // blocks b0 .. b0+3, this CTA's 64 columns of d; a block
+                    // that the keys end inside by zero-filling copies, rows
+                    // past the keys zeroed
+                    unsigned char *dst = smem + kOffV + st * kVStage;
+                    const int cpq = (tile_keys % kBlock) ? tile_keys / kBlock : -1;
+                    const int ntma = cpq >= 0 ? nbk - 1 : nbk;  // blocks 0 .. ntma-1 of the tile by TMA
+                    const int my_ntma = max(0, min(4, ntma - b0));
+                    int y = box_rows;
+                    if (lane < my_ntma) {
                         if (my_id >= 0 && my_id < p.num_blocks)
                             y = (my_id * p.num_kv_heads + it.kvh) * kBlock;
                         else
@@ -489,41 +518,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     int ys[4];
 #pragma unroll
                     for (int q = 0; q < 4; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
-                    if (lane == 0) {
-                        tc::mbar_arrive_expect_tx_remote(full, (uint32_t)(nk * 2 * 2048));
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            if (q >= nk) break;
-#pragma unroll
-                            for (int h = 0; h < 2; h++)
-                                tc::tma_load_2d_pair(dst + h * kKHalf + q * 2048, tmap_kv[0], h * 64, ys[q], full);
-                        }
-                    }
-                } else {
-                    // all 8 blocks, this CTA's 64 columns of d; a block that
-                    // the keys end inside by zero-filling copies, rows past
-                    // the keys zeroed
-                    unsigned char *dst = smem + kOffV + st * kVStage;
-                    const int cpq = (tile_keys % kBlock) ? tile_keys / kBlock : -1;
-                    const int ntma = cpq >= 0 ? nbk - 1 : nbk;  // blocks 0 .. ntma-1 by TMA
-                    int y = box_rows;
-                    if (lane < ntma) {
-                        if (my_id >= 0 && my_id < p.num_blocks)
-                            y = (my_id * p.num_kv_heads + it.kvh) * kBlock;
-                        else
-                            pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
-                    }
-                    int ys[8];
-#pragma unroll
-                    for (int q = 0; q < 8; q++) ys[q] = __shfl_sync(0xffffffffu, y, q);
-                    if (cpq >= 0 || nbk < 8) {
-                        // generic-proxy part of the tile: the partial block's
-                        // live rows by zero-filling copies, every other row
-                        // past the keys zeroed with stores
-                        const int phys = cpq >= 0 ? __shfl_sync(0xffffffffu, my_id, cpq) : 0;
+                    const int r_lo = max(kBlock * ntma, kBlock * b0), r_hi = kBlock * (b0 + 4);
+                    if (r_lo < r_hi) {
+                        // generic-proxy part of this warp's rows: the partial
+                        // block's live rows by zero-filling copies, every
+                        // other row past the keys zeroed with stores
+                        const bool mine = cpq >= b0 && cpq < b0 + 4;
+                        const int phys = mine ? __shfl_sync(0xffffffffu, my_id, cpq - b0) : 0;
                         const bool bok = phys >= 0 && phys < p.num_blocks;
-                        if (cpq >= 0 && !bok && lane == 0) pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
-                        for (int e = lane + 16 * 8 * ntma; e < BN * 8; e += 32) {
+                        if (mine && !bok && lane == 0) pkv::flag(p.status, PKV_STATUS_BAD_BLOCK);
+                        for (int e = lane + 8 * r_lo; e < 8 * r_hi; e += 32) {
                             const int r = e >> 3, c = e & 7;
                             unsigned char *d = dst + sw128(r, c);
                             if (r < tile_keys) {
@@ -543,118 +547,108 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         __syncwarp();
                     }
                     if (lane == 0) {
-                        tc::mbar_arrive_expect_tx_remote(full, (uint32_t)(ntma * 2048));
+                        tc::mbar_arrive_expect_tx_remote(full, (uint32_t)(my_ntma * 2048));
 #pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            if (q >= ntma) break;
-                            tc::tma_load_2d_pair(dst + q * 2048, tmap_kv[1], (int)rank * 64, ys[q], full);
+                        for (int q = 0; q < 4; q++) {
+                            if (q >= my_ntma) break;
+                            tc::tma_load_2d_pair(dst + (b0 + q) * 2048, &tmap_v, (int)rank * 64, ys[q], full);
                         }
                     }
                 }
             }
             if (!ok) break;
             advance(it);
-            if (is_k && even) {  // the next item, fetched while the consumers work on this one
+            if (runs_queue) {  // the next item, fetched while the consumers work on this one
                 if (lane == 0) item = next_item(p);
                 item = __shfl_sync(0xffffffffu, item, 0);
             }
         }
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        // ---------------- MMA issue: lane 0 of warp 8 (team 0's tiles) and of
-        // warp 9 (team 1's tiles) of the even CTA issue every MMA of the
-        // pair.  The two lanes touch disjoint tensor memory (each team's S/P
-        // buffer and O accumulator) and disjoint ring stages, and each
-        // lane's MMAs run in its issue order, so neither needs to order
-        // itself after the other: while one is blocked issuing into the
-        // tensor pipe (which takes an MMA about as fast as it runs it) or
-        // waiting for its team's P, the other's waits and commits proceed.
-        const int team = warp - kMmaWarp;
+    } else if (warp == kSWarp || warp == kPVWarp) {
+        // ---------------- MMA issue: lane 0 of warp 8 of the even CTA issues
+        // every S = Q K^T of the pair, lane 0 of warp 9 every O += P V.  The
+        // two lanes write disjoint tensor memory (the two S buffers; O), so
+        // neither orders itself after the other: S(g+2) goes out as soon as
+        // the softmax warps have read S(g) into registers, while they still
+        // work on it, and PV(g) as soon as they have stored P(g).
         if (even && lane == 0) {
             // one commit per CTA of the pair: each CTA's barrier i
             auto commit_both = [&](int i) {
                 tc::mma_commit_pair(bar_own(i));
                 tc::mma_commit_pair(bar_other(i));
             };
-            // Descriptors of the first 16 columns of Q and of stage 0 of the K
-            // and V rings; a stage, a half or 16 more columns is a constant
-            // number of 16-byte units on.  V is MN-major: the next 8 keys at
-            // +1 KB (SBO); this CTA's 64 columns are one 128-byte swizzle
-            // span (LBO unused).
-            const uint64_t q_desc = tc::smem_desc_sw128(sbase + kOffQ, 16, 1024);
-            const uint64_t k_desc0 = tc::smem_desc_sw128(sbase + kOffK, 16, 1024);
-            const uint64_t v_desc0 = tc::smem_desc_sw128(sbase + kOffV, kVStage, 1024);
-            int nkt_cur = 0;  // key tiles of the item being issued
-            // S(t) = Q K(t)^T into this team's S/P buffer (K(t) landed)
-            auto issue_s = [&](int t) {
-                const int st = kstage(t);
-                tc::mma_s_tile_pair<kQHalf / 16, kKHalf / 16>(tmem + team * BN, q_desc,
-                                                               k_desc0 + (uint64_t)(st * (kKStage / 16)), kIdescS);
-                commit_both(B_KEMPTY + st);
-                // the item's last two S (one per lane) are the last reads of
-                // Q: the Q barrier expects two arrivals per item
-                if (t + 2 >= nkt_cur) commit_both(B_QFREE);
-            };
-            // O(team) (+)= P(t) V(t) over keys 64h .. 64h+63 (V(t) landed,
-            // that half of P(t) stored in both CTAs)
-            auto issue_pv_half = [&](int t, int h) {
-                const int st = vstage(t);
-                tc::mma_pv_half_pair<2048 / 16>(tmem + kOCol + team * D, tmem + team * BN + h * 32,
-                                                v_desc0 + (uint64_t)(st * (kVStage / 16) + h * 4 * (2048 / 16)),
-                                                kIdescPV, (t < 2 && h == 0) ? 0u : 1u);
-                if (h == 1) commit_both(B_VEMPTY + st);
-            };
-            for (int i = 0;; i++) {
-                // Take item i alone (the other lanes idle).  The slot is
-                // reported read only after this item's Q barrier has been
-                // waited for: the queue then cannot run two items ahead of
-                // this lane, so neither Q barrier can complete a phase that
-                // this lane has not yet waited for.
-                if (!wait1(B_ITEM_FULL + (i & 1), (unsigned)((i >> 1) & 1))) { failed = true; break; }
-                const ItemInfo it = item_info(p, item_slots[i & 1], rank);
-                if (!it.stop && !it.skip && !wait1(B_GO + (go_count & 1), (unsigned)((go_count >> 1) & 1))) {
-                    failed = true;
-                    break;
-                }
-                tc::mbar_arrive_cluster(bar_own(B_ITEM_EMPTY + (i & 1)));
-                if (it.stop) break;
-                if (!it.skip) {
-                    const int nkt = it.nkt;
-                    nkt_cur = nkt;
-                    if (nkt == 1 && team == 1) {  // one S reads this Q, and it is team 0's
-                        tc::mbar_arrive_remote(bar_own(B_QFREE));
-                        tc::mbar_arrive_remote(bar_other(B_QFREE));
+            if (warp == kSWarp) {
+                // Descriptors of the first 16 columns of Q and of stage 0 of
+                // the K ring; a stage, a half or 16 more columns is a constant
+                // number of 16-byte units on.
+                const uint64_t q_desc = tc::smem_desc_sw128(sbase + kOffQ, 16, 1024);
+                const uint64_t k_desc0 = tc::smem_desc_sw128(sbase + kOffK, 16, 1024);
+                for (int i = 0;; i++) {
+                    // Take item i alone (the other lanes idle).  The slot is
+                    // reported read only after this item's Q barrier has been
+                    // waited for: the queue then cannot run two items ahead
+                    // of this lane, so neither Q barrier can complete a phase
+                    // that this lane has not yet waited for.
+                    if (!wait1(B_ITEM_FULL + (i & 1), (unsigned)((i >> 1) & 1))) { failed = true; break; }
+                    const ItemInfo it = item_info(p, item_slots[i & 1], rank);
+                    if (!it.stop && !it.skip && !wait1(B_GO + (go_count & 1), (unsigned)((go_count >> 1) & 1))) {
+                        failed = true;
+                        break;
                     }
-                    if (team < nkt) {
-                        if (!wait1(B_KFULL + kstage(team), kphase(team))) { failed = true; break; }
+                    tc::mbar_arrive_cluster(bar_own(B_ITEM_EMPTY + (i & 1)));
+                    if (it.stop) break;
+                    for (int t = 0; t < it.nkt && !failed; t++) {
+                        const int g = g0 + t, st = g % kKStages;
+                        // the softmax warps have read S(g-2) out of this buffer
+                        if (g >= 2 && !wait1(B_SFREE + (g & 1), (unsigned)(((g - 2) >> 1) & 1))) { failed = true; break; }
+                        if (!wait1(B_KFULL + st, (unsigned)((g / kKStages) & 1))) { failed = true; break; }
                         tc::fence_after_sync();
-                        issue_s(team);
+                        tc::mma_s_tile_pair<kQHalf / 16, kKHalf / 16>(tmem + (uint32_t)((g & 1) * BN), q_desc,
+                                                                       k_desc0 + (uint64_t)(st * (kKStage / 16)), kIdescS);
+                        commit_both(B_KEMPTY + st);
+                        if (t + 1 == it.nkt) commit_both(B_QFREE);  // the item's last read of Q
+                    }
+                    if (failed) break;
+                    advance(it);
+                }
+            } else {
+                // V is MN-major: the next 8 keys at +1 KB (SBO); this CTA's
+                // 64 columns are one 128-byte swizzle span (LBO unused).
+                const uint64_t v_desc0 = tc::smem_desc_sw128(sbase + kOffV, kVStage, 1024);
+                for (int i = 0;; i++) {
+                    if (!wait1(B_ITEM_FULL + (i & 1), (unsigned)((i >> 1) & 1))) { failed = true; break; }
+                    const ItemInfo it = item_info(p, item_slots[i & 1], rank);
+                    tc::mbar_arrive_cluster(bar_own(B_ITEM_EMPTY + (i & 1)));
+                    if (it.stop) break;
+                    if (it.skip) {
+                        advance(it);
+                        continue;
                     }
                     // The previous item's O has been read by both CTAs before
                     // this item's first PV overwrites it.
                     if (go_count > 0 && !wait1(B_EPI, (unsigned)((go_count - 1) & 1))) { failed = true; break; }
-                    // This team's tiles in order: PV(t) half by half as P(t)
-                    // is stored, then S(t+2) into the same buffer once K(t+2)
-                    // has landed.
-                    const int tb = team ? team_base1 : team_base0;  // the team's tiles before this item
-                    for (int t = team; t < nkt && !failed; t += 2) {
-                        if (!wait1(B_VFULL + vstage(t), vphase(t))) { failed = true; break; }
-                        for (int h = 0; h < 2 && !failed; h++) {
-                            if (!wait1(B_PFULL + 2 * team + h, (unsigned)((tb + (t >> 1)) & 1))) {
-                                failed = true;
-                                break;
-                            }
-                            tc::fence_after_sync();
-                            issue_pv_half(t, h);
+                    for (int t = 0; t < it.nkt && !failed; t++) {
+                        const int g = g0 + t, st = g % kVStages;
+                        if (!wait1(B_VFULL + st, (unsigned)((g / kVStages) & 1))) { failed = true; break; }
+                        // both halves of P(g) stored in both CTAs: either half's
+                        // PV writes every column of O, which the softmax threads
+                        // of both halves may rescale before they store P(g)
+                        if (!wait1(B_PFULL + 2 * (g & 1), (unsigned)((g >> 1) & 1)) ||
+                            !wait1(B_PFULL + 2 * (g & 1) + 1, (unsigned)((g >> 1) & 1))) {
+                            failed = true;
+                            break;
                         }
-                        if (!failed && t + 2 < nkt) {
-                            if (!wait1(B_KFULL + kstage(t + 2), kphase(t + 2))) { failed = true; break; }
-                            tc::fence_after_sync();
-                            issue_s(t + 2);
+                        tc::fence_after_sync();
+                        for (int h = 0; h < 2; h++) {
+                            tc::mma_pv_half_pair<2048 / 16>(
+                                tmem + kOCol, tmem + kPCol + (uint32_t)((g & 1) * 64 + h * 32),
+                                v_desc0 + (uint64_t)(st * (kVStage / 16) + h * 4 * (2048 / 16)), kIdescPV,
+                                (t == 0 && h == 0) ? 0u : 1u);
                         }
+                        commit_both(B_VEMPTY + st);
                     }
                     if (failed) break;
+                    advance(it);
                 }
-                advance(it);
             }
             if (failed) raise_abort();
             // every MMA of this lane has finished, and every earlier commit
@@ -662,7 +656,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // memory is released
             commit_both(B_DONE);
         }
-        if (warp == kMmaWarp && lane == 0) {
+        if (warp == kSWarp && lane == 0) {
             // in both CTAs: both lanes' final commits have arrived here (each
             // after that lane's earlier ones), so no commit of this launch
             // lands after the CTA has left
@@ -676,12 +670,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---------------- softmax teams
-        const int team = warp >> 2, quarter = warp & 3;
+        // ---------------- softmax: warp w holds rows 32 (w % 4) .. +31 of this
+        // CTA (its tensor-memory lanes) and key half w / 4 of every tile, so
+        // each row is shared by two threads, one per half
+        const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t s_col = (uint32_t)team * BN, o_col = kOCol + (uint32_t)team * D;
         const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
+        // Hand a value to the other thread of this row and take its value:
+        // 64-bit {value, tag} words in shared memory, the wait bounded like
+        // every other; one warp-wide outcome.
+        auto exchange = [&](int slot, float v, unsigned tag, float &other) -> bool {
+            volatile unsigned long long *mine = xch + (slot * 2 + half) * BM + row;
+            volatile unsigned long long *theirs = xch + (slot * 2 + (half ^ 1)) * BM + row;
+            *mine = ((unsigned long long)tag << 32) | __float_as_uint(v);
+            unsigned long long x = *theirs;
+            bool ok = true;
+            if ((unsigned)(x >> 32) != tag) {
+                const unsigned long long t0 = tc::globaltimer_ns();
+                for (;;) {
+                    x = *theirs;
+                    if ((unsigned)(x >> 32) == tag) break;
+                    if (*abort_flag || tc::globaltimer_ns() - t0 > p.wait_ns) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            other = __uint_as_float((unsigned)x);
+            const bool all = __all_sync(0xffffffffu, ok);
+            if (!all) {
+                failed = true;
+                if (lane == 0) raise_abort();
+            }
+            return all;
+        };
         for (int i = 0;; i++) {
             ItemInfo it;
             if (!take_item(i, it)) break;
@@ -692,13 +715,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const int nkt = it.nkt;
             // Without TMA, this CTA's Q rows: 128 rows x 16 chunks, 8 copies
-            // per softmax thread.  The previous item's S MMAs are all
-            // complete: this thread has been through that item's epilogue,
-            // which follows both teams' last PV.
+            // per softmax thread.  Every S of the previous item is complete:
+            // this thread has been through that item's epilogue, which
+            // follows its last PV, which follows its last S.
             if (!p.q_tma) {
 #pragma unroll
                 for (int u = 0; u < 8; u++) {
-                    const int e = tid + 2 * kTeamThreads * u;
+                    const int e = tid + kSoftmaxThreads * u;
                     const int r = e >> 4, c = e & 15;
                     const int R = it.row0 + r;
                     const int jr = R / G;
@@ -722,36 +745,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float m_used = -INFINITY, lsum = 0.f;
 
             bool ok = true;
-            for (int t = team; t < nkt; t += 2) {
-                // S(t) done (the S that read its K stage is done); the team's
-                // PV(t-2), issued before it by the same lane, is done too
-                if (!(ok = wait_warp(B_KEMPTY + kstage(t), kphase(t)))) break;
+            for (int t = 0; t < nkt; t++) {
+                const int g = g0 + t;
+                // S(g) done (the S that read its K stage is done)
+                if (!(ok = wait_warp(B_KEMPTY + g % kKStages, (unsigned)((g / kKStages) & 1)))) break;
                 tc::fence_after_sync();
+                // This thread's 64 scores in one load, whose own reduction
+                // gives their maximum; then the buffer is free for S(g+2).
+                float sv[64], mp;
+                tc::tmem_ld64_max(t_lane + (uint32_t)((g & 1) * BN + half * 64), sv, mp);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_remote(bar_even(B_SFREE + (g & 1)));
                 const bool full_tile = t * BN + BN <= it.mask_from;
-                const int lim0 = pos - t * BN;  // keys i <= lim0 of this tile are visible
-                // The row's 128 scores in one load, whose own reduction gives
-                // their maximum; masked tiles take it from the masked values.
-                // P is computed from these registers, and each score register
-                // is free once its P is packed.
-                const bool masked = !full_tile || !row_ok;
-                float sv[BN], mraw;
-                tc::tmem_ld128_max(t_lane + s_col, sv, mraw);
-                if (masked) {
+                const int lim0 = pos - t * BN - half * 64;  // this thread's keys i <= lim0 are visible
+                if (!full_tile || !row_ok) {
 #pragma unroll
-                    for (int i2 = 0; i2 < BN; i2++) sv[i2] = i2 <= lim0 ? sv[i2] : -INFINITY;
-                    float mx[16];
+                    for (int i2 = 0; i2 < 64; i2++) sv[i2] = i2 <= lim0 ? sv[i2] : -INFINITY;
+                    float mx[8];
 #pragma unroll
-                    for (int i2 = 0; i2 < 16; i2++)
-                        mx[i2] = fmaxf(fmaxf(fmaxf(sv[i2], sv[i2 + 16]), fmaxf(sv[i2 + 32], sv[i2 + 48])),
-                                       fmaxf(fmaxf(sv[i2 + 64], sv[i2 + 80]), fmaxf(sv[i2 + 96], sv[i2 + 112])));
-#pragma unroll
-                    for (int i2 = 0; i2 < 8; i2++) mx[i2] = fmaxf(mx[i2], mx[i2 + 8]);
-#pragma unroll
-                    for (int i2 = 0; i2 < 4; i2++) mx[i2] = fmaxf(mx[i2], mx[i2 + 4]);
-                    mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    for (int i2 = 0; i2 < 8; i2++)
+                        mx[i2] = fmaxf(fmaxf(fmaxf(sv[i2], sv[i2 + 8]), fmaxf(sv[i2 + 16], sv[i2 + 24])),
+                                       fmaxf(fmaxf(sv[i2 + 32], sv[i2 + 40]), fmaxf(sv[i2 + 48], sv[i2 + 56])));
+                    mp = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                 }
-                if (!row_ok) mraw = -INFINITY;
-                const float mt = mraw * p.scale_log2;  // scale > 0 commutes with max; -inf stays
+                if (!row_ok) mp = -INFINITY;
+                // the row's maximum over both halves: both threads of the row
+                // take the same decisions from here on
+                float mo;
+                if (!(ok = exchange(g & 1, mp, (unsigned)g + 1u, mo))) break;
+                const float mt = fmaxf(mp, mo) * p.scale_log2;  // scale > 0 commutes with max; -inf stays
                 const bool need = mt > m_used + 8.f;
                 float alpha = 1.f;
                 if (need) {
@@ -759,40 +783,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     lsum *= alpha;
                     m_used = mt;
                 }
-                if (t >= 2 && __any_sync(0xffffffffu, need)) {
-                    // rare: rescale the team's O (16 columns at a time beside
-                    // the scores held in registers)
+                if (t >= 1 && __any_sync(0xffffffffu, need)) {
+                    // rare: rescale this thread's half of the O row once PV(g-1)
+                    // is done (O then holds every earlier tile of the item)
+                    if (!(ok = wait_warp(B_VEMPTY + (g - 1) % kVStages, (unsigned)(((g - 1) / kVStages) & 1))))
+                        break;
+                    tc::fence_after_sync();
 #pragma unroll 1
-                    for (int c = 0; c < D; c += 16) {
+                    for (int c = 0; c < 64; c += 16) {
                         float o[16];
-                        tc::tmem_ld16(t_lane + o_col + c, o);
+                        tc::tmem_ld16(t_lane + kOCol + (uint32_t)(half * 64 + c), o);
 #pragma unroll
                         for (int i2 = 0; i2 < 16; i2++) o[i2] *= alpha;
-                        tc::tmem_st16(t_lane + o_col + c, o);
+                        tc::tmem_st16(t_lane + kOCol + (uint32_t)(half * 64 + c), o);
                     }
                 }
-                // P = 2^(s * scale - m) as bf16 pairs over the first 64 columns;
-                // the scaling and the row sum run on paired fp32 instructions
+                // P = 2^(s * scale - m) as bf16 pairs; the scaling and the row
+                // sum run on paired fp32 instructions
                 const float nbase = m_used == -INFINITY ? 0.f : -m_used;
                 const uint64_t sc2 = tc::f2(p.scale_log2, p.scale_log2), nb2 = tc::f2(nbase, nbase);
                 uint64_t acc2[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
+                float pk[32];
 #pragma unroll
-                for (int c = 0; c < BN; c += 64) {
-                    float pk[32];
-#pragma unroll
-                    for (int i2 = 0; i2 < 32; i2++) {
-                        float x0, x1;
-                        tc::unf2(tc::ffma2(tc::f2(sv[c + 2 * i2], sv[c + 2 * i2 + 1]), sc2, nb2), x0, x1);
-                        const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
-                        acc2[i2 & 1] = tc::fadd2(acc2[i2 & 1], tc::f2(e0, e1));
-                        pk[i2] = __uint_as_float(pkv::pack_bf16(e0, e1));
-                    }
-                    // keys c .. c+63 -> P columns c/2 .. c/2+31, handed to the
-                    // MMA lane once the warp's stores are complete
-                    tc::tmem_st32(t_lane + s_col + c / 2, pk);
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive_remote(bar_even(B_PFULL + 2 * team + c / 64));
+                for (int i2 = 0; i2 < 32; i2++) {
+                    float x0, x1;
+                    tc::unf2(tc::ffma2(tc::f2(sv[2 * i2], sv[2 * i2 + 1]), sc2, nb2), x0, x1);
+                    const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
+                    acc2[i2 & 1] = tc::fadd2(acc2[i2 & 1], tc::f2(e0, e1));
+                    pk[i2] = __uint_as_float(pkv::pack_bf16(e0, e1));
                 }
                 {
                     float a0, a1, b0, b1;
@@ -800,66 +818,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc::unf2(acc2[1], b0, b1);
                     lsum += (a0 + a1) + (b0 + b1);
                 }
+                // P(g)'s buffer was last read by PV(g-2)
+                if (g >= 2) {
+                    if (!(ok = wait_warp(B_VEMPTY + (g - 2) % kVStages, (unsigned)(((g - 2) / kVStages) & 1))))
+                        break;
+                    tc::fence_after_sync();
+                }
+                // keys 64 half .. +63 -> P columns 32 half .. +31 of the buffer,
+                // handed to the PV lane once the warp's stores are complete
+                tc::tmem_st32(t_lane + kPCol + (uint32_t)((g & 1) * 64 + half * 32), pk);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_remote(bar_even(B_PFULL + 2 * (g & 1) + half));
             }
             if (!ok) break;
 
-            // merge the two teams: exchange (m, l) with the other team's thread
-            // of the same row through shared memory (double-buffered by item)
-            const int my_tiles = nkt > team ? (nkt - team + 1) / 2 : 0;
-            if (my_tiles > 0) {  // the team's last PV done (the PV that read its V stage)
-                const int tl = team + 2 * (my_tiles - 1);
-                if (!wait_warp(B_VEMPTY + vstage(tl), vphase(tl))) break;
+            // the item's last PV done; the row sum over both halves
+            {
+                const int gl = g0 + nkt - 1;
+                if (!wait_warp(B_VEMPTY + gl % kVStages, (unsigned)((gl / kVStages) & 1))) break;
                 tc::fence_after_sync();
             }
-            float *rb = red + (go_count & 1) * (2 * 2 * BM);
-            rb[(team * 2 + 0) * BM + row] = m_used;
-            rb[(team * 2 + 1) * BM + row] = lsum;
-            // The fences order this thread's later reads of both teams' O
-            // after the completion the other team observed; without them the
-            // first tcgen05.ld waits microseconds.
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(reinterpret_cast<uint64_t *>(smem + kOffBar) + B_ML + team);
-            if (!wait_warp(B_ML + (team ^ 1), (unsigned)(go_count & 1))) break;
-            tc::fence_after_sync();
-            const float m0 = rb[0 * BM + row], l0 = rb[1 * BM + row];
-            const float m1 = rb[2 * BM + row], l1 = rb[3 * BM + row];
-            const float M = fmaxf(m0, m1);
-            const float f0 = M == -INFINITY ? 0.f : tc::ex2(m0 - M);
-            const float f1 = (M == -INFINITY || nkt < 2) ? 0.f : tc::ex2(m1 - M);
-            const float ltot = l0 * f0 + l1 * f1;
+            float lo;
+            if (!exchange(2, lsum, (unsigned)go_count + 1u, lo)) break;
+            const float ltot = lsum + lo;
             const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
-            const float g0 = f0 * inv, g1 = f1 * inv;
-            // Output: each thread writes its half row (team 0 columns 0..63,
-            // team 1 columns 64..127) straight from registers, 16 bytes at a
-            // time; shared memory stays free for the next item's tiles.
+            // Output: each thread writes its half row (columns 64 half ..
+            // +63) straight from registers; shared memory stays free for the
+            // next item's tiles.
             OutT *orow = static_cast<OutT *>(p.out) +
                          ((size_t)(it.q0 + (row_ok ? jrow : 0)) * p.num_q_heads + it.kvh * G + (R - jrow * G)) * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 2; c += 32) {
-                float a[32], b[32];
-                const uint32_t col = (uint32_t)(team * (D / 2) + c);
+            for (int c = 0; c < 64; c += 32) {
+                float a[32];
+                const uint32_t col = (uint32_t)(half * 64 + c);
                 tc::tmem_ld32(t_lane + kOCol + col, a);
-                if (nkt >= 2) {
-                    tc::tmem_ld32(t_lane + kOCol + D + col, b);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; e++) b[e] = 0.f;
-                }
                 if (row_ok && p.prefix_len) {
                     // shared-prefix mode: the unnormalised state (M, L, O)
                     // goes to partial slot 0 of the decode row (s = jrow)
                     const size_t prow = ((size_t)jrow * p.num_q_heads + it.kvh * G + (R - jrow * G)) * p.part_stride;
                     float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * D + col);
 #pragma unroll
-                    for (int k = 0; k < 8; k++)
-                        po[k] = make_float4(a[4 * k] * f0 + b[4 * k] * f1, a[4 * k + 1] * f0 + b[4 * k + 1] * f1,
-                                            a[4 * k + 2] * f0 + b[4 * k + 2] * f1, a[4 * k + 3] * f0 + b[4 * k + 3] * f1);
-                    if (team == 0 && c == 0) *reinterpret_cast<float2 *>(p.part_ml + prow * 2) = make_float2(M, ltot);
+                    for (int k = 0; k < 8; k++) po[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+                    if (half == 0 && c == 0) *reinterpret_cast<float2 *>(p.part_ml + prow * 2) = make_float2(m_used, ltot);
                 } else if (row_ok) {
                     alignas(16) OutT v[32];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) pkv::store2(v + e, a[e] * g0 + b[e] * g1, a[e + 1] * g0 + b[e + 1] * g1);
+                    for (int e = 0; e < 32; e += 2) pkv::store2(v + e, a[e] * inv, a[e + 1] * inv);
                     if (p.out_v8) {
                         // 32 bytes per store: each fills whole sectors of the row
                         constexpr int kVec = 32 * (int)sizeof(OutT) / 32;
