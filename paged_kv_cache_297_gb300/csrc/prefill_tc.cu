@@ -31,8 +31,8 @@
 //   * 8 softmax warps.  Warp w owns rows 32 (w % 4) .. +31 of its CTA (its
 //     tensor-memory lanes) and keys 64 (w / 4) .. +63 of every tile, so two
 //     threads share each row.  A thread reads its 64 scores in one load,
-//     whose own reduction gives their maximum, releases the S buffer, trades
-//     maxima with the other thread of its row through shared memory, masks,
+//     whose own reduction gives their maximum, releases the S buffer, masks,
+//     trades maxima with the other thread of its row through shared memory,
 //     computes p = 2^(s * scale * log2 e - m) (one paired multiply-add per
 //     two elements, ex2.approx on the special-function unit) and stores its
 //     64 keys of P as bf16 pairs; P(g) goes to the PV lane once all 8 warps
@@ -71,8 +71,10 @@
 //   Q : two 64-column halves of this CTA's 128 rows              (32 KB)
 //   K : six stages x two 64-column halves of this CTA's 64 keys  (96 KB)
 //   V : four stages x 128 keys of this CTA's 64 columns          (64 KB)
-// Waits.  Every wait on an mbarrier or on the other thread of a row is
-// bounded in time (PrefillParams::wait_ns, from %globaltimer).  A wait that
+// Waits.  Every wait on an mbarrier is bounded in time (PrefillParams::
+// wait_ns, from %globaltimer); the two warps that share rows meet at a named
+// barrier once per tile, and a warp that leaves after a failure releases its
+// partner from it.  A wait that
 // runs out makes the whole warp leave its role loop (the decision is taken
 // warp-wide, so no lane is left at a warp barrier) and raises an abort flag
 // in both CTAs, at which the other roles' waits give up too.  A role that
@@ -159,11 +161,12 @@ constexpr int kOffSlots = (kOffBar + kNumBars * 8 + 15) & ~15;  // TMEM address 
 static_assert(kOffSlots % 16 == 0, "item slots are 16-byte vectors");
 constexpr int kOffAbort = kOffSlots + 16 + 2 * 16;
 // Row exchange between the two threads that share a row: [slot][half][row]
-// 64-bit {value, tag}; slots 0 and 1 carry tile maxima, slot 2 row sums.
+// floats; slots 0 and 1 carry tile maxima (by tile parity), 2 and 3 row sums
+// (by item parity).
 constexpr int kOffX = kOffAbort + 16;
-constexpr int kXBytes = 3 * 2 * BM * 8;
+constexpr int kXBytes = 4 * 2 * BM * 4;
 constexpr int kSmemBytes = kOffX + kXBytes;
-static_assert(kOffX % 8 == 0, "exchange words are 8-byte aligned");
+static_assert(kOffX % 4 == 0, "exchange words are 4-byte aligned");
 static_assert(kSmemBytes <= 232448, "more shared memory than a CTA may have");
 static_assert(kSmemBytes > 232448 / 2, "one CTA per SM: the tensor memory is all allocated by one CTA");
 
@@ -205,6 +208,22 @@ __device__ __forceinline__ void count_exit(const PrefillParams &p) {
         atomicExch(p.item_counter, 0ull);
         atomicExch(p.item_counter + 2, 0ull);
     }
+}
+
+// The queue's record of item `item`: (item, first query, queries, length).
+__device__ __forceinline__ int4 item_record(const PrefillParams &p, int item) {
+    int4 v = make_int4(item, 0, 0, 0);
+    if (item < p.num_items && p.prefix_len) {
+        v.y = 0;  // the decode queries, one "position" per sequence
+        v.z = p.max_q_len;
+        v.w = p.prefix_len;
+    } else if (item < p.num_items) {
+        const int s = p.num_seqs - 1 - item / (p.num_kv_heads * p.tiles_per_seq);
+        v.y = p.cu_q_lens[s];
+        v.z = p.cu_q_lens[s + 1] - v.y;
+        v.w = p.context_lens[s];
+    }
+    return v;
 }
 
 // Item (sequence, pair tile, kv head) as published in the shared-memory
@@ -269,7 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffSlots);
     int4 *item_slots = reinterpret_cast<int4 *>(smem + kOffSlots + 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
-    unsigned long long *xch = reinterpret_cast<unsigned long long *>(smem + kOffX);
+    float *xch = reinterpret_cast<float *>(smem + kOffX);
     // shared::cta address of barrier i, and the shared::cluster windows of
     // the even CTA, this CTA and the other CTA
     auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
@@ -279,9 +298,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto bar_own = [&](int i) { return base_own + kOffBar + 8u * (uint32_t)i; };
     auto bar_other = [&](int i) { return base_other + kOffBar + 8u * (uint32_t)i; };
 
-    if (!misaligned) {
-        // exchange tags start at 0; every tag used is at least 1
-        for (int e = tid; e < kXBytes / 8; e += kThreads) xch[e] = 0ull;
+    // While the barriers and tensor memory are set up: the tensor maps into
+    // the TMA unit's cache, the first item's block-table row into L2, and
+    // (queue warp) the first item's record into registers.
+    int4 first_rec = make_int4(0, 0, 0, 0);
+    if (warp >= kLoadWarp0 && lane == 0 && !misaligned) {
+        const int item = (int)(blockIdx.x >> 1);
+        if (warp == kLoadWarp0) {
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+            if (p.q_tma) asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
+            if (even) first_rec = item_record(p, item);
+        } else if (warp == kLoadWarp0 + 2) {
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+        }
+        if (item < p.num_items) {
+            const int s = p.prefix_len ? 0 : p.num_seqs - 1 - item / (p.num_kv_heads * p.tiles_per_seq);
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p.block_tables + (size_t)s * p.max_blocks) : "memory");
+        }
     }
     if (tid == 0 && !misaligned) {
         uint64_t *b = reinterpret_cast<uint64_t *>(smem + kOffBar);
@@ -407,16 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int4 v = make_int4(item, 0, 0, 0);
                 if (i >= 2 && !wait_lane0(B_ITEM_EMPTY + (i & 1), (unsigned)(((i >> 1) - 1) & 1))) break;
                 if (lane == 0) {
-                    if (item < p.num_items && p.prefix_len) {
-                        v.y = 0;                // the decode queries, one "position" per sequence
-                        v.z = p.max_q_len;
-                        v.w = p.prefix_len;
-                    } else if (item < p.num_items) {
-                        const int s = p.num_seqs - 1 - item / (p.num_kv_heads * p.tiles_per_seq);
-                        v.y = p.cu_q_lens[s];
-                        v.z = p.cu_q_lens[s + 1] - v.y;
-                        v.w = p.context_lens[s];
-                    }
+                    v = i == 0 ? first_rec : item_record(p, item);
                     item_slots[i & 1] = v;
                     tc::st_cluster_v4(base_other + kOffSlots + 16 + 16 * (i & 1), v);
                     // release: each slot is visible to its CTA's waiters
@@ -678,32 +702,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
         // Hand a value to the other thread of this row and take its value:
-        // 64-bit {value, tag} words in shared memory, the wait bounded like
-        // every other; one warp-wide outcome.
-        auto exchange = [&](int slot, float v, unsigned tag, float &other) -> bool {
-            volatile unsigned long long *mine = xch + (slot * 2 + half) * BM + row;
-            volatile unsigned long long *theirs = xch + (slot * 2 + (half ^ 1)) * BM + row;
-            *mine = ((unsigned long long)tag << 32) | __float_as_uint(v);
-            unsigned long long x = *theirs;
-            bool ok = true;
-            if ((unsigned)(x >> 32) != tag) {
-                const unsigned long long t0 = tc::globaltimer_ns();
-                for (;;) {
-                    x = *theirs;
-                    if ((unsigned)(x >> 32) == tag) break;
-                    if (*abort_flag || tc::globaltimer_ns() - t0 > p.wait_ns) {
-                        ok = false;
-                        break;
-                    }
-                }
-            }
-            other = __uint_as_float((unsigned)x);
-            const bool all = __all_sync(0xffffffffu, ok);
-            if (!all) {
+        // each writes its word, the two warps holding the same rows (quarter
+        // and quarter + 4) meet at named barrier 1 + quarter, each reads the
+        // other's word.  Both warps pass the same sequence of these barriers
+        // (one per tile, one per item), so a warp that leaves its role after
+        // a failure arrives once at the barrier (pair_release below): its
+        // partner can be held at most at the next one, and checks the abort
+        // flag before every later one.  The words are double-buffered by
+        // slot: a word is rewritten only after the partner has passed the
+        // next barrier, after its read.
+        float *xv = xch;  // [slot][half][row]
+        auto exchange = [&](int slot, float v, float &other) -> bool {
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) {  // one decision for the warp
                 failed = true;
-                if (lane == 0) raise_abort();
+                return false;
             }
-            return all;
+            xv[(slot * 2 + half) * BM + row] = v;
+            asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
+            other = xv[(slot * 2 + (half ^ 1)) * BM + row];
+            return true;
         };
         for (int i = 0;; i++) {
             ItemInfo it;
@@ -771,10 +788,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                 }
                 if (!row_ok) mp = -INFINITY;
+                // P = 2^(s * scale - m) as bf16 pairs over this thread's 64 keys
+                // and their sum, against the reference m_used; the scaling and
+                // the sum run on paired fp32 instructions
+                float pk[32], lt;
+                auto compute_p = [&]() {
+                    const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+                    const uint64_t sc2 = tc::f2(p.scale_log2, p.scale_log2), nb2 = tc::f2(nbase, nbase);
+                    uint64_t acc2[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
+#pragma unroll
+                    for (int i2 = 0; i2 < 32; i2++) {
+                        float x0, x1;
+                        tc::unf2(tc::ffma2(tc::f2(sv[2 * i2], sv[2 * i2 + 1]), sc2, nb2), x0, x1);
+                        const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
+                        acc2[i2 & 1] = tc::fadd2(acc2[i2 & 1], tc::f2(e0, e1));
+                        pk[i2] = __uint_as_float(pkv::pack_bf16(e0, e1));
+                    }
+                    float a0, a1, b0, b1;
+                    tc::unf2(acc2[0], a0, a1);
+                    tc::unf2(acc2[1], b0, b1);
+                    lt = (a0 + a1) + (b0 + b1);
+                };
                 // the row's maximum over both halves: both threads of the row
                 // take the same decisions from here on
                 float mo;
-                if (!(ok = exchange(g & 1, mp, (unsigned)g + 1u, mo))) break;
+                if (!(ok = exchange(g & 1, mp, mo))) break;
                 const float mt = fmaxf(mp, mo) * p.scale_log2;  // scale > 0 commutes with max; -inf stays
                 const bool need = mt > m_used + 8.f;
                 float alpha = 1.f;
@@ -798,26 +836,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tc::tmem_st16(t_lane + kOCol + (uint32_t)(half * 64 + c), o);
                     }
                 }
-                // P = 2^(s * scale - m) as bf16 pairs; the scaling and the row
-                // sum run on paired fp32 instructions
-                const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-                const uint64_t sc2 = tc::f2(p.scale_log2, p.scale_log2), nb2 = tc::f2(nbase, nbase);
-                uint64_t acc2[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
-                float pk[32];
-#pragma unroll
-                for (int i2 = 0; i2 < 32; i2++) {
-                    float x0, x1;
-                    tc::unf2(tc::ffma2(tc::f2(sv[2 * i2], sv[2 * i2 + 1]), sc2, nb2), x0, x1);
-                    const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
-                    acc2[i2 & 1] = tc::fadd2(acc2[i2 & 1], tc::f2(e0, e1));
-                    pk[i2] = __uint_as_float(pkv::pack_bf16(e0, e1));
-                }
-                {
-                    float a0, a1, b0, b1;
-                    tc::unf2(acc2[0], a0, a1);
-                    tc::unf2(acc2[1], b0, b1);
-                    lsum += (a0 + a1) + (b0 + b1);
-                }
+                compute_p();
+                lsum += lt;
                 // P(g)'s buffer was last read by PV(g-2)
                 if (g >= 2) {
                     if (!(ok = wait_warp(B_VEMPTY + (g - 2) % kVStages, (unsigned)(((g - 2) / kVStages) & 1))))
@@ -840,7 +860,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc::fence_after_sync();
             }
             float lo;
-            if (!exchange(2, lsum, (unsigned)go_count + 1u, lo)) break;
+            if (!exchange(2 + (go_count & 1), lsum, lo)) break;
             const float ltot = lsum + lo;
             const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
             // Output: each thread writes its half row (columns 64 half ..
@@ -885,6 +905,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_remote(bar_even(B_EPI));
             advance(it);
+        }
+        if (failed) {
+            // the abort flag (raised by whichever wait failed) is visible to
+            // the partner warp before it is let past the pending barrier
+            *abort_flag = 1;
+            __threadfence_block();
+            asm volatile("bar.arrive %0, 64;\n" ::"r"(1 + quarter) : "memory");
         }
     }
 
