@@ -81,9 +81,11 @@
 // has left issues no further copies or MMAs.  At the end one thread of each
 // CTA waits for both MMA lanes' final commits, which arrive after every
 // earlier one (a separate, fixed bound of one second), the pair meets at a
-// cluster barrier, and if anything failed both CTAs wait 100 us more so that
-// copies already issued land before either CTA's shared memory is released;
-// the CTA records PKV_STATUS_INTERNAL, frees its tensor memory and returns.
+// cluster barrier, and if anything failed (every failure raises the abort
+// flag in both CTAs, so both take the same branch) both CTAs wait 100 us
+// more, so that copies already issued land before either CTA's shared
+// memory is released, and meet again; the CTA records PKV_STATUS_INTERNAL,
+// frees its tensor memory and returns.
 // (A failure stops all further issue, so the only copies that can still be
 // in flight were issued before it; a TMA load or cp.async of a few KB lands
 // within microseconds.  Waiting on their barriers instead is not possible:
@@ -196,12 +198,13 @@ __device__ __forceinline__ int next_item(const PrefillParams &p) {
     return item < (unsigned long long)p.num_items ? (int)item : 0x7fffffff;
 }
 
-// Count this CTA's exit in the second pair of the workspace counter,
-// {launch tag, CTAs done}, installed like the first.  The launch's last CTA
-// clears both tags, so the next launch installs its own pairs even when it
-// carries this launch's tag: a launch replayed from a CUDA graph keeps the
-// parameters, tag included, that it was captured with.  (By then every CTA
-// has made its last fetch from the first pair.)
+// Count this CTA in the second pair of the workspace counter, {launch tag,
+// CTAs done}, installed like the first: the even CTA once its queue has made
+// its last fetch, the odd CTA (which fetches nothing) at once.  The launch's
+// last count clears both tags, so the next launch installs its own pairs
+// even when it carries this launch's tag: a launch replayed from a CUDA
+// graph keeps the parameters, tag included, that it was captured with.  (By
+// then every CTA has made its last fetch from the first pair.)
 __device__ __forceinline__ void count_exit(const PrefillParams &p) {
     const unsigned long long k = pkv::tagged_add(p.item_counter + 2, p.launch_tag);
     if (k == (unsigned long long)gridDim.x - 1) {
@@ -397,12 +400,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
     // Take item i from this CTA's queue (every role reads every item): lane 0
     // waits, the warp reads, lane 0 reports the slot read to the even CTA.
+    // The stop record is the last one: no slot is refilled after it, so it is
+    // not reported read (the cluster-scope release of that report would wait
+    // for the reader's output stores to complete).
     auto take_item = [&](int i, ItemInfo &it) -> bool {
         if (!wait_lane0(B_ITEM_FULL + (i & 1), (unsigned)((i >> 1) & 1))) return false;
         const int4 v = item_slots[i & 1];
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive_cluster(bar_even(B_ITEM_EMPTY + (i & 1)));
         it = item_info(p, v, rank);
+        if (lane == 0 && !it.stop) tc::mbar_arrive_cluster(bar_even(B_ITEM_EMPTY + (i & 1)));
         return true;
     };
 
@@ -418,7 +424,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
 
     if (failed) {
-        // nothing: misaligned shared memory (reported below)
+        // nothing but the exit count: misaligned shared memory (reported below)
+        if (tid == 0) count_exit(p);
     } else if (warp >= kLoadWarp0) {
         // ---------------- loaders: two for K (each 2 of this CTA's 4 blocks
         // of a tile, both 64-column halves) and two for V (each 4 of the 8
@@ -587,6 +594,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 item = __shfl_sync(0xffffffffu, item, 0);
             }
         }
+        // this CTA's fetches are over (the odd CTA makes none)
+        if (runs_queue && lane == 0) count_exit(p);
     } else if (warp == kSWarp || warp == kPVWarp) {
         // ---------------- MMA issue: lane 0 of warp 8 of the even CTA issues
         // every S = Q K^T of the pair, lane 0 of warp 9 every O += P V.  The
@@ -594,6 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // neither orders itself after the other: S(g+2) goes out as soon as
         // the softmax warps have read S(g) into registers, while they still
         // work on it, and PV(g) as soon as they have stored P(g).
+        if (!even && warp == kPVWarp && lane == 0) count_exit(p);  // the odd CTA fetches no item
         if (even && lane == 0) {
             // one commit per CTA of the pair: each CTA's barrier i
             auto commit_both = [&](int i) {
@@ -618,8 +628,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         failed = true;
                         break;
                     }
-                    tc::mbar_arrive_cluster(bar_own(B_ITEM_EMPTY + (i & 1)));
                     if (it.stop) break;
+                    tc::mbar_arrive_cluster(bar_own(B_ITEM_EMPTY + (i & 1)));
                     for (int t = 0; t < it.nkt && !failed; t++) {
                         const int g = g0 + t, st = g % kKStages;
                         // the softmax warps have read S(g-2) out of this buffer
@@ -641,8 +651,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int i = 0;; i++) {
                     if (!wait1(B_ITEM_FULL + (i & 1), (unsigned)((i >> 1) & 1))) { failed = true; break; }
                     const ItemInfo it = item_info(p, item_slots[i & 1], rank);
-                    tc::mbar_arrive_cluster(bar_own(B_ITEM_EMPTY + (i & 1)));
                     if (it.stop) break;
+                    tc::mbar_arrive_cluster(bar_own(B_ITEM_EMPTY + (i & 1)));
                     if (it.skip) {
                         advance(it);
                         continue;
@@ -688,6 +698,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             while (!tc::mbar_try_cluster(bar(B_DONE), 0)) {
                 if (tc::globaltimer_ns() - t0 > kDrainNs) {
                     failed = true;
+                    raise_abort();
                     break;
                 }
             }
@@ -918,20 +929,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     pkv::cp_async_wait<0>();
     tc::fence_before_sync();
     const bool any_failed = __syncthreads_or(failed) != 0;
-    if (any_failed && tid == 0) pkv::flag(p.status, PKV_STATUS_INTERNAL);
+    if (any_failed && tid == 0) {
+        pkv::flag(p.status, PKV_STATUS_INTERNAL);
+        if (!misaligned) raise_abort();  // the pair takes the same branch below
+    }
     tc::cluster_sync();  // both CTAs done with each other's barriers; abort flags final
-    if (*abort_flag || any_failed) {
+    // the same decision in both CTAs: every failure raised the abort flag in
+    // both, and misaligned shared memory is the pair's (same base)
+    if (misaligned || *abort_flag) {
         // copies already issued (by either CTA, counted on the even CTA's
         // barriers) land before either CTA leaves
         const unsigned long long t0 = tc::globaltimer_ns();
         while (tc::globaltimer_ns() - t0 < kGraceNs) {
         }
+        tc::cluster_sync();
     }
-    tc::cluster_sync();
     tc::fence_after_sync();
     if (warp == 0 && !misaligned) tc::tmem_dealloc_pair(tmem, kTmemCols);
-    // every role of the pair has passed its last item fetch
-    if (tid == 0) count_exit(p);
 }
 
 }  // namespace
