@@ -20,6 +20,9 @@
 
 namespace {
 
+// x rounded to the nearest bf16 (ties to even), as a float.
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 using pkv::kBlock;
 using pkv::PrefillParams;
 
@@ -177,10 +180,13 @@ __global__ void __launch_bounds__(kThreads) prefill_bf16_kernel(const PrefillPar
             float sumA = 0.f, sumB = 0.f;
 #pragma unroll
             for (int nt = 0; nt < ST; nt++) {
-                sc[nt][0] = pkv::fast_exp2(sc[nt][0] - baseA);
-                sc[nt][1] = pkv::fast_exp2(sc[nt][1] - baseA);
-                sc[nt][2] = pkv::fast_exp2(sc[nt][2] - baseB);
-                sc[nt][3] = pkv::fast_exp2(sc[nt][3] - baseB);
+                // P rounded to bf16 here, as the PV product takes it, so that
+                // the row sum adds the same values (numerator and denominator
+                // share the rounding)
+                sc[nt][0] = round_bf16(pkv::fast_exp2(sc[nt][0] - baseA));
+                sc[nt][1] = round_bf16(pkv::fast_exp2(sc[nt][1] - baseA));
+                sc[nt][2] = round_bf16(pkv::fast_exp2(sc[nt][2] - baseB));
+                sc[nt][3] = round_bf16(pkv::fast_exp2(sc[nt][3] - baseB));
                 sumA += sc[nt][0] + sc[nt][1];
                 sumB += sc[nt][2] + sc[nt][3];
             }

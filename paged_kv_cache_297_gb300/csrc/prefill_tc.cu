@@ -811,9 +811,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int i2 = 0; i2 < 32; i2++) {
                         float x0, x1;
                         tc::unf2(tc::ffma2(tc::f2(sv[2 * i2], sv[2 * i2 + 1]), sc2, nb2), x0, x1);
-                        const float e0 = tc::ex2(x0), e1 = tc::ex2(x1);
-                        acc2[i2 & 1] = tc::fadd2(acc2[i2 & 1], tc::f2(e0, e1));
-                        pk[i2] = __uint_as_float(pkv::pack_bf16(e0, e1));
+                        const uint32_t w = pkv::pack_bf16(tc::ex2(x0), tc::ex2(x1));
+                        pk[i2] = __uint_as_float(w);
+                        // the row sum adds the bf16 values the PV product
+                        // multiplies, so that numerator and denominator share
+                        // their rounding (a row whose weight sits on one key
+                        // then gets that key's V, not V times 1 +- 2^-9)
+                        acc2[i2 & 1] = tc::fadd2(acc2[i2 & 1],
+                                                 tc::f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
                     }
                     float a0, a1, b0, b1;
                     tc::unf2(acc2[0], a0, a1);

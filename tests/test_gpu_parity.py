@@ -171,6 +171,28 @@ def test_prefill_edges(priors, chunks, hq, hkv, d):
     _check_step(b)
 
 
+@pytest.mark.parametrize("scale,d", [(30.0, 128), (-30.0, 128), (30.0, 64)])
+def test_prefill_late_score_jumps_in_either_key_half(scale, d):
+    # Keys scaled x30 at a few positions of later key tiles, in either 64-key
+    # half of their tile (positions 300, 700, 900: first half; 500, 1100,
+    # 1150: second half): the running maximum of many rows jumps by far more
+    # than 8 (log2 units) mid-sequence.  The reference of both threads of a
+    # row must move, whichever half holds the jump, and O must be rescaled.
+    # The negative scale makes the jumps land on other rows.  A row whose
+    # weight then sits on one key must get that key's V: P enters the PV
+    # product in bf16, and the row sum must add those same values.  d = 64
+    # runs the mma.sync kernel.
+    b = W.custom_prefill("bf16", 32, 8, d, [1000, 0], [200, 300], seed=331)
+    prior, table = 1000, b.prefill_block_tables
+    for pos in (300, 500, 700, 900, 1100, 1150):
+        if pos < prior:
+            blk = int(table[0, pos // 16])
+            b.k_cache[blk, :, pos % 16, :] = (b.k_cache[blk, :, pos % 16, :].float() * scale).to(b.dtype)
+        else:  # sequence 0's new tokens come first in k_new
+            b.k_new[pos - prior] = (b.k_new[pos - prior].float() * scale).to(b.dtype)
+    _check_step(b)
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_prefill_output_only_16_byte_aligned(out_dtype):
     # the epilogue writes 32 bytes per store only to a 32-byte aligned output
