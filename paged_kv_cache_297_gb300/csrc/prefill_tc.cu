@@ -806,24 +806,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 auto compute_p = [&]() {
                     const float nbase = m_used == -INFINITY ? 0.f : -m_used;
                     const uint64_t sc2 = tc::f2(p.scale_log2, p.scale_log2), nb2 = tc::f2(nbase, nbase);
-                    uint64_t acc2[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
+                    // the row sum adds the bf16 values the PV product
+                    // multiplies, so that numerator and denominator share
+                    // their rounding (a row whose weight sits on one key then
+                    // gets that key's V, not V times 1 +- 2^-9): each half of
+                    // a packed pair added to an fp32 sum as it stands
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int i2 = 0; i2 < 32; i2++) {
                         float x0, x1;
                         tc::unf2(tc::ffma2(tc::f2(sv[2 * i2], sv[2 * i2 + 1]), sc2, nb2), x0, x1);
                         const uint32_t w = pkv::pack_bf16(tc::ex2(x0), tc::ex2(x1));
                         pk[i2] = __uint_as_float(w);
-                        // the row sum adds the bf16 values the PV product
-                        // multiplies, so that numerator and denominator share
-                        // their rounding (a row whose weight sits on one key
-                        // then gets that key's V, not V times 1 +- 2^-9)
-                        acc2[i2 & 1] = tc::fadd2(acc2[i2 & 1],
-                                                 tc::f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+                        tc::add_bf16_pair(w, acc[(i2 & 1) * 2], acc[(i2 & 1) * 2 + 1]);
                     }
-                    float a0, a1, b0, b1;
-                    tc::unf2(acc2[0], a0, a1);
-                    tc::unf2(acc2[1], b0, b1);
-                    lt = (a0 + a1) + (b0 + b1);
+                    lt = (acc[0] + acc[1]) + (acc[2] + acc[3]);
                 };
                 // the row's maximum over both halves: both threads of the row
                 // take the same decisions from here on

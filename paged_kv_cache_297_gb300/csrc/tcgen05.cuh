@@ -162,6 +162,14 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// lo += the low bf16 of w, hi += its high bf16 (each converted exactly and
+// added in fp32, rounded to nearest).
+__device__ __forceinline__ void add_bf16_pair(uint32_t w, float &lo, float &hi) {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n add.rn.f32.bf16 %0, l, %0;\n add.rn.f32.bf16 %1, h, %1;\n}\n"
+        : "+f"(lo), "+f"(hi)
+        : "r"(w));
+}
+
 // Paired fp32 arithmetic (sm_100 family): two lanes of a 64-bit register
 // pair in one instruction, each rounded as its scalar counterpart.
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
