@@ -717,7 +717,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // and quarter + 4) meet at named barrier 1 + quarter, each reads the
         // other's word.  Both warps pass the same sequence of these barriers
         // (one per tile, one per item), so a warp that leaves its role after
-        // a failure arrives once at the barrier (pair_release below): its
+        // a failure arrives once at the barrier (at the end of the role): its
         // partner can be held at most at the next one, and checks the abort
         // flag before every later one.  The words are double-buffered by
         // slot: a word is rewritten only after the partner has passed the
@@ -800,8 +800,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (!row_ok) mp = -INFINITY;
                 // P = 2^(s * scale - m) as bf16 pairs over this thread's 64 keys
-                // and their sum, against the reference m_used; the scaling and
-                // the sum run on paired fp32 instructions
+                // and their sum, against the reference m_used; the scaling runs
+                // on paired fp32 multiply-adds
                 float pk[32], lt;
                 auto compute_p = [&]() {
                     const float nbase = m_used == -INFINITY ? 0.f : -m_used;
