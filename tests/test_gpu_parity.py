@@ -193,6 +193,42 @@ def test_prefill_late_score_jumps_in_either_key_half(scale, d):
     _check_step(b)
 
 
+def _random_prefill_case(rng):
+    """One seeded random prefill shape: group size, head_dim, priors and chunk
+    sizes (empty chunks included), output type, and sometimes keys of the
+    first sequence scaled x25 (score jumps in later tiles)."""
+    hkv = rng.choice([1, 2, 4, 8])
+    g = rng.choice([1, 2, 3, 4, 6, 8, 12, 16])
+    d = rng.choice([128, 128, 64])
+    nseq = rng.randint(1, 6)
+    priors = [rng.choice([0, rng.randint(0, 3000), rng.randint(3000, 6000)]) for _ in range(nseq)]
+    chunks = [rng.choice([0, 1, rng.randint(1, 700), rng.randint(700, 1500)]) for _ in range(nseq)]
+    if sum(chunks) == 0:
+        chunks[0] = rng.randint(1, 300)
+    b = W.custom_prefill("bf16", hkv * g, hkv, d, priors, chunks, seed=rng.randint(1, 10 ** 6))
+    jump = rng.choice([None, None, 25.0, -25.0])
+    if jump is not None:
+        L0 = priors[0] + chunks[0]
+        for _ in range(4):
+            pos = rng.randrange(0, max(1, L0))
+            if pos < priors[0]:
+                blk = int(b.prefill_block_tables[0, pos // 16])
+                b.k_cache[blk, :, pos % 16, :] = (b.k_cache[blk, :, pos % 16, :].float() * jump).to(b.dtype)
+            else:
+                b.k_new[pos - priors[0]] = (b.k_new[pos - priors[0]].float() * jump).to(b.dtype)
+    return b, rng.choice([torch.float32, torch.bfloat16])
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_prefill_random_shapes(case):
+    # Seeded random shapes beyond the hand-picked edges: several items per CTA
+    # pair, queries that G does not divide into the 128-row tile, empty
+    # chunks beside long ones, both kernels, both output types.
+    import random
+    b, out_dtype = _random_prefill_case(random.Random(7100 + case))
+    _check_step(b, out_dtype)
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_prefill_output_only_16_byte_aligned(out_dtype):
     # the epilogue writes 32 bytes per store only to a 32-byte aligned output
