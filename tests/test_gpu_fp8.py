@@ -152,6 +152,24 @@ def test_fp8_decode_step_equals_append_then_decode(case):
     assert torch.equal(out_a, out_b)
 
 
+@pytest.mark.parametrize("case", range(6))
+def test_fp8_random_shapes(case):
+    # Seeded random fp8 batches: groups 1-16, lengths 1 token to 20k,
+    # adaptive or fixed partitions, both output types; caches bit-exact.
+    import random
+    rng = random.Random(7400 + case)
+    hkv = rng.choice([1, 2, 4, 8])
+    g = rng.choice([1, 2, 4, 8, 12, 16])
+    S = rng.randint(1, 48)
+    hi = rng.choice([600, 5000, 20000])
+    lens = [rng.choice([1, rng.randint(16, hi), rng.randint(1, 64)]) for _ in range(S)]
+    b = W.fp8_batch(W.custom_batch("bf16", S, hkv * g, hkv, 128, lens, seed=rng.randint(1, 10 ** 6)))
+    ref, out, (kc_o, vc_o), (kc_g, vc_g) = _fp8_step(b, rng.choice([torch.float32, torch.bfloat16]),
+                                                       partition_size=rng.choice([0, 256, 512, 1536]))
+    assert torch.equal(kc_g, kc_o) and torch.equal(vc_g, vc_o)
+    assert_parity(out, ref, torch.bfloat16, "fp8 decode")
+
+
 def test_fp8_rejects_what_it_does_not_support():
     b = W.fp8_batch(W.custom_batch("bf16", 2, 8, 8, 64, [5, 9], seed=2))
     t = to_dev(b)

@@ -193,6 +193,45 @@ def test_prefill_late_score_jumps_in_either_key_half(scale, d):
     _check_step(b)
 
 
+@pytest.mark.parametrize("case", range(8))
+def test_decode_random_shapes(case):
+    # Seeded random decode batches: group sizes 1-16, head_dim 64 and 128,
+    # lengths from 1 token to 20k (outlier rows in some), partitions from 16
+    # tokens to adaptive, both output types.
+    import random
+    rng = random.Random(7200 + case)
+    hkv = rng.choice([1, 2, 4, 8])
+    g = rng.choice([1, 2, 4, 8, 12, 16])
+    d = rng.choice([64, 128])
+    S = rng.randint(1, 48)
+    hi = rng.choice([600, 5000, 20000])
+    lens = [rng.choice([1, rng.randint(16, hi), rng.randint(1, 64)]) for _ in range(S)]
+    b = W.custom_batch("bf16", S, hkv * g, hkv, d, lens, seed=rng.randint(1, 10 ** 6),
+                       outlier_p=rng.choice([0.0, 0.01]), outlier_scale=20.0)
+    _check_step(b, rng.choice([torch.float32, torch.bfloat16]), partition_size=rng.choice([0, 16, 256, 1536]))
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_shared_prefix_random_shapes(case):
+    # Seeded random cascade batches: prefix of 1-40 blocks, suffixes of 1 to
+    # ~1500 tokens, groups 1-12, appended or fused, adaptive or 256/512-token
+    # partitions; caches bit-exact, output within the bf16 bound.
+    import random
+    rng = random.Random(7300 + case)
+    hkv = rng.choice([4, 8])
+    g = rng.choice([1, 2, 4, 8, 12])
+    S, pb = rng.randint(2, 120), rng.randint(1, 40)
+    lo = rng.randint(1, 64)
+    b = W.make_batch("shared_prefix_cow", num_seqs=S, ctx=(lo, lo + rng.randint(0, 1500)), prefix_blocks=pb,
+                     heads=(hkv * g, hkv))
+    kc_o, vc_o, out_o, _ = oracle_step(b)
+    t, out = _cascade_step(b, pb * 16, fused=rng.choice([True, False]), partition=rng.choice([0, 256, 512]))
+    assert pkv.get_status() == 0
+    assert_bits_equal(t["k_cache"], kc_o, "k_cache")
+    assert_bits_equal(t["v_cache"], vc_o, "v_cache")
+    assert_parity(out, out_o, b.dtype, "cascade decode")
+
+
 def _random_prefill_case(rng):
     """One seeded random prefill shape: group size, head_dim, priors and chunk
     sizes (empty chunks included), output type, and sometimes keys of the
